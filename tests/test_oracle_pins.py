@@ -1,0 +1,421 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: the
+codebook the FP4 explainer prints, torch's float8 cast (a library routine),
+an independent arithmetic formulation of round-to-nearest-even, closed forms
+(softmax on a single tile, V = 1), the exactness of the online softmax, and
+invariants of the rank-one smoothing.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+LOG2E_RSQRT_D = math.log2(math.e) / math.sqrt(128)
+
+
+def _read_golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append([float(x) for x in line.split()])
+    return rows
+
+
+# --------------------------------------------------------------------------
+# formats
+# --------------------------------------------------------------------------
+
+def test_e2m1_codebook_matches_page():
+    mags = sorted(r[0] for r in _read_golden("e2m1_codebook.txt"))
+    pos = sorted(orc.e2m1_value(c) for c in range(8))
+    assert pos == mags
+    for c in range(8):
+        v = orc.e2m1_value(c + 8)
+        assert v == -orc.e2m1_value(c) and math.copysign(1.0, v) == -1.0
+    # about 15 distinct values (+0 and -0 coincide), range +-6
+    vals = {orc.e2m1_value(c) for c in range(16)}
+    assert len(vals) == 15 and max(vals) == 6 and min(vals) == -6
+
+
+def test_e2m1_rounding_examples():
+    for x, want in _read_golden("e2m1_rounding_examples.txt"):
+        for sgn in (1.0, -1.0):
+            code = int(orc.e2m1_encode([sgn * x])[0])
+            assert abs(orc.e2m1_value(code)) == want, (x, code)
+            assert (code >> 3) == (1 if sgn < 0 else 0)
+
+
+def _rne_grid_e2m1(a):
+    """Independent formulation: round |a| on the local grid spacing with
+    numpy's half-to-even rint; spacing 0.5 below 2, 1 below 4, 2 above."""
+    a = np.abs(a)
+    h = np.where(a < 2, 0.5, np.where(a < 4, 1.0, 2.0))
+    v = h * np.rint(a / h)
+    return np.minimum(v, 6.0)
+
+
+def test_e2m1_encode_matches_rint_formulation():
+    rng = np.random.default_rng(1)
+    x = np.concatenate([
+        rng.uniform(-8, 8, 200000),
+        np.arange(-700, 701) / 100.0,                    # dense sweep incl. every tie point
+        np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0, 6.5, -0.0, 0.0]),
+    ])
+    codes = orc.e2m1_encode(x)
+    got = np.array([abs(orc.e2m1_value(int(c))) for c in codes])
+    np.testing.assert_array_equal(got, _rne_grid_e2m1(x))
+    np.testing.assert_array_equal(codes >> 3, np.signbit(x).astype(np.uint8))
+
+
+def test_e4m3_table_matches_torch():
+    t = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    ours = np.array([orc.e4m3_value(c) for c in range(256)])
+    nan = np.isnan(t)
+    assert nan.sum() == 2 and np.array_equal(nan, np.isnan(ours))
+    np.testing.assert_array_equal(ours[~nan], t[~nan])
+    assert orc.e4m3_value(0x7E) == 448.0 and orc.e4m3_value(1) == 2.0 ** -9
+
+
+def test_e4m3_encode_matches_torch_cast():
+    rng = np.random.default_rng(2)
+    mags = np.exp2(rng.uniform(-14, math.log2(463.0), 300000))
+    x = (mags * rng.choice([-1.0, 1.0], mags.size)).astype(np.float32).astype(np.float64)
+    vals = np.array([orc.e4m3_value(c) for c in range(0x7F)])
+    mids = (vals[:-1] + vals[1:]) / 2                    # every tie point
+    x = np.concatenate([x, mids, -mids, [0.0, -0.0, 2.0 ** -10, 3 * 2.0 ** -11, 460.0]])
+    x32 = x.astype(np.float32)                           # the encoder is fed fp32 values
+    assert np.array_equal(x32.astype(np.float64), x)     # all of these are fp32-exact
+    ref = torch.from_numpy(x32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(orc.e4m3_encode(x), ref)
+
+
+def test_e4m3_encode_saturates():
+    x = np.array([448.0, 464.0, 470.0, 1e4, 1e30])
+    assert (orc.e4m3_encode(x) == 0x7E).all()
+    assert (orc.e4m3_encode(-x) == 0xFE).all()
+
+
+def test_bf16_round_matches_torch():
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal(100000) * np.exp2(rng.uniform(-20, 20, 100000))).astype(np.float32)
+    x = np.concatenate([x, np.array([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -0.0], np.float32)])
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(orc.bf16_round(x.astype(np.float64)), ref)
+
+
+# --------------------------------------------------------------------------
+# quantizers
+# --------------------------------------------------------------------------
+
+def test_nvfp4_representable_roundtrip():
+    """A tensor built from codes x block scales x s round-trips exactly when
+    each block contains a magnitude-6 element and one block has scale 448."""
+    rng = np.random.default_rng(4)
+    rows, d = 64, 128
+    s = np.float32(2.0 ** -5)                             # amax = 6*448*s = 84
+    e4m3_vals = np.array([orc.e4m3_value(c) for c in range(1, 0x7F)])
+    sb = rng.choice(e4m3_vals[e4m3_vals >= 2 ** -3], (rows, d // 16))
+    sb[0, 0] = 448.0
+    codes = rng.integers(0, 16, (rows, d))
+    codes[:, ::16] = 7                                     # magnitude 6 in every block
+    vals = np.array([orc.e2m1_value(int(c)) for c in range(16)])[codes]
+    x = (vals * np.repeat(sb, 16, axis=1) * float(s)).astype(np.float32)
+    assert np.array_equal(x.astype(np.float64), vals * np.repeat(sb, 16, axis=1) * float(s))
+    amax = np.float32(np.abs(x).max())
+    assert orc.tensor_scale(amax, 2688.0) == s
+    qc, qs = orc.nvfp4_quantize(x, s)
+    np.testing.assert_array_equal(np.array([orc.e4m3_value(int(c)) for c in qs.ravel()]),
+                                  sb.ravel())
+    deq = orc.nvfp4_dequant(qc, qs) * float(s)
+    # codes compare by value (+0 and -0 both decode to 0)
+    np.testing.assert_array_equal(deq, x.astype(np.float64))
+    lo = (qc & 15).astype(np.int64)
+    hi = (qc >> 4).astype(np.int64)
+    interleaved = np.stack([lo, hi], axis=-1).reshape(rows, d)
+    nz = vals != 0
+    np.testing.assert_array_equal(interleaved[nz], codes[nz])   # low nibble = lower index
+
+
+def _nvfp4_error_bound(x, s, qs):
+    sbs = np.repeat(np.array([orc.e4m3_value(int(c)) for c in qs.ravel()]).reshape(qs.shape),
+                    16, axis=1) * float(s)
+    y = np.abs(x.astype(np.float64)) / np.where(sbs > 0, sbs, 1)
+    half = np.where(y < 2, 0.25, np.where(y < 4, 0.5, 1.0))
+    bound = np.maximum(half, y - 6.0) * sbs
+    return np.where(sbs > 0, bound * (1 + 1e-6), np.abs(x))
+
+
+@pytest.mark.parametrize("dist", ["normal", "outliers", "tiny"])
+def test_nvfp4_invariants(dist):
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((512, 128)).astype(np.float32)
+    if dist == "outliers":
+        x[:, 7] *= 20
+        x += rng.standard_normal(128).astype(np.float32) * 1.4
+    if dist == "tiny":
+        x *= 1e-30
+    x = torch.from_numpy(x).to(torch.bfloat16).float().numpy()
+    amax = np.float32(np.abs(x).max())
+    s = orc.tensor_scale(amax, 2688.0)
+    assert s == np.float32(amax / np.float32(2688.0))
+    qc, qs = orc.nvfp4_quantize(x, s)
+    assert qs.max() <= 0x7E                                # block scales never exceed 448
+    r, c = np.unravel_index(np.argmax(np.abs(x)), x.shape)
+    assert qs[r, c // 16] == 0x7E                          # the amax block gets scale 448
+    deq = orc.nvfp4_dequant(qc, qs) * float(s)
+    err = np.abs(deq - x.astype(np.float64))
+    assert (err <= _nvfp4_error_bound(x, s, qs)).all()
+
+
+def test_nvfp4_zero_tensor():
+    x = np.zeros((4, 128), np.float32)
+    s = orc.tensor_scale(0.0, 2688.0)
+    assert s == 1.0
+    qc, qs = orc.nvfp4_quantize(x, s)
+    assert (qc == 0).all() and (qs == 0).all()
+
+
+def test_fp8_v_quantizer():
+    rng = np.random.default_rng(6)
+    v = torch.from_numpy(rng.standard_normal((300, 128)).astype(np.float32) * 3)
+    v = v.to(torch.bfloat16).float().numpy()
+    s = orc.tensor_scale(np.abs(v).max(), 448.0)
+    codes = orc.fp8_quantize(v, s)
+    ref = torch.from_numpy((v / s).astype(np.float32)).to(torch.float8_e4m3fn).view(
+        torch.uint8).numpy()
+    np.testing.assert_array_equal(codes, ref)
+    assert np.abs(orc.fp8_dequant(codes)).max() == 448.0
+
+
+def test_block_means_match_numpy():
+    rng = np.random.default_rng(7)
+    x = torch.from_numpy(rng.standard_normal((4 * 128, 128)).astype(np.float32) * 2 + 0.7)
+    x = x.to(torch.bfloat16).float().numpy()
+    qbar, xp = orc.block_means(x, 128)
+    ref = x.astype(np.float64).reshape(4, 128, 128).mean(axis=1).astype(np.float32)
+    np.testing.assert_array_equal(qbar, ref)
+    np.testing.assert_array_equal(xp, (x.reshape(4, 128, 128) - qbar[:, None, :]).reshape(-1, 128))
+
+
+# --------------------------------------------------------------------------
+# attention
+# --------------------------------------------------------------------------
+
+def _rand_qkv(n, nk=None, seed=0, scale=1.0):
+    rng = np.random.default_rng(seed)
+    nk = n if nk is None else nk
+    q = rng.standard_normal((n, 128)) * scale
+    k = rng.standard_normal((nk, 128)) * scale
+    v = rng.standard_normal((nk, 128))
+    return q, k, v
+
+
+@pytest.mark.parametrize("n,causal", [(16, False), (32, True), (64, False), (300, True),
+                                      (300, False), (257, True)])
+def test_online_softmax_equals_full_softmax(n, causal):
+    """Quantizers off (identity, unrounded P): the tiled online softmax equals
+    the exact softmax (the FlashAttention-2 identity)."""
+    q, k, v = _rand_qkv(n, seed=n, scale=1.5)
+    o1, l1 = orc.attn_online(q, None, k, v, score_scale=LOG2E_RSQRT_D, out_scale=1.0,
+                             causal=causal, round_p=False)
+    o2, l2 = orc.attn_exact(q, k, v, causal=causal)
+    np.testing.assert_allclose(o1, o2, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-11)
+
+
+@pytest.mark.parametrize("chunk,kv_len", [(128, 300), (256, 513), (128, 129), (384, 1000)])
+def test_split_kv_combine_equals_full_softmax(chunk, kv_len):
+    q, k, v = _rand_qkv(4, nk=1024, seed=chunk + kv_len)
+    o1, l1 = orc.attn_online(q, None, k, v, score_scale=LOG2E_RSQRT_D, out_scale=1.0,
+                             causal=False, kv_len=kv_len, chunk=chunk, round_p=False)
+    o2, l2 = orc.attn_exact(q, k, v, causal=False, kv_len=kv_len)
+    np.testing.assert_allclose(o1, o2, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-11)
+
+
+def test_qadd_is_added_to_every_score():
+    """S = (q + qadd).k: one row of qadd shared by all rows equals adding it to q."""
+    q, k, v = _rand_qkv(200, seed=11)
+    u = np.random.default_rng(12).standard_normal(128)
+    qadd = np.tile(u, (200, 1))
+    o1, l1 = orc.attn_online(q, qadd, k, v, score_scale=LOG2E_RSQRT_D, out_scale=1.0,
+                             causal=True, round_p=False)
+    o2, l2 = orc.attn_exact(q + u, k, v, causal=True)
+    np.testing.assert_allclose(o1, o2, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, atol=1e-10)
+
+
+@pytest.mark.parametrize("n", [16, 64, 128])
+def test_single_tile_rounded_p_direct_formula(n):
+    """One KV tile: P8 = E4M3(2^8 2^(t - max t)) (torch's e4m3 cast),
+    O = sum P8 v / sum P8, LSE = ln2 (max t + log2 sum P8 - 8)."""
+    q, k, v = _rand_qkv(n, seed=100 + n, scale=1.3)
+    o1, l1 = orc.attn_online(q, None, k, v, score_scale=LOG2E_RSQRT_D, out_scale=1.0,
+                             causal=False, round_p=True)
+    t = (q @ k.T) * LOG2E_RSQRT_D
+    m = t.max(axis=1, keepdims=True)
+    p = np.exp2(t - m) * 256.0
+    p8 = torch.from_numpy(p).to(torch.float8_e4m3fn).double().numpy()
+    o2 = (p8 @ v) / p8.sum(axis=1, keepdims=True)
+    l2 = math.log(2) * (m[:, 0] + np.log2(p8.sum(axis=1)) - 8)
+    np.testing.assert_allclose(o1, o2, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, atol=1e-12)
+
+
+def test_shared_rounding_rows_sum_to_one():
+    """The running sum adds the same rounded P codes the PV product uses, so
+    V = 1 gives O = 1 exactly for every row, over many tiles and splits."""
+    q, k, _ = _rand_qkv(700, seed=21, scale=2.0)
+    v = np.ones((700, 128))
+    for chunk in (0, 256):
+        o, _ = orc.attn_online(q, None, k, v, score_scale=LOG2E_RSQRT_D, out_scale=1.0,
+                               causal=True, chunk=chunk, round_p=True)
+        np.testing.assert_allclose(o, 1.0, rtol=0, atol=1e-14)
+
+
+def test_one_split_equals_no_split():
+    q, k, v = _rand_qkv(3, nk=900, seed=31)
+    a = orc.attn_online(q, None, k, v, score_scale=0.1, out_scale=1.0, causal=False,
+                        kv_len=777, chunk=0)
+    b = orc.attn_online(q, None, k, v, score_scale=0.1, out_scale=1.0, causal=False,
+                        kv_len=777, chunk=896)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_empty_rows():
+    q, k, v = _rand_qkv(2, nk=10, seed=41)
+    o, l = orc.attn_online(q, None, k, v, score_scale=0.1, out_scale=1.0, causal=False,
+                           kv_len=0, chunk=128)
+    assert (o == 0).all() and np.isneginf(l).all()
+
+
+# --------------------------------------------------------------------------
+# the method end to end (oracle only)
+# --------------------------------------------------------------------------
+
+def _bf16(x):
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(
+        torch.bfloat16).float().numpy()
+
+
+def _rel_l2(a, b):
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
+
+
+def _emulate_vs_exact(Q, K, V, compensate, causal=False):
+    qz = orc.quantize_q_prefill(Q, compensate)
+    kz = orc.quantize_k(K)
+    vz = orc.quantize_v(V)
+    em = orc.prefill_emulate(qz, kz, vz, causal=causal)
+    ex = orc.prefill_exact(Q, K, V, causal=causal)
+    a = np.concatenate([em[h][0] for h in sorted(em)])
+    b = np.concatenate([ex[h][0] for h in sorted(ex)])
+    return a, b, qz
+
+
+def test_zero_mean_blocks_make_compensation_vanish():
+    """Rows paired (x, -x) inside every 128-row block give qbar = 0: the codes
+    of Q are the same with and without the smoothing and O is identical."""
+    rng = np.random.default_rng(51)
+    half = _bf16(rng.standard_normal((1, 128, 1, 128)) * 1.7)
+    Q = np.concatenate([half, -half], axis=1)              # [1, 256, 1, 128]
+    Q = Q[:, np.r_[0:64, 128:192, 64:128, 192:256]]         # each 128-block holds x and -x
+    K = _bf16(rng.standard_normal((1, 256, 1, 128)))
+    V = _bf16(rng.standard_normal((1, 256, 1, 128)))
+    on = orc.quantize_q_prefill(Q, True)
+    off = orc.quantize_q_prefill(Q, False)
+    assert (on["qbar"] == 0).all()
+    assert on["s_q"] == off["s_q"]
+    np.testing.assert_array_equal(on["qc"] & 0x77, off["qc"] & 0x77)   # magnitudes
+    np.testing.assert_array_equal(on["qs"], off["qs"])
+    assert (on["qbs"] == 0).all() and (on["qbc"] & 0x77 == 0).all()
+    kz, vz = orc.quantize_k(K), orc.quantize_v(V)
+    a = orc.prefill_emulate(on, kz, vz, causal=True)[(0, 0)]
+    b = orc.prefill_emulate(off, kz, vz, causal=True)[(0, 0)]
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_compensation_exact_for_representable_block_means():
+    """Every row of a 128-row block equal to a block mean mu_b that NVFP4
+    represents exactly: with the smoothing, Q' = 0 and the rank-one term alone
+    carries mu_b K^T, so O equals the unsmoothed result bit for bit, and all
+    rows of a block agree.  A flipped sign, a dropped term or a wrong
+    row-to-block mapping breaks the equality."""
+    rng = np.random.default_rng(81)
+    s = 2.0 ** -6                                         # amax = 6 * 448 * s = 42
+    e4 = np.array([orc.e4m3_value(c) for c in range(0x30, 0x7F)])
+    mus = []
+    for b in range(3):
+        codes = rng.integers(0, 16, 128)
+        codes[::16] = 7 + 8 * rng.integers(0, 2, 8)       # magnitude 6 in every 16-block
+        sb = rng.choice(e4, 8)
+        sb[0] = 448.0
+        vals = np.array([orc.e2m1_value(int(c)) for c in range(16)])[codes]
+        mus.append(vals * np.repeat(sb, 16) * s)
+    Q = np.repeat(np.stack(mus), 128, axis=0)[None, :, None, :].astype(np.float32)
+    assert np.array_equal(_bf16(Q), Q)
+    K = _bf16(rng.standard_normal((1, 384, 1, 128)))
+    V = _bf16(rng.standard_normal((1, 384, 1, 128)))
+    on = orc.quantize_q_prefill(Q, True)
+    off = orc.quantize_q_prefill(Q, False)
+    assert on["s_q"] == off["s_q"] == np.float32(s)
+    np.testing.assert_array_equal(on["qbar"][0, 0], np.stack(mus).astype(np.float32))
+    assert (on["qc"] & 0x77 == 0).all()                   # Q' = 0
+    assert (on["qbs"][..., 1, :] == 0).all()               # mu_b exact: no residual term
+    kz, vz = orc.quantize_k(K), orc.quantize_v(V)
+    for causal in (False, True):
+        a = orc.prefill_emulate(on, kz, vz, causal=causal)[(0, 0)]
+        b = orc.prefill_emulate(off, kz, vz, causal=causal)[(0, 0)]
+        np.testing.assert_array_equal(a[0], b[0])
+        np.testing.assert_array_equal(a[1], b[1])
+    a = orc.prefill_emulate(on, kz, vz, causal=False)[(0, 0)][0]
+    for blk in range(3):
+        assert (a[blk * 128:(blk + 1) * 128] == a[blk * 128]).all()
+    assert not np.array_equal(a[0], a[128])
+
+
+def test_compensation_reduces_error_with_query_mean():
+    """With a large per-channel offset on Q (the case the rank-one smoothing
+    targets) the mean error over seeds is clearly lower with the two-term
+    compensation; a dropped or sign-flipped rank-one term makes it many times
+    larger instead."""
+    rng = np.random.default_rng(71)
+    e_on, e_off = [], []
+    for _ in range(8):
+        Q = _bf16(rng.standard_normal((1, 256, 1, 128)) + 6.0 * rng.standard_normal(128))
+        K = _bf16(rng.standard_normal((1, 256, 1, 128)))
+        V = _bf16(rng.standard_normal((1, 256, 1, 128)))
+        a_on, ex, _ = _emulate_vs_exact(Q, K, V, True)
+        a_off, _, _ = _emulate_vs_exact(Q, K, V, False)
+        e_on.append(_rel_l2(a_on, ex))
+        e_off.append(_rel_l2(a_off, ex))
+    assert np.mean(e_on) < 0.8 * np.mean(e_off), (e_on, e_off)
+    assert max(e_on) < 0.4
+
+
+def test_decode_emulate_matches_prefill_last_row():
+    """A decode query against keys [0, L) equals the prefill row L-1 of a
+    causal forward with the same codes, when there is one split and no smoothing."""
+    rng = np.random.default_rng(61)
+    L = 384
+    K = _bf16(rng.standard_normal((1, L, 1, 128)))
+    V = _bf16(rng.standard_normal((1, L, 1, 128)))
+    Q = _bf16(rng.standard_normal((1, L, 1, 128)))
+    qz = orc.quantize_q_prefill(Q, False)
+    kz, vz = orc.quantize_k(K), orc.quantize_v(V)
+    pre = orc.prefill_emulate(qz, kz, vz, causal=True, rows=[L - 1])[(0, 0)]
+    dq = dict(qc=qz["qc"][:, :, L - 1], qs=qz["qs"][:, :, L - 1], qbc=None, qbs=None,
+              s_q=qz["s_q"])
+    dec = orc.decode_emulate(dq, kz, vz, np.array([L]), chunk=0)[(0, 0)]
+    np.testing.assert_array_equal(dec[0], pre[0][0])
+    assert dec[1] == pre[1][0]
