@@ -1,0 +1,248 @@
+"""Python binding of ``libmpfa.so`` (the MpFA QK4PV8 attention forward).
+
+Argument marshalling only: this module allocates outputs and workspaces with
+torch on the caller's device, passes raw pointers and the current CUDA stream
+through the C ABI (``include/mpfa.h``) and raises on a non-zero status.  Every
+step of the computation runs in the library's CUDA kernels; there is no
+fallback.  If the library is missing this import fails.
+
+Method: "MpFA: Hardware-Efficient Train-Free QK4V8 FlashAttention Kernels on
+Blackwell GPUs" (abstract) -- NVFP4 Q/K, FP8 P/V, rank-one smoothing
+compensation, split work for decode.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmpfa.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it first "
+        "(python -c 'import __graft_entry__ as g; g.build()' or "
+        "python flashattention_mpfa_quantize_gb300/build.py)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+D = 128
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
+
+
+class MpfaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        name = _lib.mpfa_status_string(status).decode()
+        super().__init__(f"{where}: {name} ({status})")
+        self.status = status
+
+
+class NVFP4(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("tensor_scale", ctypes.c_void_p)]
+
+
+class FP8(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("tensor_scale", ctypes.c_void_p)]
+
+
+class Rank1(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+_lib.mpfa_status_string.restype = ctypes.c_char_p
+_lib.mpfa_status_string.argtypes = [_I]
+_lib.mpfa_quantize_workspace_size.restype = _SZ
+_lib.mpfa_quantize_workspace_size.argtypes = [_I, _I, _I, _I]
+_lib.mpfa_quantize_qkv.restype = _I
+_lib.mpfa_quantize_qkv.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                                   ctypes.POINTER(NVFP4), ctypes.POINTER(Rank1),
+                                   ctypes.POINTER(NVFP4), ctypes.POINTER(FP8), _P, _SZ, _P]
+_lib.mpfa_prefill.restype = _I
+_lib.mpfa_prefill.argtypes = [ctypes.POINTER(NVFP4), ctypes.POINTER(Rank1),
+                              ctypes.POINTER(NVFP4), ctypes.POINTER(FP8), _I, _I, _I, _I, _I,
+                              _I, _I, _I, _P, _P, _P]
+_lib.mpfa_decode_workspace_size.restype = _SZ
+_lib.mpfa_decode_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I]
+_lib.mpfa_decode.restype = _I
+_lib.mpfa_decode.argtypes = [_P, ctypes.POINTER(NVFP4), ctypes.POINTER(FP8), _P, _I, _I, _I, _I,
+                             _I, _I, _I, _I, _P, _P, ctypes.POINTER(NVFP4),
+                             ctypes.POINTER(Rank1), ctypes.POINTER(_I), _P, _SZ, _P]
+_lib.mpfa_get_error.restype = _I
+_lib.mpfa_get_error.argtypes = [_P]
+
+lib = _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(status, where):
+    if status != OK:
+        raise MpfaError(status, where)
+
+
+def get_error(device=None) -> int:
+    """Synchronize the current stream and return (and clear) the device status."""
+    return _lib.mpfa_get_error(_stream(device))
+
+
+# --------------------------------------------------------------------------
+# quantization
+# --------------------------------------------------------------------------
+
+def alloc_nvfp4(rows_shape, device):
+    """codes [..., 64] u8, tiled scales (rows*8 bytes) u8, tensor scale f32[1]."""
+    rows = 1
+    for s in rows_shape:
+        rows *= s
+    return dict(codes=torch.empty(*rows_shape, 64, dtype=torch.uint8, device=device),
+                scales=torch.empty(rows * 8, dtype=torch.uint8, device=device),
+                scale=torch.empty(1, dtype=torch.float32, device=device))
+
+
+def quantize_qkv(q=None, k=None, v=None, *, compensate=True, T=2, workspace=None):
+    """Quantize bf16 q [B,Nq,Hq,128], k / v [B,Nk,Hkv,128] (any may be None).
+
+    Returns a dict with ``q`` (codes [B,Hq,Nq,64], scales, scale), ``qbar``
+    (codes [B,Hq,Nq/128,T,64], scales [B,Hq,Nq/128,T,8]) when compensating,
+    ``k`` (codes [B,Hkv,Nk,64], scales, scale), ``v`` (codes [B,Hkv,Nk,128],
+    scale), plus the shape fields."""
+    ref = next(t for t in (q, k, v) if t is not None)
+    dev = ref.device
+    B = ref.shape[0]
+    Nq, Hq = (q.shape[1], q.shape[2]) if q is not None else (0, 0)
+    src_kv = k if k is not None else v
+    Nk, Hkv = (src_kv.shape[1], src_kv.shape[2]) if src_kv is not None else (0, 0)
+    comp = bool(compensate) and q is not None
+    for t in (q, k, v):
+        if t is not None:
+            assert t.dtype == torch.bfloat16 and t.is_contiguous() and t.shape[-1] == D
+    out = dict(B=B, Nq=Nq, Nk=Nk, Hq=Hq, Hkv=Hkv, compensate=comp, T=T if comp else 0)
+    qs = ks = vs = None
+    rb = None
+    if q is not None:
+        out["q"] = alloc_nvfp4((B, Hq, Nq), dev)
+        qs = NVFP4(out["q"]["codes"].data_ptr(), out["q"]["scales"].data_ptr(),
+                   out["q"]["scale"].data_ptr())
+        if comp:
+            out["qbar"] = dict(
+                codes=torch.empty(B, Hq, Nq // 128, T, 64, dtype=torch.uint8, device=dev),
+                scales=torch.empty(B, Hq, Nq // 128, T, 8, dtype=torch.uint8, device=dev))
+            rb = Rank1(out["qbar"]["codes"].data_ptr(), out["qbar"]["scales"].data_ptr())
+    if k is not None:
+        out["k"] = alloc_nvfp4((B, Hkv, Nk), dev)
+        ks = NVFP4(out["k"]["codes"].data_ptr(), out["k"]["scales"].data_ptr(),
+                   out["k"]["scale"].data_ptr())
+    if v is not None:
+        out["v"] = dict(codes=torch.empty(B, Hkv, Nk, 128, dtype=torch.uint8, device=dev),
+                        scale=torch.empty(1, dtype=torch.float32, device=dev))
+        vs = FP8(out["v"]["codes"].data_ptr(), out["v"]["scale"].data_ptr())
+    ws_bytes = _lib.mpfa_quantize_workspace_size(B, Nq, Hq, int(comp))
+    if workspace is None or workspace.numel() < ws_bytes:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    st = _lib.mpfa_quantize_qkv(
+        _ptr(q), _ptr(k), _ptr(v), B, Nq, Nk, Hq, Hkv, D, int(comp), int(T),
+        ctypes.byref(qs) if qs is not None else None, ctypes.byref(rb) if rb is not None else None,
+        ctypes.byref(ks) if ks is not None else None, ctypes.byref(vs) if vs is not None else None,
+        _ptr(workspace), workspace.numel(), _stream(dev))
+    _check(st, "mpfa_quantize_qkv")
+    out["_workspace"] = workspace
+    return out
+
+
+# --------------------------------------------------------------------------
+# prefill / decode
+# --------------------------------------------------------------------------
+
+def _nvfp4(d):
+    return NVFP4(d["codes"].data_ptr(), d["scales"].data_ptr(), d["scale"].data_ptr())
+
+
+def prefill(qz, *, causal, out=None, lse=None, want_lse=True):
+    """Attention forward on the output of quantize_qkv (q, k and v given).
+    Returns (o bf16 [B,N,Hq,128], lse f32 [B,Hq,N] or None)."""
+    B, N, Hq, Hkv = qz["B"], qz["Nq"], qz["Hq"], qz["Hkv"]
+    assert qz["Nk"] == N, "prefill takes N_q == N_k"
+    dev = qz["q"]["codes"].device
+    if out is None:
+        out = torch.empty(B, N, Hq, D, dtype=torch.bfloat16, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty(B, Hq, N, dtype=torch.float32, device=dev)
+    qs, ks = _nvfp4(qz["q"]), _nvfp4(qz["k"])
+    vs = FP8(qz["v"]["codes"].data_ptr(), qz["v"]["scale"].data_ptr())
+    comp = qz["compensate"]
+    rb = Rank1(qz["qbar"]["codes"].data_ptr(), qz["qbar"]["scales"].data_ptr()) if comp else None
+    st = _lib.mpfa_prefill(ctypes.byref(qs), ctypes.byref(rb) if rb is not None else None,
+                           ctypes.byref(ks), ctypes.byref(vs), B, N, Hq, Hkv, D, int(bool(causal)),
+                           int(comp), int(qz["T"]), _ptr(out), _ptr(lse), _stream(dev))
+    _check(st, "mpfa_prefill")
+    return out, lse
+
+
+def decode_workspace_bytes(B, Hq, Hkv, Lmax, kv_chunk=0) -> int:
+    return int(_lib.mpfa_decode_workspace_size(B, Hq, Hkv, D, Lmax, kv_chunk))
+
+
+def decode(q, cache, seqlens, *, compensate=True, T=2, kv_chunk=0, out=None, lse=None,
+           want_lse=True, return_query_codes=False, workspace=None):
+    """One decode step: q bf16 [B,Hq,128] against a cache from quantize_qkv
+    (k and v given, q None), seqlens int32 [B] on the device.
+    Returns dict(o, lse, chunk[, q, qbar])."""
+    B, Hq, _ = q.shape
+    Hkv, Lmax = cache["Hkv"], cache["Nk"]
+    dev = q.device
+    assert q.dtype == torch.bfloat16 and q.is_contiguous()
+    assert seqlens.dtype == torch.int32 and seqlens.device == dev
+    if out is None:
+        out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+    ws_bytes = decode_workspace_bytes(B, Hq, Hkv, Lmax, kv_chunk)
+    if workspace is None or workspace.numel() < ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ks = _nvfp4(cache["k"])
+    vs = FP8(cache["v"]["codes"].data_ptr(), cache["v"]["scale"].data_ptr())
+    res = dict(o=out, lse=lse)
+    qq = rb = None
+    if return_query_codes:
+        res["q"] = dict(codes=torch.empty(B, Hq, 64, dtype=torch.uint8, device=dev),
+                        scales=torch.empty(B, Hq, 8, dtype=torch.uint8, device=dev),
+                        scale=torch.empty(1, dtype=torch.float32, device=dev))
+        qq = _nvfp4(res["q"])
+        if compensate:
+            res["qbar"] = dict(codes=torch.empty(B, Hkv, T, 64, dtype=torch.uint8, device=dev),
+                               scales=torch.empty(B, Hkv, T, 8, dtype=torch.uint8, device=dev))
+            rb = Rank1(res["qbar"]["codes"].data_ptr(), res["qbar"]["scales"].data_ptr())
+    used = ctypes.c_int(0)
+    st = _lib.mpfa_decode(_ptr(q), ctypes.byref(ks), ctypes.byref(vs), _ptr(seqlens), B, Hq, Hkv,
+                          D, Lmax, int(bool(compensate)), int(T), int(kv_chunk), _ptr(out),
+                          _ptr(lse), ctypes.byref(qq) if qq is not None else None,
+                          ctypes.byref(rb) if rb is not None else None, ctypes.byref(used),
+                          _ptr(workspace), workspace.numel(), _stream(dev))
+    _check(st, "mpfa_decode")
+    res["chunk"] = used.value
+    res["_workspace"] = workspace
+    return res
+
+
+# --------------------------------------------------------------------------
+# layout utility (inspection only; not on the compute path)
+# --------------------------------------------------------------------------
+
+def untile_scales(tiled: torch.Tensor, rows: int) -> torch.Tensor:
+    """Tiled block scales (rows*8 bytes) -> row-major [rows, 8]."""
+    r = torch.arange(rows, device=tiled.device).view(-1, 1)
+    j = torch.arange(8, device=tiled.device).view(1, -1)
+    off = (r // 128) * 1024 + (j // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (j % 4)
+    return tiled.view(-1)[off.view(-1)].view(rows, 8)

@@ -1,0 +1,255 @@
+// api.cu -- the C ABI declared in include/mpfa.h: argument validation, the
+// device status word, workspace carving and kernel launches.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "mpfa.h"
+
+namespace {
+
+// Device status word: kernels record MPFA_ERR_TIMEOUT here when a bounded
+// on-chip wait expires.  One word per device (static storage, not an
+// allocation); its address is looked up once per device.
+__device__ int g_status;
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices] = {nullptr};
+
+int* status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
+
+mpfa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MPFA_OK : MPFA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* mpfa_status_string(mpfa_status s) {
+  switch (s) {
+    case MPFA_OK: return "MPFA_OK";
+    case MPFA_ERR_INVALID_ARG: return "MPFA_ERR_INVALID_ARG";
+    case MPFA_ERR_UNSUPPORTED: return "MPFA_ERR_UNSUPPORTED";
+    case MPFA_ERR_CUDA: return "MPFA_ERR_CUDA";
+    case MPFA_ERR_TIMEOUT: return "MPFA_ERR_TIMEOUT";
+  }
+  return "MPFA_ERR_UNKNOWN";
+}
+
+size_t mpfa_quantize_workspace_size(int B, int Nq, int Hq, int compensate) {
+  if (B < 0 || Nq < 0 || Hq < 0) return 0;
+  return mpfa::quant_workspace_bytes(B, Nq, Hq, compensate);
+}
+
+mpfa_status mpfa_quantize_qkv(const void* q_bf16, const void* k_bf16, const void* v_bf16, int B,
+                              int Nq, int Nk, int Hq, int Hkv, int d, int compensate, int T,
+                              mpfa_nvfp4* q_out, mpfa_rank1* qbar_out, mpfa_nvfp4* k_out,
+                              mpfa_fp8* v_out, void* workspace, size_t ws_bytes,
+                              mpfa_stream_t stream) {
+  if (d != 128) return MPFA_ERR_UNSUPPORTED;
+  if (B <= 0) return MPFA_ERR_INVALID_ARG;
+  if (!q_bf16 && !k_bf16 && !v_bf16) return MPFA_ERR_INVALID_ARG;
+  mpfa::QuantArgs a = {};
+  a.B = B;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.compensate = q_bf16 ? (compensate != 0) : 0;
+  a.T = T;
+  if (q_bf16) {
+    if (Nq <= 0 || Nq % 128 || Hq <= 0 || !ok_ptr(q_bf16) || !q_out || !ok_ptr(q_out->codes) ||
+        !ok_ptr(q_out->scales) || !q_out->tensor_scale)
+      return MPFA_ERR_INVALID_ARG;
+    if (a.compensate) {
+      if (T != 1 && T != 2) return MPFA_ERR_UNSUPPORTED;
+      if (!qbar_out || !ok_ptr(qbar_out->codes) || !qbar_out->scales)
+        return MPFA_ERR_INVALID_ARG;
+    }
+    a.q = q_bf16;
+    a.qc = q_out->codes;
+    a.qs = q_out->scales;
+    a.s_q = q_out->tensor_scale;
+    if (a.compensate) {
+      a.qbc = qbar_out->codes;
+      a.qbs = qbar_out->scales;
+    }
+  } else if (q_out) {
+    return MPFA_ERR_INVALID_ARG;
+  }
+  if (k_bf16) {
+    if (Nk <= 0 || Nk % 128 || Hkv <= 0 || !ok_ptr(k_bf16) || !k_out ||
+        !ok_ptr(k_out->codes) || !ok_ptr(k_out->scales) || !k_out->tensor_scale)
+      return MPFA_ERR_INVALID_ARG;
+    a.k = k_bf16;
+    a.kc = k_out->codes;
+    a.ks = k_out->scales;
+    a.s_k = k_out->tensor_scale;
+  } else if (k_out) {
+    return MPFA_ERR_INVALID_ARG;
+  }
+  if (v_bf16) {
+    if (Nk <= 0 || Nk % 128 || Hkv <= 0 || !ok_ptr(v_bf16) || !v_out ||
+        !ok_ptr(v_out->codes) || !v_out->tensor_scale)
+      return MPFA_ERR_INVALID_ARG;
+    a.v = v_bf16;
+    a.vc = v_out->codes;
+    a.s_v = v_out->tensor_scale;
+  } else if (v_out) {
+    return MPFA_ERR_INVALID_ARG;
+  }
+  if (!ok_ptr(workspace) ||
+      ws_bytes < mpfa::quant_workspace_bytes(B, q_bf16 ? Nq : 0, Hq, a.compensate))
+    return MPFA_ERR_INVALID_ARG;
+  a.amax = static_cast<unsigned*>(workspace);
+  a.qbar = a.compensate ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 256)
+                        : nullptr;
+  a.err = status_ptr();
+  if (!a.err) return MPFA_ERR_CUDA;
+  return from_cuda(mpfa::launch_quantize(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mpfa_status mpfa_prefill(const mpfa_nvfp4* q, const mpfa_rank1* qbar, const mpfa_nvfp4* k,
+                         const mpfa_fp8* v, int B, int N, int Hq, int Hkv, int d, int causal,
+                         int compensate, int T, void* o_bf16, float* lse,
+                         mpfa_stream_t stream) {
+  if (d != 128) return MPFA_ERR_UNSUPPORTED;
+  if (compensate && T != 1 && T != 2) return MPFA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || B <= 0 || N <= 0 || N % 128 || Hq <= 0 || Hkv <= 0 || Hq % Hkv)
+    return MPFA_ERR_INVALID_ARG;
+  if (!ok_ptr(q->codes) || !ok_ptr(q->scales) || !q->tensor_scale || !ok_ptr(k->codes) ||
+      !ok_ptr(k->scales) || !k->tensor_scale || !ok_ptr(v->codes) || !v->tensor_scale ||
+      !ok_ptr(o_bf16))
+    return MPFA_ERR_INVALID_ARG;
+  if (compensate && (!qbar || !ok_ptr(qbar->codes) || !qbar->scales))
+    return MPFA_ERR_INVALID_ARG;
+  if ((uint64_t)B * Hq * N >= (1ull << 31) || (uint64_t)B * Hkv * N >= (1ull << 31))
+    return MPFA_ERR_INVALID_ARG;
+  mpfa::PrefillArgs a = {};
+  a.qc = q->codes;
+  a.qs = q->scales;
+  a.s_q = q->tensor_scale;
+  a.qbc = compensate ? qbar->codes : nullptr;
+  a.qbs = compensate ? qbar->scales : nullptr;
+  a.kc = k->codes;
+  a.ks = k->scales;
+  a.s_k = k->tensor_scale;
+  a.vc = v->codes;
+  a.s_v = v->tensor_scale;
+  a.B = B;
+  a.N = N;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.causal = causal != 0;
+  a.compensate = compensate != 0;
+  a.T = compensate ? T : 0;
+  a.o = o_bf16;
+  a.lse = lse;
+  a.err = status_ptr();
+  if (!a.err) return MPFA_ERR_CUDA;
+  return from_cuda(mpfa::launch_prefill(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t mpfa_decode_workspace_size(int B, int Hq, int Hkv, int d, int Lmax, int kv_chunk) {
+  if (d != 128 || B <= 0 || Hq <= 0 || Hkv <= 0 || Lmax <= 0) return 0;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int chunk = kv_chunk > 0 ? kv_chunk : mpfa::decode_default_chunk(B, Hkv, Lmax, sms);
+  int nsplit = (Lmax + chunk - 1) / chunk;
+  return mpfa::decode_workspace_bytes(B, Hq, Hkv, nsplit);
+}
+
+mpfa_status mpfa_decode(const void* q_bf16, const mpfa_nvfp4* k_cache, const mpfa_fp8* v_cache,
+                        const int32_t* seqlens, int B, int Hq, int Hkv, int d, int Lmax,
+                        int compensate, int T, int kv_chunk, void* o_bf16, float* lse,
+                        mpfa_nvfp4* q_quant_out, mpfa_rank1* qbar_quant_out, int* used_chunk,
+                        void* workspace, size_t ws_bytes, mpfa_stream_t stream) {
+  if (d != 128) return MPFA_ERR_UNSUPPORTED;
+  if (compensate && T != 1 && T != 2) return MPFA_ERR_UNSUPPORTED;
+  if (!ok_ptr(q_bf16) || !k_cache || !v_cache || !seqlens || B <= 0 || Hq <= 0 || Hkv <= 0 ||
+      Hq % Hkv || Lmax <= 0 || Lmax % 128 || kv_chunk < 0 || kv_chunk % 128 || !ok_ptr(o_bf16))
+    return MPFA_ERR_INVALID_ARG;
+  if (!ok_ptr(k_cache->codes) || !ok_ptr(k_cache->scales) || !k_cache->tensor_scale ||
+      !ok_ptr(v_cache->codes) || !v_cache->tensor_scale)
+    return MPFA_ERR_INVALID_ARG;
+  if (Hq / Hkv > 16) return MPFA_ERR_UNSUPPORTED;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int chunk = kv_chunk > 0 ? kv_chunk : mpfa::decode_default_chunk(B, Hkv, Lmax, sms);
+  const int nsplit = (Lmax + chunk - 1) / chunk;
+  const size_t need = mpfa::decode_workspace_bytes(B, Hq, Hkv, nsplit);
+  if (!ok_ptr(workspace) || ws_bytes < need) return MPFA_ERR_INVALID_ARG;
+  mpfa::DecodeArgs a = {};
+  a.q = q_bf16;
+  a.kc = k_cache->codes;
+  a.ks = k_cache->scales;
+  a.s_k = k_cache->tensor_scale;
+  a.vc = v_cache->codes;
+  a.s_v = v_cache->tensor_scale;
+  a.seqlens = seqlens;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Lmax = Lmax;
+  a.compensate = compensate != 0;
+  a.T = compensate ? T : 0;
+  a.chunk = chunk;
+  a.nsplit = nsplit;
+  a.o = o_bf16;
+  a.lse = lse;
+  // workspace carve: [amax 256 B][s_q 256 B][qc][qs][qbc][qbs][qbar][part_o][part_lse]
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  auto take = [&](size_t bytes) {
+    uint8_t* p = w;
+    w += (bytes + 255) & ~size_t(255);
+    return p;
+  };
+  a.amax = reinterpret_cast<unsigned*>(take(256));
+  float* s_q_ws = reinterpret_cast<float*>(take(256));
+  uint8_t* qc_ws = take((size_t)B * Hq * 64);
+  uint8_t* qs_ws = take((size_t)B * Hq * 8);
+  uint8_t* qbc_ws = take((size_t)B * Hkv * 2 * 64);
+  uint8_t* qbs_ws = take((size_t)B * Hkv * 2 * 8);
+  a.qbar = reinterpret_cast<float*>(take((size_t)B * Hkv * 128 * sizeof(float)));
+  a.part_o = reinterpret_cast<float*>(take((size_t)B * Hq * nsplit * 128 * sizeof(float)));
+  a.part_lse = reinterpret_cast<float*>(take((size_t)B * Hq * nsplit * sizeof(float)));
+  const bool qout = q_quant_out && q_quant_out->codes && q_quant_out->scales &&
+                    q_quant_out->tensor_scale;
+  a.qc = qout ? q_quant_out->codes : qc_ws;
+  a.qs = qout ? q_quant_out->scales : qs_ws;
+  a.s_q = qout ? q_quant_out->tensor_scale : s_q_ws;
+  const bool bout = qbar_quant_out && qbar_quant_out->codes && qbar_quant_out->scales;
+  a.qbc = bout ? qbar_quant_out->codes : qbc_ws;
+  a.qbs = bout ? qbar_quant_out->scales : qbs_ws;
+  a.err = status_ptr();
+  if (!a.err) return MPFA_ERR_CUDA;
+  if (used_chunk) *used_chunk = chunk;
+  return from_cuda(mpfa::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mpfa_status mpfa_get_error(mpfa_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return MPFA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return MPFA_ERR_CUDA;
+  if (v != 0) {
+    int zero = 0;
+    cudaMemcpyToSymbol(g_status, &zero, sizeof(int));
+  }
+  return v == 0 ? MPFA_OK : static_cast<mpfa_status>(v);
+}
+
+}  // extern "C"

@@ -1,0 +1,76 @@
+// internal.h -- host-side launch interfaces between the C ABI (api.cu) and
+// the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mpfa {
+
+// Everything the two quantization passes need.  Pointers are device pointers;
+// a tensor whose input pointer is null is skipped.
+struct QuantArgs {
+  const void* q;  // bf16 [B][Nq][Hq][128]
+  const void* k;  // bf16 [B][Nk][Hkv][128]
+  const void* v;  // bf16 [B][Nk][Hkv][128]
+  int B, Nq, Nk, Hq, Hkv;
+  int compensate, T;
+  uint8_t *qc, *qs;
+  float* s_q;
+  uint8_t *qbc, *qbs;
+  uint8_t *kc, *ks;
+  float* s_k;
+  uint8_t* vc;
+  float* s_v;
+  // workspace
+  unsigned* amax;  // [3] fp32 bit patterns of amax(Q or Q'/qbar), amax(K), amax(V)
+  float* qbar;     // [B][Hq][Nq/128][128] fp32 block means (compensate only)
+  int* err;
+};
+
+size_t quant_workspace_bytes(int B, int Nq, int Hq, int compensate);
+cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream);
+
+struct PrefillArgs {
+  const uint8_t *qc, *qs;
+  const float* s_q;
+  const uint8_t *qbc, *qbs;  // rank-one terms (null when compensate == 0)
+  const uint8_t *kc, *ks;
+  const float* s_k;
+  const uint8_t* vc;
+  const float* s_v;
+  int B, N, Hq, Hkv, causal, compensate, T;
+  void* o;     // bf16 [B][N][Hq][128]
+  float* lse;  // [B][Hq][N] or null
+  int* err;
+};
+
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+
+struct DecodeArgs {
+  const void* q;  // bf16 [B][Hq][128]
+  const uint8_t *kc, *ks;
+  const float* s_k;
+  const uint8_t* vc;
+  const float* s_v;
+  const int32_t* seqlens;
+  int B, Hq, Hkv, Lmax, compensate, T, chunk, nsplit;
+  void* o;     // bf16 [B][Hq][128]
+  float* lse;  // [B][Hq] or null
+  // quantized query (workspace or caller buffers)
+  uint8_t *qc, *qs;    // [B][Hq][64], [B][Hq][8]
+  uint8_t *qbc, *qbs;  // [B][Hkv][T][64], [B][Hkv][T][8]
+  float* s_q;
+  unsigned* amax;      // [1]
+  float* qbar;         // [B][Hkv][128]
+  float* part_o;       // [B][Hq][nsplit][128]
+  float* part_lse;     // [B][Hq][nsplit]
+  int* err;
+};
+
+int decode_default_chunk(int B, int Hkv, int Lmax, int num_sms);
+size_t decode_workspace_bytes(int B, int Hq, int Hkv, int nsplit);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+}  // namespace mpfa

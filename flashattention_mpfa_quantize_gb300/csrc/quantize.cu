@@ -1,0 +1,374 @@
+// quantize.cu -- online NVFP4 quantization of Q and K and FP8 quantization
+// of V (MpFA abstract: "NVFP4 for QK and FP8 for PV"; formats per the FP4
+// section of the "FlashAttention压到4位" explainer: E2M1 codes, one E4M3 scale
+// per 16 elements, one FP32 tensor scale), plus the rank-one smoothing of Q
+// (block mean removed before quantization, the mean kept as T NVFP4 terms).
+//
+// Two HBM-streaming passes, because every tensor scale depends on the whole
+// tensor:
+//   stats_kernel : amax of K and V; for Q either amax(Q) or, with the
+//                  smoothing, the fp32 block means qbar (exact fp64 sums) and
+//                  max(amax(Q - qbar), amax(qbar)).
+//   quant_kernel : codes and scales of Q (or Q - qbar), of the qbar terms,
+//                  of K and of V; the tensor scales.
+// All rounding follows the rules in include/mpfa.h, one IEEE operation at a
+// time (no fast math), so the codes are bit-identical to a plain
+// sequential implementation of those rules.
+#include <cuda_runtime.h>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace mpfa {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr float kNvfp4Max = 2688.0f;  // 6 * 448
+constexpr float kFp8Max = 448.0f;
+
+__device__ __forceinline__ float tensor_scale(unsigned amax_bits, float qmax) {
+  float a = __uint_as_float(amax_bits);
+  return a == 0.0f ? 1.0f : __fdiv_rn(a, qmax);
+}
+
+// Byte offset of block scale (row, j) in the 128-row tile layout.
+__device__ __forceinline__ size_t sf_offset(size_t row, int j) {
+  return (row >> 7) * 1024 + (size_t)(j >> 2) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4;
+}
+
+__device__ __forceinline__ void load16_bf16(const __nv_bfloat16* p, float (&x)[16]) {
+  const uint4* p4 = reinterpret_cast<const uint4*>(p);
+  uint4 a = __ldg(p4), b = __ldg(p4 + 1);
+  uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    x[2 * i] = bf16_lo(w[i]);
+    x[2 * i + 1] = bf16_hi(w[i]);
+  }
+}
+
+// E2M1 value of a 4-bit code.
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+  uint32_t e = (c >> 1) & 3u, m = c & 1u;
+  float mag = (e == 0) ? 0.5f * (float)m : (1.0f + 0.5f * (float)m) * (float)(1u << (e - 1));
+  return (c & 8u) ? -mag : mag;
+}
+
+// One NVFP4 block of 16 fp32 values with tensor scale s: eight code bytes
+// (element 2i in the low nibble of byte i) and the E4M3 block scale.
+__device__ __forceinline__ void nvfp4_block(const float (&x)[16], float s, uint2& codes,
+                                            uint32_t& sb) {
+  float bamax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) bamax = fmaxf(bamax, fabsf(x[i]));
+  float t = __fdiv_rn(bamax, __fmul_rn(6.0f, s));
+  sb = e4m3_pos(t);
+  uint32_t w0 = 0, w1 = 0;
+  if (sb != 0) {
+    float denom = __fmul_rn(e4m3_value(sb), s);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint32_t byte = e2m1x2(__fdiv_rn(x[2 * i], denom), __fdiv_rn(x[2 * i + 1], denom));
+      if (i < 4)
+        w0 |= byte << (8 * i);
+      else
+        w1 |= byte << (8 * (i - 4));
+    }
+  }
+  codes = make_uint2(w0, w1);
+}
+
+// Warp-cooperative write of one scale byte per lane (lane = 8 * row_in_warp
+// + block j) into the tile layout: lanes with j % 4 == 0 store 4 bytes.
+__device__ __forceinline__ void store_scales_tiled(uint8_t* scales, size_t row, int j,
+                                                   uint32_t sb) {
+  uint32_t b1 = __shfl_down_sync(0xffffffffu, sb, 1);
+  uint32_t b2 = __shfl_down_sync(0xffffffffu, sb, 2);
+  uint32_t b3 = __shfl_down_sync(0xffffffffu, sb, 3);
+  if ((j & 3) == 0) {
+    uint32_t word = sb | (b1 << 8) | (b2 << 16) | (b3 << 24);
+    *reinterpret_cast<uint32_t*>(scales + sf_offset(row, j)) = word;
+  }
+}
+
+__device__ __forceinline__ unsigned block_max_u32(unsigned v, unsigned* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < kThreads / 32; ++i) v = max(v, red[i]);
+  }
+  __syncthreads();
+  return v;
+}
+
+// amax of a bf16 tensor of n8 groups of 8 values (grid-stride over `nblk`
+// CTAs starting at block b0) -> atomicMax on the fp32 bit pattern.
+__device__ void amax_bf16(const uint4* p, size_t n8, int b0, int nblk, unsigned* out,
+                          unsigned* red) {
+  unsigned m = 0;
+  for (size_t i = (size_t)(blockIdx.x - b0) * kThreads + threadIdx.x; i < n8;
+       i += (size_t)nblk * kThreads) {
+    uint4 a = __ldg(p + i);
+    m = __vmaxu2(m, a.x & 0x7FFF7FFFu);
+    m = __vmaxu2(m, a.y & 0x7FFF7FFFu);
+    m = __vmaxu2(m, a.z & 0x7FFF7FFFu);
+    m = __vmaxu2(m, a.w & 0x7FFF7FFFu);
+  }
+  m = max(m & 0xFFFFu, m >> 16);
+  m = block_max_u32(m, red);
+  if (threadIdx.x == 0 && m) atomicMax(out, m << 16);
+}
+
+// ---------------------------------------------------------------------------
+// pass 1
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kThreads) stats_kernel(QuantArgs a, int nq_blocks,
+                                                         int nk_blocks, int nv_blocks) {
+  __shared__ unsigned red[kThreads / 32];
+  __shared__ double part[8][128];
+  __shared__ float qb[128];
+  int bid = blockIdx.x;
+  if (bid < nq_blocks) {
+    if (!a.compensate) {
+      size_t n8 = (size_t)a.B * a.Nq * a.Hq * 16;
+      amax_bf16(reinterpret_cast<const uint4*>(a.q), n8, 0, nq_blocks, &a.amax[0], red);
+      return;
+    }
+    // One CTA per (b, h, 128-row block): exact column sums in fp64.
+    int nblk = a.Nq / 128;
+    int blk = bid % nblk;
+    int bh = bid / nblk;
+    int h = bh % a.Hq, b = bh / a.Hq;
+    int cg = threadIdx.x & 15, rg = threadIdx.x >> 4;
+    const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(a.q);
+    double acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int i = 0; i < 16; ++i) {
+      size_t n = (size_t)blk * 128 + rg + 8 * i;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+          q + (((size_t)b * a.Nq + n) * a.Hq + h) * 128 + 8 * cg));
+      uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        acc[2 * t] += (double)bf16_lo(w[t]);
+        acc[2 * t + 1] += (double)bf16_hi(w[t]);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t) part[rg][8 * cg + t] = acc[t];
+    __syncthreads();
+    {
+      int c = threadIdx.x;
+      double s = 0.0;
+#pragma unroll
+      for (int g = 0; g < 8; ++g) s += part[g][c];
+      float mean = (float)(s * (1.0 / 128.0));
+      qb[c] = mean;
+      a.qbar[((size_t)bh * nblk + blk) * 128 + c] = mean;
+    }
+    __syncthreads();
+    unsigned m = __float_as_uint(fabsf(qb[threadIdx.x]));
+    for (int i = 0; i < 16; ++i) {
+      size_t n = (size_t)blk * 128 + rg + 8 * i;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+          q + (((size_t)b * a.Nq + n) * a.Hq + h) * 128 + 8 * cg));
+      uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        float d0 = __fsub_rn(bf16_lo(w[t]), qb[8 * cg + 2 * t]);
+        float d1 = __fsub_rn(bf16_hi(w[t]), qb[8 * cg + 2 * t + 1]);
+        m = max(m, __float_as_uint(fabsf(d0)));
+        m = max(m, __float_as_uint(fabsf(d1)));
+      }
+    }
+    m = block_max_u32(m, red);
+    if (threadIdx.x == 0 && m) atomicMax(&a.amax[0], m);
+    return;
+  }
+  bid -= nq_blocks;
+  if (bid < nk_blocks) {
+    size_t n8 = (size_t)a.B * a.Nk * a.Hkv * 16;
+    amax_bf16(reinterpret_cast<const uint4*>(a.k), n8, nq_blocks, nk_blocks, &a.amax[1], red);
+    return;
+  }
+  size_t n8 = (size_t)a.B * a.Nk * a.Hkv * 16;
+  amax_bf16(reinterpret_cast<const uint4*>(a.v), n8, nq_blocks + nk_blocks, nv_blocks,
+            &a.amax[2], red);
+}
+
+// ---------------------------------------------------------------------------
+// pass 2
+// ---------------------------------------------------------------------------
+
+// blockIdx.y: 0 = Q rows, 1 = qbar terms, 2 = K rows, 3 = V elements.
+__global__ void __launch_bounds__(kThreads) quant_kernel(QuantArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int warps_total = gridDim.x * (kThreads / 32);
+  const int gwarp = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+  const int j = lane & 7;     // 16-element block within the row
+  const int ri = lane >> 3;   // row within the warp's 4 rows
+  const int part = blockIdx.y;
+
+  if (part == 0 && a.q) {
+    float s = tensor_scale(a.amax[0], kNvfp4Max);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.s_q = s;
+    const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(a.q);
+    size_t rows = (size_t)a.B * a.Hq * a.Nq;
+    int nblk = a.Nq / 128;
+    for (size_t u = gwarp; u < rows / 4; u += warps_total) {
+      size_t r = u * 4 + ri;  // output row (b, h, n)
+      size_t n = r % a.Nq;
+      size_t bh = r / a.Nq;
+      size_t h = bh % a.Hq, b = bh / a.Hq;
+      float x[16];
+      load16_bf16(q + ((b * a.Nq + n) * a.Hq + h) * 128 + 16 * j, x);
+      if (a.compensate) {
+        const float4* qb =
+            reinterpret_cast<const float4*>(a.qbar + (bh * nblk + n / 128) * 128 + 16 * j);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          float4 m = qb[t];
+          x[4 * t] = __fsub_rn(x[4 * t], m.x);
+          x[4 * t + 1] = __fsub_rn(x[4 * t + 1], m.y);
+          x[4 * t + 2] = __fsub_rn(x[4 * t + 2], m.z);
+          x[4 * t + 3] = __fsub_rn(x[4 * t + 3], m.w);
+        }
+      }
+      uint2 codes;
+      uint32_t sb;
+      nvfp4_block(x, s, codes, sb);
+      *reinterpret_cast<uint2*>(a.qc + r * 64 + 8 * j) = codes;
+      store_scales_tiled(a.qs, r, j, sb);
+    }
+    return;
+  }
+  if (part == 1 && a.q && a.compensate) {
+    float s = tensor_scale(a.amax[0], kNvfp4Max);
+    size_t rows = (size_t)a.B * a.Hq * (a.Nq / 128);
+    for (size_t u = gwarp; u < rows / 4 + 1; u += warps_total) {
+      size_t r = u * 4 + ri;
+      if (r >= rows) continue;
+      float x[16];
+      const float4* src = reinterpret_cast<const float4*>(a.qbar + r * 128 + 16 * j);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        float4 m = src[t];
+        x[4 * t] = m.x;
+        x[4 * t + 1] = m.y;
+        x[4 * t + 2] = m.z;
+        x[4 * t + 3] = m.w;
+      }
+      for (int term = 0; term < a.T; ++term) {
+        uint2 codes;
+        uint32_t sb;
+        nvfp4_block(x, s, codes, sb);
+        *reinterpret_cast<uint2*>(a.qbc + (r * a.T + term) * 64 + 8 * j) = codes;
+        a.qbs[(r * a.T + term) * 8 + j] = (uint8_t)sb;
+        // residual for the next term: x - fp32(fp32(code * sb) * s)
+        float sbv = e4m3_value(sb);
+        uint32_t w[2] = {codes.x, codes.y};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          uint32_t c = (w[i >> 3] >> (4 * (i & 7))) & 15u;
+          float deq = __fmul_rn(__fmul_rn(e2m1_value(c), sbv), s);
+          x[i] = __fsub_rn(x[i], deq);
+        }
+      }
+    }
+    return;
+  }
+  if (part == 2 && a.k) {
+    float s = tensor_scale(a.amax[1], kNvfp4Max);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.s_k = s;
+    const __nv_bfloat16* k = reinterpret_cast<const __nv_bfloat16*>(a.k);
+    size_t rows = (size_t)a.B * a.Hkv * a.Nk;
+    for (size_t u = gwarp; u < rows / 4; u += warps_total) {
+      size_t r = u * 4 + ri;
+      size_t n = r % a.Nk;
+      size_t bh = r / a.Nk;
+      size_t h = bh % a.Hkv, b = bh / a.Hkv;
+      float x[16];
+      load16_bf16(k + ((b * a.Nk + n) * a.Hkv + h) * 128 + 16 * j, x);
+      uint2 codes;
+      uint32_t sb;
+      nvfp4_block(x, s, codes, sb);
+      *reinterpret_cast<uint2*>(a.kc + r * 64 + 8 * j) = codes;
+      store_scales_tiled(a.ks, r, j, sb);
+    }
+    return;
+  }
+  if (part == 3 && a.v) {
+    float s = tensor_scale(a.amax[2], kFp8Max);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.s_v = s;
+    const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(a.v);
+    size_t units = (size_t)a.B * a.Hkv * a.Nk * 8;  // 16-element units
+    size_t tid = (size_t)blockIdx.x * kThreads + threadIdx.x;
+    for (size_t e = tid; e < units; e += (size_t)gridDim.x * kThreads) {
+      size_t r = e >> 3;  // output row (b, h, n)
+      int jj = (int)(e & 7);
+      size_t n = r % a.Nk;
+      size_t bh = r / a.Nk;
+      size_t h = bh % a.Hkv, b = bh / a.Hkv;
+      float x[16];
+      load16_bf16(v + ((b * a.Nk + n) * a.Hkv + h) * 128 + 16 * jj, x);
+      uint32_t w[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        w[t] = e4m3_signed(__fdiv_rn(x[4 * t], s)) |
+               (e4m3_signed(__fdiv_rn(x[4 * t + 1], s)) << 8) |
+               (e4m3_signed(__fdiv_rn(x[4 * t + 2], s)) << 16) |
+               (e4m3_signed(__fdiv_rn(x[4 * t + 3], s)) << 24);
+      }
+      *reinterpret_cast<uint4*>(a.vc + r * 128 + 16 * jj) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+}  // namespace
+
+size_t quant_workspace_bytes(int B, int Nq, int Hq, int compensate) {
+  size_t bytes = 256;  // amax words
+  if (compensate) bytes += (size_t)B * Hq * (Nq / 128) * 128 * sizeof(float);
+  return bytes;
+}
+
+cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(a.amax, 0, 3 * sizeof(unsigned), stream);
+  if (e != cudaSuccess) return e;
+  const int sms = num_sms();
+  auto amax_blocks = [&](size_t elems) {
+    size_t need = (elems / 8 + kThreads - 1) / kThreads;
+    size_t cap = (size_t)sms * 8;
+    return (int)(need < cap ? (need ? need : 1) : cap);
+  };
+  int nq = 0, nk = 0, nv = 0;
+  if (a.q)
+    nq = a.compensate ? a.B * a.Hq * (a.Nq / 128)
+                      : amax_blocks((size_t)a.B * a.Nq * a.Hq * 128);
+  if (a.k) nk = amax_blocks((size_t)a.B * a.Nk * a.Hkv * 128);
+  if (a.v) nv = amax_blocks((size_t)a.B * a.Nk * a.Hkv * 128);
+  if (nq + nk + nv > 0) {
+    stats_kernel<<<nq + nk + nv, kThreads, 0, stream>>>(a, nq, nk, nv);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid(sms * 8, 4);
+  quant_kernel<<<grid, kThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace mpfa

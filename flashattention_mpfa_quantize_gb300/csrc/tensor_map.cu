@@ -1,0 +1,37 @@
+// tensor_map.cu -- host-side TMA descriptors (cuTensorMapEncodeTiled, looked
+// up through the runtime so the library needs no link against libcuda).
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+namespace mpfa {
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2-D byte matrix [rows][inner_bytes] (row pitch = inner_bytes), loaded in
+// boxes of box_rows full rows with the given shared-memory swizzle.
+bool make_map_2d_u8(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows,
+                    uint32_t box_rows, CUtensorMapSwizzle sw) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner_bytes, rows};
+  cuuint64_t strides[1] = {inner_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)inner_bytes, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace mpfa

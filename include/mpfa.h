@@ -1,0 +1,176 @@
+/*
+ * mpfa.h -- C ABI of the MpFA QK4PV8 attention forward for GB300 (sm_103a).
+ *
+ * The method: "MpFA: Hardware-Efficient Train-Free QK4V8 FlashAttention
+ * Kernels on Blackwell GPUs" (abstract).  Q and K are quantized online to
+ * NVFP4 and multiplied on block-scaled FP4 tensor cores; P and V are FP8
+ * E4M3 and multiplied on FP8 tensor cores ("QK4PV8"); a rank-one smoothing
+ * compensation is one extra tensor-core MMA into the score accumulator; work
+ * is partitioned differently for prefill and decode.  The number formats
+ * follow the FP4 section ("FP4 只有约 15 个可表示的数") of the
+ * "FlashAttention压到4位" explainer: E2M1 codes, one E4M3 scale per 16
+ * elements, one FP32 tensor scale.  The online softmax follows that
+ * explainer's FlashAttention-2 section ("注意力慢在哪儿").
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - All pointers are DEVICE pointers unless stated otherwise, owned by the
+ *    caller, 16-byte aligned.  The library allocates and frees nothing and
+ *    never synchronizes (except mpfa_get_error).  Work is enqueued on the
+ *    caller's stream and runs asynchronously.
+ *  - Head dimension d must be 128.  Query head h uses KV head h / (Hq/Hkv).
+ *  - Host-checkable faults return synchronously with nothing enqueued:
+ *    MPFA_ERR_INVALID_ARG (null pointer, misaligned pointer, bad size,
+ *    workspace too small) or MPFA_ERR_UNSUPPORTED (d != 128, a T other than
+ *    1 or 2).  A failed launch returns MPFA_ERR_CUDA.  A kernel whose bounded
+ *    wait on an on-chip barrier expires records MPFA_ERR_TIMEOUT in a device
+ *    status word and exits; mpfa_get_error reports it.
+ *
+ * Quantized layouts
+ * -----------------
+ *  NVFP4 codes: [rows][64] bytes, two E2M1 codes per byte, the element with
+ *  the lower index in the low nibble.  E2M1 code: bit 3 sign, bits 2..1
+ *  exponent, bit 0 mantissa (magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6).
+ *
+ *  NVFP4 block scales ("128-row tile layout"): rows*8 bytes of unsigned E4M3
+ *  (OCP E4M3, bias 7, max 448).  The scale of row r, block j (elements
+ *  16j..16j+15, j = 0..7) is at byte
+ *      (r / 128) * 1024 + (j / 4) * 512 + (r % 32) * 16 + ((r / 32) % 4) * 4 + (j % 4)
+ *  so that each 128-row tile holds, per 64-element chunk, one 512-byte block
+ *  the tensor core reads directly.  Row counts must be multiples of 128.
+ *
+ *  FP8 codes: OCP E4M3 bytes.
+ *
+ *  Quantization rules (FP32 arithmetic, each operation rounded once):
+ *      s   = amax / 2688 (1 if amax == 0)        tensor scale, NVFP4
+ *      sb  = E4M3_rne_sat(bamax / (6 * s))        per 16 elements
+ *      code= E2M1_rne_sat(x / (sb * s)), all zero if sb == 0; sign bit = sign of x
+ *      V:   s_v = amax / 448, code = E4M3_rne_sat(v / s_v)
+ *  Rank-one smoothing (compensate != 0): per query block (128 rows of one
+ *  (b, h) in prefill; the Hq/Hkv query heads of one KV head in decode)
+ *      qbar = fp32 mean of the block's rows, Q' = Q - qbar,
+ *      s_q from max(amax(Q'), amax(qbar)), codes of Q' and T NVFP4 terms of
+ *      qbar (term 1 of qbar, term 2 of the fp32 residual qbar - deq(term 1)),
+ *      all sharing s_q.  The score is s_q s_k (Q'K^T + 1 * (sum_t term_t) K^T).
+ */
+#ifndef MPFA_H
+#define MPFA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the CUDA runtime's stream handle). */
+typedef struct CUstream_st *mpfa_stream_t;
+
+typedef enum {
+    MPFA_OK = 0,
+    MPFA_ERR_INVALID_ARG = 1,
+    MPFA_ERR_UNSUPPORTED = 2,
+    MPFA_ERR_CUDA = 3,
+    MPFA_ERR_TIMEOUT = 4
+} mpfa_status;
+
+/* NVFP4 tensor: codes [rows][64], scales in the 128-row tile layout,
+ * tensor_scale points at one device float. */
+typedef struct {
+    uint8_t *codes;
+    uint8_t *scales;
+    float *tensor_scale;
+} mpfa_nvfp4;
+
+/* FP8 E4M3 tensor with one device float tensor scale. */
+typedef struct {
+    uint8_t *codes;
+    float *tensor_scale;
+} mpfa_fp8;
+
+/* Rank-one smoothing terms: codes [nblocks][T][64], scales [nblocks][T][8]
+ * (row-major E4M3), sharing the query tensor scale. */
+typedef struct {
+    uint8_t *codes;
+    uint8_t *scales;
+} mpfa_rank1;
+
+/* Human-readable name of a status. */
+const char *mpfa_status_string(mpfa_status s);
+
+/* Bytes of device workspace mpfa_quantize_qkv needs (amax words and the
+ * fp32 block means of Q when compensate != 0). */
+size_t mpfa_quantize_workspace_size(int B, int Nq, int Hq, int compensate);
+
+/*
+ * Online quantization of one attention layer's inputs (MpFA abstract:
+ * "NVFP4 for QK and FP8 for PV"; formats per the FP4 explainer section).
+ *
+ *   q_bf16 [B][Nq][Hq][d], k_bf16 / v_bf16 [B][Nk][Hkv][d]  bf16, device.
+ *   Any of q/k/v may be NULL to skip it (its output must then be NULL too);
+ *   e.g. q = NULL builds a decode KV cache.
+ *   q_out:  codes [B][Hq][Nq][64], scales tiled over the B*Hq*Nq rows.
+ *   qbar_out (compensate != 0): codes [B][Hq][Nq/128][T][64], scales [..][T][8].
+ *   k_out:  codes [B][Hkv][Nk][64], scales tiled over B*Hkv*Nk rows.
+ *   v_out:  codes [B][Hkv][Nk][128].
+ *   Nq, Nk multiples of 128 (when the tensor is given), T in {1, 2}.
+ *   Tensor scales are computed over each whole tensor argument.
+ *   workspace: device buffer of at least mpfa_quantize_workspace_size bytes.
+ */
+mpfa_status mpfa_quantize_qkv(const void *q_bf16, const void *k_bf16, const void *v_bf16,
+                              int B, int Nq, int Nk, int Hq, int Hkv, int d, int compensate,
+                              int T, mpfa_nvfp4 *q_out, mpfa_rank1 *qbar_out, mpfa_nvfp4 *k_out,
+                              mpfa_fp8 *v_out, void *workspace, size_t ws_bytes,
+                              mpfa_stream_t stream);
+
+/*
+ * Prefill forward (MpFA abstract; FlashAttention-2 tiling and online softmax
+ * per the explainer): O = softmax(s_q s_k S / sqrt(d)) V with S from the
+ * block-scaled FP4 product plus the rank-one term, P stored as E4M3(2^8 p),
+ * KV tiles of 128 keys in ascending order, N_q = N_k = N (causal: key j
+ * visible to query i iff j <= i).
+ *   q/k/v from mpfa_quantize_qkv; qbar NULL iff compensate == 0.
+ *   o_bf16 [B][N][Hq][d]; lse [B][Hq][N] natural-log sum-exp of the scaled
+ *   logits (may be NULL).  N multiple of 128, Hq % Hkv == 0.
+ */
+mpfa_status mpfa_prefill(const mpfa_nvfp4 *q, const mpfa_rank1 *qbar, const mpfa_nvfp4 *k,
+                         const mpfa_fp8 *v, int B, int N, int Hq, int Hkv, int d, int causal,
+                         int compensate, int T, void *o_bf16, float *lse, mpfa_stream_t stream);
+
+/* Bytes of device workspace mpfa_decode needs for kv_chunk (0 = the chunk
+ * the library would choose). */
+size_t mpfa_decode_workspace_size(int B, int Hq, int Hkv, int d, int Lmax, int kv_chunk);
+
+/*
+ * Split-KV decode (MpFA abstract: "adaptive parallel partitioning across
+ * prefill and decode"): one new query token per sequence against a
+ * quantized KV cache.
+ *   q_bf16 [B][Hq][d]; k_cache codes [B][Hkv][Lmax][64] + tiled scales,
+ *   v_cache codes [B][Hkv][Lmax][128]; seqlens int32 [B] (device) with
+ *   0 <= seqlens[b] <= Lmax.  Lmax multiple of 128.
+ *   The query is quantized inside the call (rank-one block = the Hq/Hkv
+ *   heads of one KV head).  Keys [s*C, min(L, (s+1)*C)) form split s
+ *   (C = kv_chunk, a multiple of 128; 0 = chosen by the library, returned in
+ *   *used_chunk, a host int).  Splits combine by their LSE.
+ *   o_bf16 [B][Hq][d]; lse [B][Hq] or NULL.  A sequence of length 0 gets
+ *   O = 0 and LSE = -inf.
+ *   q_quant_out (optional, may be NULL): codes [B][Hq][64], scales
+ *   [B][Hq][8] row-major, tensor scale; qbar_quant_out (optional):
+ *   codes [B][Hkv][T][64], scales [B][Hkv][T][8].
+ */
+mpfa_status mpfa_decode(const void *q_bf16, const mpfa_nvfp4 *k_cache, const mpfa_fp8 *v_cache,
+                        const int32_t *seqlens, int B, int Hq, int Hkv, int d, int Lmax,
+                        int compensate, int T, int kv_chunk, void *o_bf16, float *lse,
+                        mpfa_nvfp4 *q_quant_out, mpfa_rank1 *qbar_quant_out, int *used_chunk,
+                        void *workspace, size_t ws_bytes, mpfa_stream_t stream);
+
+/* Synchronizes the stream, then returns and clears the device status word
+ * (MPFA_ERR_TIMEOUT after an expired on-chip wait), or MPFA_ERR_CUDA if the
+ * stream reports a CUDA error. */
+mpfa_status mpfa_get_error(mpfa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MPFA_H */

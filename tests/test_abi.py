@@ -1,0 +1,64 @@
+"""The C-ABI library builds, loads and exports every symbol include/mpfa.h
+declares (no compute calls: these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mpfa.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mpfa_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    path = __graft_entry__._builder().build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_entry_points():
+    names = _declared()
+    for n in ("mpfa_quantize_qkv", "mpfa_prefill", "mpfa_decode", "mpfa_get_error",
+              "mpfa_status_string", "mpfa_quantize_workspace_size",
+              "mpfa_decode_workspace_size"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in _declared():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    lib.mpfa_status_string.restype = ctypes.c_char_p
+    assert lib.mpfa_status_string(0) == b"MPFA_OK"
+    assert lib.mpfa_status_string(4) == b"MPFA_ERR_TIMEOUT"
+
+
+def test_host_side_validation_without_gpu(lib):
+    """Bad arguments are rejected on the host before anything is enqueued."""
+    f = lib.mpfa_prefill
+    f.restype = ctypes.c_int
+    # d != 128 -> unsupported; null tensors -> invalid
+    assert f(None, None, None, None, 1, 128, 1, 1, 64, 0, 0, 0, None, None, None) == 2
+    assert f(None, None, None, None, 1, 128, 1, 1, 128, 0, 0, 0, None, None, None) == 1
+    q = lib.mpfa_quantize_qkv
+    q.restype = ctypes.c_int
+    assert q(None, None, None, 1, 128, 128, 1, 1, 128, 0, 2, None, None, None, None, None, 0,
+             None) == 1
+    assert q(None, None, None, 1, 128, 128, 1, 1, 96, 0, 2, None, None, None, None, None, 0,
+             None) == 2
+
+
+def test_workspace_size_queries(lib):
+    lib.mpfa_quantize_workspace_size.restype = ctypes.c_size_t
+    n0 = lib.mpfa_quantize_workspace_size(1, 256, 2, 0)
+    n1 = lib.mpfa_quantize_workspace_size(1, 256, 2, 1)
+    assert n1 - n0 == 2 * 2 * 128 * 4
