@@ -1,0 +1,393 @@
+"""Benchmark of the MpFA QK4PV8 attention forward on GB300.
+
+One step = the whole prefill hot path on the Llama-3.1-8B attention shape
+(B=1, 32 query / 8 KV heads, d=128, N=16384, causal): online NVFP4/FP8
+quantization of Q, K, V (mpfa_quantize_qkv) followed by the prefill kernel
+(mpfa_prefill), on synthetic inputs resident in HBM.  ``value`` is the
+algorithmic attention TFLOP/s of that step (512 FLOP per visible
+(query, key) pair: 256 for QK^T in FP4, 256 for PV in FP8).  L2 is flushed
+(a 512 MB write) before every timed step.
+
+The same JSON line carries:
+  roofline      prefill kernel vs the FP4/FP8 tensor-pipe roofline
+  decode        split-KV decode on B=64 x 32K cached tokens: KV GB/s vs HBM
+  e2e           the step through the C ABI with host buffers (pinned H2D of
+                bf16 Q/K/V, D2H of O) inside the timed region
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload
+  clocks        nvidia-smi samples taken during the timed region
+
+``--impl reference`` times the CPU oracle instead (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import mpfa_inputs as mi  # noqa: E402
+
+METRIC = "prefill attention TFLOP/s & decode KV GB/s on 1 GB300, % of FP4/FP8/HBM roofline"
+PREFILL_CFG = mi.PREFILL["llama8b_n16k_causal"]
+DECODE_CFG = mi.DECODE["decode_b64_l32k"]
+FLOP_PER_PAIR = 512
+KV_BYTES_PER_TOKEN = 64 + 8 + 128   # K codes + K block scales + V codes, per KV head
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sus=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle on a bounded sample (cpu_baseline and the reference arm)
+# ----------------------------------------------------------------------------
+
+def oracle_sample(Q, K, V, rows_per_head=64, heads=((0, 0), (0, 9), (0, 22), (0, 31))):
+    """Time the CPU oracle on query rows sampled from the prefill workload:
+    tensor scales from the whole tensors, the codes of the sampled heads, and
+    the emulated forward of the sampled rows (last tile and spread positions).
+    Returns (tflops, seconds, description, threads)."""
+    import numpy as np
+
+    import oracle as orc
+    cfg = PREFILL_CFG
+    g = cfg.Hq // cfg.Hkv
+    t0 = time.perf_counter()
+    Qn = Q.float().cpu().numpy()
+    Kn = K.float().cpu().numpy()
+    Vn = V.float().cpu().numpy()
+    # whole-tensor statistics the codes depend on
+    amax_q = np.float32(0)
+    for h in range(cfg.Hq):
+        qb, qp = orc.block_means(np.ascontiguousarray(Qn[0, :, h, :]), 128)
+        amax_q = max(amax_q, np.float32(np.abs(qp).max()), np.float32(np.abs(qb).max()))
+    s_q = orc.tensor_scale(amax_q, 2688.0)
+    s_k = orc.tensor_scale(np.abs(Kn).max(), 2688.0)
+    s_v = orc.tensor_scale(np.abs(Vn).max(), 448.0)
+    flops = 0
+    n = cfg.N
+    rows = np.unique(np.linspace(0, n - 1, rows_per_head).astype(np.int64))
+    for (b, h) in heads:
+        hk = h // g
+        qb, qp = orc.block_means(np.ascontiguousarray(Qn[b, :, h, :]), 128)
+        qc, qs = orc.nvfp4_quantize(qp, s_q)
+        tc, ts = orc.rank_one_terms(qb, s_q, 2)
+        kc, ks = orc.nvfp4_quantize(np.ascontiguousarray(Kn[b, :, hk, :]), s_k)
+        vc = orc.fp8_quantize(np.ascontiguousarray(Vn[b, :, hk, :]), s_v)
+        qz = dict(qc=qc[None, None], qs=qs[None, None], qbc=tc[None, None], qbs=ts[None, None],
+                  s_q=s_q)
+        kz = dict(kc=kc[None, None], ks=ks[None, None], s_k=s_k)
+        vz = dict(vc=vc[None, None], s_v=s_v)
+        orc.prefill_emulate(qz, kz, vz, causal=cfg.causal, heads=[(0, 0)], rows=rows)
+        flops += FLOP_PER_PAIR * int((rows + 1).sum() if cfg.causal else rows.size * n)
+    dt = time.perf_counter() - t0
+    desc = (f"{len(heads)} heads x {rows.size} query rows of {cfg.name} (full causal key range "
+            f"each), incl. whole-tensor amax and per-head quantization")
+    return flops / dt / 1e12, dt, desc, orc.num_threads()
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle as orc
+    orc.build()
+    Q, K, V = mi.prefill_inputs(PREFILL_CFG, "cpu", 0)
+    for _ in range(args.warmup):
+        oracle_sample(Q, K, V, rows_per_head=2, heads=((0, 0),))
+    vals, times = [], []
+    for _ in range(args.steps):
+        v, dt, desc, thr = oracle_sample(Q, K, V)
+        vals.append(v)
+        times.append(dt)
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (emulated nvfp4/fp8 codes)",
+            "data": "synthetic", "config": {"workload": PREFILL_CFG.name, "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def run_gpu(args):
+    import flashattention_mpfa_quantize_gb300 as mp
+    ws, rank, local = _dist()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    peaks = _peaks()
+    cfg = PREFILL_CFG
+    stream = torch.cuda.current_stream(dev)
+
+    Q, K, V = mi.prefill_inputs(cfg, dev, seed=rank)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    qz = mp.quantize_qkv(Q, K, V, compensate=True, T=2)
+    ws_q = qz["_workspace"]
+    o, lse = mp.prefill(qz, causal=cfg.causal)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        z = mp.quantize_qkv(Q, K, V, compensate=True, T=2, workspace=ws_q)
+        if ev is not None:
+            ev[1].record(stream)
+        mp.prefill(z, causal=cfg.causal, out=o, lse=lse)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if mp.get_error() != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = Clocks(dev.index)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if ws > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
+    quant_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    pre_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    ms = statistics.mean(step_ms)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    flops = FLOP_PER_PAIR * cfg.pairs
+    value = ws * flops / (ms * 1e-3) / 1e12
+
+    # prefill roofline: FP4 QK^T + FP8 PV against the measured bf16 peak times
+    # the nominal dense ratios (FP4 = 6x, FP8 = 2x bf16)
+    pre = statistics.mean(pre_ms)
+    f4 = f8 = flops / 2
+    p4, p8 = 6 * peaks["bf16"], 2 * peaks["bf16"]
+    t_roof = f4 / (p4 * 1e12) + f8 / (p8 * 1e12)
+    peak_eff = (f4 + f8) / t_roof / 1e12
+    achieved = flops / (pre * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_eff, "unit": "TFLOP/s",
+                "frac": achieved / peak_eff, "traffic": None,
+                "kernel": "prefill_kernel", "peak_source": peaks["source"] + " bf16 burst x "
+                "nominal FP4 (6x) / FP8 (2x) ratios, harmonic mix for equal FP4 and FP8 FLOPs",
+                "quantize_ms": statistics.mean(quant_ms), "prefill_ms": pre}
+
+    dec = run_decode(mp, dev, stream, peaks, flush, args) if args.only != "prefill" else {}
+    e2e = run_e2e(mp, dev, stream, Q, K, V, args) if args.only is None else None
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and args.only is None:
+        try:
+            Qc, Kc, Vc = Q.cpu(), K.cpu(), V.cpu()
+            v, dt, desc, thr = oracle_sample(Qc, Kc, Vc)
+            cpu = {"value": v, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                   "sample": desc, "seconds": dt}
+        except Exception as ex:  # pragma: no cover - reported, not fatal
+            cpu = {"error": repr(ex)}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "nvfp4 e2m1 (QK) + fp8 e4m3 (PV), fp32 accumulate", "data": "synthetic",
+                "config": {"workload": cfg.name, "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv,
+                           "N": cfg.N, "d": 128, "causal": cfg.causal, "compensate": True,
+                           "T": 2, "step": "mpfa_quantize_qkv + mpfa_prefill",
+                           "l2": "flushed (512 MB write) before every step",
+                           "parallelism": "replicas" if ws > 1 else "single"},
+                "roofline": roofline, "decode": dec, "e2e": e2e, "cpu_baseline": cpu,
+                "gpu_launches": args.steps * 3 + dec.get("gpu_launches", 0),
+                "clocks": clk, "wall_s": t_wall}
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_decode(mp, dev, stream, peaks, flush, args):
+    cfg = DECODE_CFG
+    if args.decode_batch:
+        cfg = mi.custom_decode(args.decode_batch, cfg.Hq, cfg.Hkv, cfg.Lmax, cfg.len_lo,
+                               cfg.len_hi, name=f"{cfg.name}_b{args.decode_batch}")
+    q, K, V, seqlens = mi.decode_inputs(cfg, dev, seed=1)
+    cache = mp.quantize_qkv(None, K, V)
+    del K, V
+    res = mp.decode(q, cache, seqlens)
+    ws_d = res["_workspace"]
+    out, lse = res["o"], res["lse"]
+    for _ in range(3):
+        flush.zero_()
+        mp.decode(q, cache, seqlens, out=out, lse=lse, workspace=ws_d)
+    torch.cuda.synchronize()
+    n = max(args.steps, 5)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for i in range(n):
+        flush.zero_()
+        evs[i][0].record(stream)
+        mp.decode(q, cache, seqlens, out=out, lse=lse, workspace=ws_d)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    tokens = int(seqlens.long().sum().item())
+    nbytes = tokens * cfg.Hkv * KV_BYTES_PER_TOKEN
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del cache
+    return {"workload": cfg.name, "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "L": cfg.Lmax,
+            "value": gbs, "unit": "GB/s", "ms": ms, "chunk": res["chunk"],
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm"], "traffic": None,
+                         "algorithmic_bytes": nbytes},
+            "gpu_launches": 4 * n}
+
+
+def run_e2e(mp, dev, stream, Q, K, V, args):
+    """Same step through the public API with pinned host buffers: H2D of the
+    bf16 inputs, quantize, prefill, D2H of O, all inside the timed region."""
+    cfg = PREFILL_CFG
+    hq = torch.empty(Q.shape, dtype=Q.dtype, pin_memory=True)
+    hk = torch.empty(K.shape, dtype=K.dtype, pin_memory=True)
+    hv = torch.empty(V.shape, dtype=V.dtype, pin_memory=True)
+    hq.copy_(Q)
+    hk.copy_(K)
+    hv.copy_(V)
+    ho = torch.empty(Q.shape, dtype=torch.bfloat16, pin_memory=True)
+    dq, dk, dv = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    o = torch.empty_like(Q)
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        z = mp.quantize_qkv(dq, dk, dv, compensate=True, T=2)
+        mp.prefill(z, causal=cfg.causal, out=o, want_lse=False)
+        ho.copy_(o, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    n = max(args.steps, 3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(n):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / n
+    flops = FLOP_PER_PAIR * cfg.pairs
+    h2d = (Q.numel() + K.numel() + V.numel()) * 2
+    return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": Q.numel() * 2}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+                    help="profiling aid: time only this part (no e2e / cpu baseline)")
+    ap.add_argument("--decode-batch", type=int, default=None,
+                    help="profiling aid: smaller decode batch than the workload's 64")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

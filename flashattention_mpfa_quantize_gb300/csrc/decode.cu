@@ -51,7 +51,7 @@ constexpr uint32_t kOffP = kOffQs + 3 * 1024;           // 2 x 2 KB: P^T (16 row
 constexpr uint32_t kOffOnes = kOffP + 2 * 2048;         // 4 KB ones (128 rows x 32 B)
 constexpr uint32_t kOffRed = kOffOnes + 4096;           // 4 warps x 16 floats
 constexpr uint32_t kOffBar = kOffRed + 4 * 16 * 4;
-constexpr uint32_t kNumBars = 8 + 3 * kStages;
+constexpr uint32_t kNumBars = 8 + 3 * kStages + 2;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemUsed = kOffMisc + 64;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;
@@ -62,6 +62,7 @@ enum : int {
   kBarPReady0 = 3,  // +bank
   kBarODone = 5,
   kBarDrain = 6,
+  kBarPFree0 = 7 + 3 * kStages + 1,  // +bank: P^T buffer read by its PV MMAs
   kBarKFull0 = 8,
   kBarVFull0 = 8 + kStages,
   kBarKvEmpty0 = 8 + 2 * kStages,
@@ -231,6 +232,8 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
     mbar_init(bar(kBarPReady0 + 1), 128);
     mbar_init(bar(kBarODone), 1);
     mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarPFree0), 1);
+    mbar_init(bar(kBarPFree0 + 1), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(kBarKFull0 + s), 1);
       mbar_init(bar(kBarVFull0 + s), 1);
@@ -297,6 +300,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
                      id_l, (jp > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(bar(kBarODone));
+        if (jp + 2 < ntiles) tc_commit(bar(kBarPFree0 + bp));
         if (jp + kStages < ntiles) tc_commit(bar(kBarKvEmpty0 + sp));
         return true;
       };
@@ -426,9 +430,11 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
         any_change |= (n < g) && (alpha[n] != 1.0f);
         m[n] = mn;
       }
-      // P^T: row n, column key (128-byte rows, 128-byte swizzle)
-      if (j >= 2 &&
-          !named_bar_and(2, 128, mbar_wait(bar(kBarODone), (j - 2) & 1, a.err, abort_flag))) {
+      // P^T: row n, column key (128-byte rows, 128-byte swizzle).  Buffer
+      // j % 2 was last read by PV_{j-2}; its own barrier completes once per
+      // two tiles, so the parity cannot run two phases ahead of this wait.
+      if (j >= 2 && !named_bar_and(2, 128, mbar_wait(bar(kBarPFree0 + bkk), ((j >> 1) - 1) & 1,
+                                                     a.err, abort_flag))) {
         ok = false;
         break;
       }
