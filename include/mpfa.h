@@ -124,6 +124,29 @@ mpfa_status mpfa_quantize_qkv(const void *q_bf16, const void *k_bf16, const void
                               mpfa_stream_t stream);
 
 /*
+ * mpfa_quantize_qkv without a caller workspace.  The paper has no
+ * counterpart: this entry point exists for callers that cannot allocate
+ * device memory (a serving process whose HBM is owned by its own pool and
+ * must not call cudaMalloc after start-up; a host that hands the library only
+ * its input and output tensors).  It allocates nothing; its scratch is a
+ * fixed device array inside the library of 256 + 16 MiB bytes, which every
+ * GPU that loads the library holds until the process exits.
+ *   Arguments, layouts and results are those of mpfa_quantize_qkv.
+ *   Limit: with compensate != 0 the block means of Q must fit, i.e.
+ *   B * Hq * Nq / 128 <= 32768 query blocks; larger problems return
+ *   MPFA_ERR_INVALID_ARG with nothing enqueued (use mpfa_quantize_qkv).
+ *   The first call on each device looks up the array's device address (with
+ *   that device current) and caches it; make that first call before any
+ *   stream capture.  All calls on a device share the array: calls whose work
+ *   overlaps on the GPU race, so order them (one stream, or events).
+ */
+mpfa_status mpfa_quantize_qkv_noalloc(const void *q_bf16, const void *k_bf16,
+                                      const void *v_bf16, int B, int Nq, int Nk, int Hq, int Hkv,
+                                      int d, int compensate, int T, mpfa_nvfp4 *q_out,
+                                      mpfa_rank1 *qbar_out, mpfa_nvfp4 *k_out, mpfa_fp8 *v_out,
+                                      mpfa_stream_t stream);
+
+/*
  * Prefill forward (MpFA abstract; FlashAttention-2 tiling and online softmax
  * per the explainer): O = softmax(s_q s_k S / sqrt(d)) V with S from the
  * block-scaled FP4 product plus the rank-one term, P stored as E4M3(2^8 p),
