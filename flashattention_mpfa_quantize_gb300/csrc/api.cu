@@ -3,6 +3,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "device.cuh"
 #include "internal.h"
 #include "mpfa.h"
 
@@ -25,6 +26,16 @@ int* status_ptr() {
     g_status_ptr[dev] = static_cast<int*>(p);
   }
   return g_status_ptr[dev];
+}
+
+// One thread waits on a shared-memory barrier that nothing arrives on; the
+// bounded wait gives up after limit_ns and records MPFA_ERR_TIMEOUT.
+__global__ void selftest_wait_kernel(int* err, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = mpfa::smem_u32(&bar);
+  mpfa::mbar_init(b, 1);
+  mpfa::fence_barrier_init();
+  mpfa::mbar_wait(b, 0, err, nullptr, limit_ns);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -238,6 +249,14 @@ mpfa_status mpfa_decode(const void* q_bf16, const mpfa_nvfp4* k_cache, const mpf
   if (!a.err) return MPFA_ERR_CUDA;
   if (used_chunk) *used_chunk = chunk;
   return from_cuda(mpfa::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mpfa_status mpfa_selftest_wait_timeout(unsigned long long limit_ns, mpfa_stream_t stream) {
+  if (limit_ns == 0 || limit_ns > 2000000000ull) return MPFA_ERR_INVALID_ARG;
+  int* err = status_ptr();
+  if (!err) return MPFA_ERR_CUDA;
+  selftest_wait_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err, limit_ns);
+  return from_cuda(cudaGetLastError());
 }
 
 mpfa_status mpfa_get_error(mpfa_stream_t stream) {

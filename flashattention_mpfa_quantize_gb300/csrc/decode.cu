@@ -425,8 +425,9 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
 #pragma unroll
       for (int n = 0; n < kMaxG; ++n) {
         const float smax = fmaxf(fmaxf(red[n], red[16 + n]), fmaxf(red[32 + n], red[48 + n]));
-        const float mn = fmaxf(m[n], __fmul_rn(smax, cs));
-        alpha[n] = (m[n] == -INFINITY) ? 0.0f : ex2(m[n] - mn);
+        const float tmax = __fmul_rn(smax, cs);
+        const float mn = (m[n] == -INFINITY || tmax > m[n] + kRescaleTau) ? tmax : m[n];
+        alpha[n] = (m[n] == -INFINITY) ? 0.0f : (mn == m[n] ? 1.0f : ex2(m[n] - mn));
         any_change |= (n < g) && (alpha[n] != 1.0f);
         m[n] = mn;
       }
@@ -442,7 +443,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
 #pragma unroll
       for (int n = 0; n < kMaxG; ++n) {
         if (n < g) {
-          const float pv = (m[n] == -INFINITY) ? 0.0f : ex2(fmaf(v[n], cs, 8.0f - m[n]));
+          const float pv = (m[n] == -INFINITY) ? 0.0f : ex2(fmaf(v[n], cs, kPShift - m[n]));
           pt[n * 128 + ((((t >> 4) ^ (n & 7))) << 4) + (t & 15)] = (uint8_t)e4m3_pos(pv);
         }
       }
@@ -525,7 +526,8 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
         const size_t row = (size_t)bk * g + n;
         a.part_o[(row * a.nsplit + split) * 128 + t] = __uint_as_float(o16[n]) * __fdiv_rn(sv, l);
         if (t == 0)
-          a.part_lse[row * a.nsplit + split] = 0.69314718055994531f * (m[n] + __log2f(l) - 8.0f);
+          a.part_lse[row * a.nsplit + split] =
+              0.69314718055994531f * (m[n] + __log2f(l) - kPShift);
       }
     }
   }

@@ -11,16 +11,23 @@
 // explainer's Direct-P section states that rule).
 //
 // One CTA computes one 128-row query tile of one (batch, head):
-//   warp 4    TMA producer: Q tile once, then K / K-scale / V tiles through a
-//             ring of kStages shared-memory stages.
-//   warp 5    MMA issuer: block scales into TMEM (tcgen05.cp), QK^T and the
-//             rank-one MMAs into score bank j % 2, then PV_{j-1} and the
-//             row-sum MMA once the softmax has published P_{j-1}.
-//   warps 0-3 softmax + correction + epilogue, one query row per thread
-//             (TMEM lane = row): max, exp2, E4M3 P stored over the scores,
-//             rescale of O when the running max moves, O / l and LSE.
+//   warp 8    TMA producer: Q tile once, then K / K-scale tiles through a
+//             ring of kKStages stages and V tiles through kVStages stages.
+//   warp 9    MMA issuer: block scales into TMEM (tcgen05.cp), QK^T and the
+//             rank-one MMAs into score bank j % 2; once the softmax has read
+//             S_j and published P_j it issues PV_j and the row-sum MMA, then
+//             QK_{j+2} into the freed bank.
+//   warps 0-7 softmax + correction + epilogue in two warpgroups: thread
+//             (row r, half h) owns keys 64h..64h+63 of query row r (TMEM lane
+//             r), so two warps share each scheduler.  The two halves of a row
+//             exchange their partial maxima through shared memory; each
+//             stores its 16 columns of E4M3 P over the scores, rescales its
+//             64 columns of O when the running max moves, and writes its half
+//             of the output row.
 // Tensor memory (512 columns): S0 [0,128) S1 [128,256) O [256,384)
-// L [384,400) scale factors [400,448).
+// P0 [384,416) P1 [416,448) L [448,464) scale factors [464,512).  P has its
+// own columns so the scores of tile j+2 can be computed into bank j % 2 as
+// soon as the softmax has read tile j, while PV_j still reads P_j.
 #include <cmath>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -35,24 +42,29 @@ bool make_map_2d_u8(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint
 
 namespace {
 
-constexpr int kStages = 3;
-constexpr int kThreads = 192;
+constexpr int kKStages = 4;   // K tiles: released once QK has read them
+constexpr int kVStages = 3;   // V tiles: released once PV has read them
+constexpr int kSfSlots = 3;   // TMEM block-scale slots for K (slot j % 3)
+constexpr int kThreads = 320;
+constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr int kSoftmaxThreads = 256;
 constexpr int kTmemCols = 512;
 
-constexpr uint32_t kColS0 = 0, kColO = 256, kColL = 384, kColSfQ = 400, kColSfQb = 408,
-                   kColSfK = 424;
+constexpr uint32_t kColS0 = 0, kColO = 256, kColP0 = 384, kColL = 448, kColSfQ = 464,
+                   kColSfQb = 472, kColSfK = 488;
 
 // shared memory layout (offsets from a 1024-byte aligned base)
 constexpr uint32_t kOffQ = 0;                           // 8 KB
 constexpr uint32_t kOffQb = kOffQ + 8192;               // 2 x 8 KB
-constexpr uint32_t kOffK = kOffQb + 2 * 8192;           // kStages x 8 KB
-constexpr uint32_t kOffV = kOffK + kStages * 8192;      // kStages x 16 KB
-constexpr uint32_t kOffQs = kOffV + kStages * 16384;    // 1 KB
-constexpr uint32_t kOffQbs = kOffQs + 1024;             // 2 x 1 KB
-constexpr uint32_t kOffKs = kOffQbs + 2048;             // kStages x 1 KB
-constexpr uint32_t kOffOnes = kOffKs + kStages * 1024;  // 2 KB
-constexpr uint32_t kOffBar = kOffOnes + 2048;
-constexpr uint32_t kNumBars = 8 + 3 * kStages;
+constexpr uint32_t kOffK = kOffQb + 2 * 8192;            // kKStages x 8 KB
+constexpr uint32_t kOffV = kOffK + kKStages * 8192;      // kVStages x 16 KB
+constexpr uint32_t kOffQs = kOffV + kVStages * 16384;    // 1 KB
+constexpr uint32_t kOffQbs = kOffQs + 1024;              // 2 x 1 KB
+constexpr uint32_t kOffKs = kOffQbs + 2048;              // kKStages x 1 KB
+constexpr uint32_t kOffOnes = kOffKs + kKStages * 1024;  // 2 KB
+constexpr uint32_t kOffRed = kOffOnes + 2048;          // 2 x 2 x 128 floats (row maxima)
+constexpr uint32_t kOffBar = kOffRed + 2048;
+constexpr uint32_t kNumBars = 9 + 2 * kKStages + 2 * kVStages;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemUsed = kOffMisc + 64;
 // Request more than half an SM's shared memory so a single CTA owns the
@@ -64,13 +76,14 @@ static_assert(kSmemUsed + 1024 <= kSmemBytes, "shared memory layout overflow");
 enum : int {
   kBarQFull = 0,
   kBarQbReady = 1,
-  kBarSFull0 = 2,   // +bank
-  kBarPReady0 = 4,  // +bank
-  kBarODone = 6,
-  kBarDrain = 7,
-  kBarKFull0 = 8,                  // +stage
-  kBarVFull0 = 8 + kStages,        // +stage
-  kBarKvEmpty0 = 8 + 2 * kStages,  // +stage
+  kBarSFull0 = 2,   // +bank: scores of tile j in bank j % 2
+  kBarPReady0 = 4,  // +bank: softmax has read S_j and written P_j
+  kBarODone0 = 6,   // +bank: PV_j (reading P bank j % 2) has completed
+  kBarDrain = 8,
+  kBarKFull0 = 9,                          // +K stage
+  kBarKEmpty0 = 9 + kKStages,              // +K stage
+  kBarVFull0 = 9 + 2 * kKStages,           // +V stage
+  kBarVEmpty0 = 9 + 2 * kKStages + kVStages,  // +V stage
 };
 
 struct Params {
@@ -113,27 +126,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(bar(kBarQFull), 1);
-    mbar_init(bar(kBarQbReady), 128);
+    mbar_init(bar(kBarQbReady), kSoftmaxThreads);
     mbar_init(bar(kBarSFull0), 1);
     mbar_init(bar(kBarSFull0 + 1), 1);
-    mbar_init(bar(kBarPReady0), 128);
-    mbar_init(bar(kBarPReady0 + 1), 128);
-    mbar_init(bar(kBarODone), 1);
+    mbar_init(bar(kBarPReady0), kSoftmaxThreads);
+    mbar_init(bar(kBarPReady0 + 1), kSoftmaxThreads);
+    mbar_init(bar(kBarODone0), 1);
+    mbar_init(bar(kBarODone0 + 1), 1);
     mbar_init(bar(kBarDrain), 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(bar(kBarKFull0 + s), 1);
+      mbar_init(bar(kBarKEmpty0 + s), 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(bar(kBarVFull0 + s), 1);
-      mbar_init(bar(kBarKvEmpty0 + s), 1);
+      mbar_init(bar(kBarVEmpty0 + s), 1);
     }
     fence_barrier_init();
   }
-  if (warp == 5) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  if (warp == kWarpMma) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == kWarpTma) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       prefetch_tensormap(&map_q);
@@ -144,28 +161,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_2d(sbase + kOffQ, &map_q, 0, qrow, bar(kBarQFull));
       bulk_load(sbase + kOffQs, a.qs + (size_t)qrow * 8, 1024, bar(kBarQFull));
       const int kvrow0 = (b * a.Hkv + hk) * a.N;
-      int issued = 0;
-      for (int j = 0; j < nkv; ++j) {
-        const int s = j % kStages;
-        if (j >= kStages &&
-            !mbar_wait(bar(kBarKvEmpty0 + s), ((j / kStages) - 1) & 1, a.err, abort_flag))
-          break;
+      // loads in the order the MMA warp consumes them: K_0, K_1, then
+      // V_j and K_{j+2} for j = 0, 1, ...
+      int k_issued = 0, v_issued = 0;
+      auto load_k = [&](int j) -> bool {
+        const int s = j % kKStages;
+        if (j >= kKStages &&
+            !mbar_wait(bar(kBarKEmpty0 + s), ((j / kKStages) - 1) & 1, a.err, abort_flag))
+          return false;
         const int row = kvrow0 + j * 128;
         mbar_expect_tx(bar(kBarKFull0 + s), 8192 + 1024);
         tma_load_2d(sbase + kOffK + s * 8192, &map_k, 0, row, bar(kBarKFull0 + s));
         bulk_load(sbase + kOffKs + s * 1024, a.ks + (size_t)row * 8, 1024, bar(kBarKFull0 + s));
+        k_issued = j + 1;
+        return true;
+      };
+      auto load_v = [&](int j) -> bool {
+        const int s = j % kVStages;
+        if (j >= kVStages &&
+            !mbar_wait(bar(kBarVEmpty0 + s), ((j / kVStages) - 1) & 1, a.err, abort_flag))
+          return false;
         mbar_expect_tx(bar(kBarVFull0 + s), 16384);
-        tma_load_2d(sbase + kOffV + s * 16384, &map_v, 0, row, bar(kBarVFull0 + s));
-        issued = j + 1;
+        tma_load_2d(sbase + kOffV + s * 16384, &map_v, 0, kvrow0 + j * 128, bar(kBarVFull0 + s));
+        v_issued = j + 1;
+        return true;
+      };
+      bool lok = load_k(0) && (nkv < 2 || load_k(1));
+      for (int j = 0; lok && j < nkv; ++j) {
+        if (!load_v(j)) break;
+        if (j + 2 < nkv && !load_k(j + 2)) break;
       }
       // drain: every stage's last load must have landed before the CTA exits
-      for (int j = issued - kStages > 0 ? issued - kStages : 0; j < issued; ++j) {
-        const int s = j % kStages;
-        mbar_wait(bar(kBarKFull0 + s), (j / kStages) & 1, a.err, nullptr);
-        mbar_wait(bar(kBarVFull0 + s), (j / kStages) & 1, a.err, nullptr);
-      }
+      for (int j = k_issued - kKStages > 0 ? k_issued - kKStages : 0; j < k_issued; ++j)
+        mbar_wait(bar(kBarKFull0 + j % kKStages), (j / kKStages) & 1, a.err, nullptr);
+      for (int j = v_issued - kVStages > 0 ? v_issued - kVStages : 0; j < v_issued; ++j)
+        mbar_wait(bar(kBarVFull0 + j % kVStages), (j / kVStages) & 1, a.err, nullptr);
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       const uint32_t id_qk = idesc_nvfp4(128, 128);
@@ -185,30 +217,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 smem_desc(sbase + kOffQbs + 1024 * t + 512 * kc, 128, 128, kSwizzleNone));
       }
       const uint64_t ones = smem_desc(sbase + kOffOnes, 128, 256, kSwizzleNone);
-      auto issue_pv = [&](int jp) -> bool {
-        const int bp = jp & 1, sp = jp % kStages;
-        if (!mbar_wait(bar(kBarPReady0 + bp), (jp >> 1) & 1, a.err, abort_flag)) return false;
-        if (!mbar_wait(bar(kBarVFull0 + sp), (jp / kStages) & 1, a.err, abort_flag))
-          return false;
+      // QK_j (and the rank-one MMAs) into score bank j % 2
+      auto issue_qk = [&](int j) -> bool {
+        const int s = j % kKStages, bk = j & 1;
+        if (!mbar_wait(bar(kBarKFull0 + s), (j / kKStages) & 1, a.err, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t pcol = tmem + kColS0 + 128 * bp;
-        const uint32_t vaddr = sbase + kOffV + sp * 16384;
-        for (int kk = 0; kk < 4; ++kk)
-          mma_fp8_ts(tmem + kColO, pcol + 8 * kk, smem_desc(vaddr + 4096 * kk, 16, 1024, kSwizzle128B),
-                     id_pv, (jp > 0 || kk > 0) ? 1u : 0u);
-        for (int kk = 0; kk < 4; ++kk)
-          mma_fp8_ts(tmem + kColL, pcol + 8 * kk, ones, id_l, (jp > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(bar(kBarODone));
-        if (jp + kStages < nkv) tc_commit(bar(kBarKvEmpty0 + sp));
-        return true;
-      };
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int s = j % kStages, bk = j & 1;
-        if (!mbar_wait(bar(kBarKFull0 + s), (j / kStages) & 1, a.err, abort_flag)) break;
-        // bank bk was last read by PV_{j-2}
-        if (j >= 2 && !mbar_wait(bar(kBarODone), (j - 2) & 1, a.err, abort_flag)) break;
-        tc_fence_after();
-        const uint32_t sfk = tmem + kColSfK + 8 * s;
+        // slot j % 3: its last reader, QK_{j-3}, completed before the softmax
+        // of tile j-1 read its scores, which this issue waited for
+        const uint32_t sfk = tmem + kColSfK + 8 * (j % kSfSlots);
         for (int kc = 0; kc < 2; ++kc)
           tmem_cp_32x128b_x4(sfk + 4 * kc,
                              smem_desc(sbase + kOffKs + 1024 * s + 512 * kc, 128, 128, kSwizzleNone));
@@ -216,100 +232,152 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t kaddr = sbase + kOffK + 8192 * s;
         for (int kc = 0; kc < 2; ++kc)
           mma_nvfp4_ss(dS, smem_desc(sbase + kOffQ + 32 * kc, 16, 512, kSwizzle64B),
-                       smem_desc(kaddr + 32 * kc, 16, 512, kSwizzle64B), id_qk, tmem + kColSfQ + 4 * kc,
-                       sfk + 4 * kc, kc > 0 ? 1u : 0u);
+                       smem_desc(kaddr + 32 * kc, 16, 512, kSwizzle64B), id_qk,
+                       tmem + kColSfQ + 4 * kc, sfk + 4 * kc, kc > 0 ? 1u : 0u);
         for (int t = 0; t < T; ++t)
           for (int kc = 0; kc < 2; ++kc)
             mma_nvfp4_ss(dS, smem_desc(sbase + kOffQb + 8192 * t + 32 * kc, 16, 512, kSwizzle64B),
                          smem_desc(kaddr + 32 * kc, 16, 512, kSwizzle64B), id_qk,
                          tmem + kColSfQb + 8 * t + 4 * kc, sfk + 4 * kc, 1u);
         tc_commit(bar(kBarSFull0 + bk));
-        if (j >= 1 && !issue_pv(j - 1)) {
-          ok = false;
-          break;
-        }
+        if (j + kKStages < nkv) tc_commit(bar(kBarKEmpty0 + s));
+        return true;
+      };
+      // PV_j and the row-sum MMA (P from P bank j % 2, V from stage j % kVStages)
+      auto issue_pv = [&](int j) -> bool {
+        const int bp = j & 1, sp = j % kVStages;
+        if (!mbar_wait(bar(kBarVFull0 + sp), (j / kVStages) & 1, a.err, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t pcol = tmem + kColP0 + 32 * bp;
+        const uint32_t vaddr = sbase + kOffV + sp * 16384;
+        for (int kk = 0; kk < 4; ++kk)
+          mma_fp8_ts(tmem + kColO, pcol + 8 * kk,
+                     smem_desc(vaddr + 4096 * kk, 16, 1024, kSwizzle128B), id_pv,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 4; ++kk)
+          mma_fp8_ts(tmem + kColL, pcol + 8 * kk, ones, id_l, (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(bar(kBarODone0 + bp));
+        if (j + kVStages < nkv) tc_commit(bar(kBarVEmpty0 + sp));
+        return true;
+      };
+      if (ok) ok = issue_qk(0) && (nkv < 2 || issue_qk(1));
+      for (int j = 0; ok && j < nkv; ++j) {
+        // softmax(j) has read S_j (bank j % 2 is free) and written P_j
+        if (!mbar_wait(bar(kBarPReady0 + (j & 1)), (j >> 1) & 1, a.err, abort_flag)) break;
+        if (!issue_pv(j)) break;
+        if (j + 2 < nkv && !issue_qk(j + 2)) break;
       }
-      if (ok && nkv > 0) issue_pv(nkv - 1);
       // drain the tensor pipe before the CTA releases TMEM
       tc_commit(bar(kBarDrain));
       mbar_wait(bar(kBarDrain), 0, a.err, nullptr);
     }
   } else {
     // ---------------- softmax / correction / epilogue ----------------
-    const int row = threadIdx.x;  // 0..127, TMEM lane
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int half = warp >> 2;              // 0: keys 0..63, 1: keys 64..127
+    const int row = threadIdx.x & 127;       // query row = TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     // Rank-one operand tiles: every row holds the block's term t (same 64
     // bytes), written with the 64-byte swizzle the TMA applies to Q and K.
     const int nblk = a.N / 128;
-    for (int t = 0; t < T; ++t) {
-      const uint8_t* src = a.qbc + (((size_t)bh * nblk + qt) * a.T + t) * 64;
-      uint4* dst = reinterpret_cast<uint4*>(smem + kOffQb + 8192 * t + 64 * row);
+    if (half == 0) {
+      for (int t = 0; t < T; ++t) {
+        const uint8_t* src = a.qbc + (((size_t)bh * nblk + qt) * a.T + t) * 64;
+        uint4* dst = reinterpret_cast<uint4*>(smem + kOffQb + 8192 * t + 64 * row);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) dst[c ^ ((row >> 1) & 3)] = reinterpret_cast<const uint4*>(src)[c];
-      const uint8_t* ssrc = a.qbs + (((size_t)bh * nblk + qt) * a.T + t) * 8;
-      uint32_t w0 = *reinterpret_cast<const uint32_t*>(ssrc);
-      uint32_t w1 = *reinterpret_cast<const uint32_t*>(ssrc + 4);
-      reinterpret_cast<uint32_t*>(smem + kOffQbs + 1024 * t)[row] = w0;
-      reinterpret_cast<uint32_t*>(smem + kOffQbs + 1024 * t + 512)[row] = w1;
+        for (int c = 0; c < 4; ++c)
+          dst[c ^ ((row >> 1) & 3)] = reinterpret_cast<const uint4*>(src)[c];
+      }
+    } else {
+      for (int t = 0; t < T; ++t) {
+        const uint8_t* ssrc = a.qbs + (((size_t)bh * nblk + qt) * a.T + t) * 8;
+        uint32_t w0 = *reinterpret_cast<const uint32_t*>(ssrc);
+        uint32_t w1 = *reinterpret_cast<const uint32_t*>(ssrc + 4);
+        reinterpret_cast<uint32_t*>(smem + kOffQbs + 1024 * t)[row] = w0;
+        reinterpret_cast<uint32_t*>(smem + kOffQbs + 1024 * t + 512)[row] = w1;
+      }
+      // ones tile (E4M3 1.0 = 0x38) for the row-sum MMA
+      reinterpret_cast<uint4*>(smem + kOffOnes)[row] =
+          make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
     }
-    // ones tile (E4M3 1.0 = 0x38) for the row-sum MMA
-    reinterpret_cast<uint4*>(smem + kOffOnes)[row] = make_uint4(0x38383838u, 0x38383838u,
-                                                                 0x38383838u, 0x38383838u);
     fence_proxy_async_smem();
     mbar_arrive(bar(kBarQbReady));
 
+    float* red = reinterpret_cast<float*>(smem + kOffRed);  // [2 buffers][2 halves][128 rows]
+    const int pair_bar = 1 + (warp & 3);                     // warps w and w + 4
     const float cs = __fmul_rn(__fmul_rn(*a.s_q, *a.s_k), p.log2e_rsqrt_d);
     float m = -INFINITY;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
       const int bk = j & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarSFull0 + bk), (j >> 1) & 1, a.err, abort_flag))) {
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(bar(kBarSFull0 + bk), (j >> 1) & 1, a.err, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
       const uint32_t sS = tmem + lane_off + kColS0 + 128 * bk;
-      uint32_t sr[4][32];
-      tmem_ld32(sS, sr[0]);
-      tmem_ld32(sS + 32, sr[1]);
-      tmem_ld32(sS + 64, sr[2]);
-      tmem_ld32(sS + 96, sr[3]);
+      uint32_t sr[2][32];
+      tmem_ld32(sS + 64 * half, sr[0]);
+      tmem_ld32(sS + 64 * half + 32, sr[1]);
       tmem_ld_wait();
       if (a.causal && j == qt) {  // diagonal tile: key > row is masked
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (32 * c + i > row) sr[c][i] = 0xFF800000u;  // -inf
+            if (64 * half + 32 * c + i > row) sr[c][i] = 0xFF800000u;  // -inf
       }
-      // cs > 0, so max_i(S_i * cs) == (max_i S_i) * cs exactly
-      float smax = __uint_as_float(sr[0][0]);
+      // partial max over this thread's 64 keys (a tree of 3-input max)
+      float pm[11];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int k = 0; k < 10; ++k) {
+        const int e = 6 * k;
+        pm[k] = fmax3(fmax3(__uint_as_float(sr[e >> 5][e & 31]),
+                            __uint_as_float(sr[(e + 1) >> 5][(e + 1) & 31]),
+                            __uint_as_float(sr[(e + 2) >> 5][(e + 2) & 31])),
+                      __uint_as_float(sr[(e + 3) >> 5][(e + 3) & 31]),
+                      fmaxf(__uint_as_float(sr[(e + 4) >> 5][(e + 4) & 31]),
+                            __uint_as_float(sr[(e + 5) >> 5][(e + 5) & 31])));
+      }
+      pm[10] = fmax3(fmax3(__uint_as_float(sr[1][28]), __uint_as_float(sr[1][29]),
+                           __uint_as_float(sr[1][30])),
+                     __uint_as_float(sr[1][31]), -INFINITY);
+      const float lmax = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]),
+                               fmax3(fmax3(pm[6], pm[7], pm[8]), pm[9], pm[10]));
+      float* rb = red + 256 * bk;
+      rb[128 * half + row] = lmax;
+      named_bar_sync(pair_bar, 64);
+      const float smax = fmaxf(lmax, rb[128 * (half ^ 1) + row]);
+      // cs > 0, so max_i(S_i * cs) == (max_i S_i) * cs exactly.  The reference
+      // max moves only when the tile max exceeds it by more than kRescaleTau,
+      // so O and L rarely need a rescale once the first tiles are done.
+      const float tmax = __fmul_rn(smax, cs);
+      const float mn = (m == -INFINITY || tmax > m + kRescaleTau) ? tmax : m;
+      const float alpha = (m == -INFINITY) ? 0.0f : (mn == m ? 1.0f : ex2(m - mn));
+      const float bias = kPShift - mn;  // P8 = E4M3(2^(t - m) * 2^kPShift)
+      uint32_t pw[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) smax = fmaxf(smax, __uint_as_float(sr[c][i]));
-      const float mn = fmaxf(m, __fmul_rn(smax, cs));
-      const float alpha = (m == -INFINITY) ? 0.0f : ex2(m - mn);
-      const float bias = 8.0f - mn;  // P8 = E4M3(2^(t - m) * 2^8)
-      uint32_t pw[32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int w = 0; w < 8; ++w)
           pw[8 * c + w] = e4m3x4(ex2(fmaf(__uint_as_float(sr[c][4 * w]), cs, bias)),
                                  ex2(fmaf(__uint_as_float(sr[c][4 * w + 1]), cs, bias)),
                                  ex2(fmaf(__uint_as_float(sr[c][4 * w + 2]), cs, bias)),
                                  ex2(fmaf(__uint_as_float(sr[c][4 * w + 3]), cs, bias)));
-      tmem_st32(sS, pw);
-      // correction: O and L scale by alpha once PV_{j-1} has landed
+      // P bank j % 2 was last read by PV_{j-2}, which completed before S_j
+      // did: the MMA warp issues QK_j after PV_{j-2} and S_j's commit tracks it.
+      tmem_st16(tmem + lane_off + kColP0 + 32 * bk + 16 * half, pw);
+      // correction: O (this half's 64 columns) and L scale by alpha once
+      // PV_{j-1} has landed
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarODone), (j - 1) & 1, a.err, abort_flag))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarODone0 + ((j - 1) & 1)),
+                                               ((j - 1) >> 1) & 1, a.err, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t oO = tmem + lane_off + kColO;
-        for (int c = 0; c < 4; ++c) {
+        const uint32_t oO = tmem + lane_off + kColO + 64 * half;
+        for (int c = 0; c < 2; ++c) {
           uint32_t o[32];
           tmem_ld32(oO + 32 * c, o);
           tmem_ld_wait();
@@ -317,11 +385,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
           tmem_st32(oO + 32 * c, o);
         }
-        uint32_t l4[4];
-        tmem_ld4(tmem + lane_off + kColL, l4);
-        tmem_ld_wait();
-        l4[0] = __float_as_uint(__uint_as_float(l4[0]) * alpha);
-        tmem_st4(tmem + lane_off + kColL, l4);
+        if (half == 0) {
+          uint32_t l4[4];
+          tmem_ld4(tmem + lane_off + kColL, l4);
+          tmem_ld_wait();
+          l4[0] = __float_as_uint(__uint_as_float(l4[0]) * alpha);
+          tmem_st4(tmem + lane_off + kColL, l4);
+        }
       }
       tmem_st_wait();
       tc_fence_before();
@@ -329,7 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       m = mn;
     }
     if (ok && nkv > 0 &&
-        __all_sync(0xffffffffu, mbar_wait(bar(kBarODone), (nkv - 1) & 1, a.err, abort_flag))) {
+        __all_sync(0xffffffffu, mbar_wait(bar(kBarODone0 + ((nkv - 1) & 1)), ((nkv - 1) >> 1) & 1,
+                                          a.err, abort_flag))) {
       tc_fence_after();
       uint32_t l4[4];
       tmem_ld4(tmem + lane_off + kColL, l4);
@@ -338,10 +409,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float sc = __fdiv_rn(*a.s_v, l);
       const size_t grow = (size_t)qt * 128 + row;
       uint4* out = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) +
-                                            (((size_t)b * a.N + grow) * a.Hq + h) * 128);
-      for (int c = 0; c < 4; ++c) {
+                                            (((size_t)b * a.N + grow) * a.Hq + h) * 128 +
+                                            64 * half);
+      for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_off + kColO + 32 * c, o);
+        tmem_ld32(tmem + lane_off + kColO + 64 * half + 32 * c, o);
         tmem_ld_wait();
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
@@ -355,13 +427,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           out[4 * c + q4] = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
-      if (a.lse) a.lse[(size_t)bh * a.N + grow] = 0.69314718055994531f * (m + __log2f(l) - 8.0f);
+      if (a.lse && half == 0)
+        a.lse[(size_t)bh * a.N + grow] =
+            0.69314718055994531f * (m + __log2f(l) - kPShift);
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);

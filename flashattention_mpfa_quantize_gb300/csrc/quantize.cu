@@ -7,7 +7,7 @@
 // Two HBM-streaming passes, because every tensor scale depends on the whole
 // tensor:
 //   stats_kernel : amax of K and V; for Q either amax(Q) or, with the
-//                  smoothing, the fp32 block means qbar (exact fp64 sums) and
+//                  smoothing, the fp32 block means qbar (exact integer sums) and
 //                  max(amax(Q - qbar), amax(qbar)).
 //   quant_kernel : codes and scales of Q (or Q - qbar), of the qbar terms,
 //                  of K and of V; the tensor scales.
@@ -138,52 +138,105 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(QuantArgs a, int nq_blo
       amax_bf16(reinterpret_cast<const uint4*>(a.q), n8, 0, nq_blocks, &a.amax[0], red);
       return;
     }
-    // One CTA per (b, h, 128-row block): exact column sums in fp64.
+    // One CTA per (b, h, 128-row block).  Each column sum is computed
+    // exactly in integers: a bf16 value is M * 2^(e - 134) (M < 256); scaled
+    // to units of 2^(emax - 182), where emax is the column's largest
+    // exponent, every term is an integer below 2^56 and 128 of them fit an
+    // int64.  The sum then rounds once to fp32 (exact scaling by 2^k), i.e.
+    // the mean is the fp32 rounding of the exact mean.  A column whose values
+    // span more than 2^48 (or whose mean would be subnormal) takes an fp64
+    // path with a compensation term instead.
     int nblk = a.Nq / 128;
     int blk = bid % nblk;
     int bh = bid / nblk;
     int h = bh % a.Hq, b = bh / a.Hq;
     int cg = threadIdx.x & 15, rg = threadIdx.x >> 4;
     const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(a.q);
-    double acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    uint32_t w[16][4];
+#pragma unroll
     for (int i = 0; i < 16; ++i) {
       size_t n = (size_t)blk * 128 + rg + 8 * i;
       const uint4 v = __ldg(reinterpret_cast<const uint4*>(
           q + (((size_t)b * a.Nq + n) * a.Hq + h) * 128 + 8 * cg));
-      uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        acc[2 * t] += (double)bf16_lo(w[t]);
-        acc[2 * t + 1] += (double)bf16_hi(w[t]);
-      }
+      w[i][0] = v.x;
+      w[i][1] = v.y;
+      w[i][2] = v.z;
+      w[i][3] = v.w;
     }
+    auto bits = [&](int i, int t) -> uint32_t {  // bf16 bits of row i, column t (0..7)
+      return (t & 1) ? (w[i][t >> 1] >> 16) : (w[i][t >> 1] & 0xFFFFu);
+    };
+    int* emax_s = reinterpret_cast<int*>(&part[0][0]);  // [8][128] ints, reused below
 #pragma unroll
-    for (int t = 0; t < 8; ++t) part[rg][8 * cg + t] = acc[t];
+    for (int t = 0; t < 8; ++t) {
+      int e = 1;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) e = max(e, (int)((bits(i, t) >> 7) & 0xFFu));
+      emax_s[rg * 128 + 8 * cg + t] = e;
+    }
+    __syncthreads();
+    __shared__ int col_emax[128];
+    {
+      int e = emax_s[threadIdx.x];
+#pragma unroll
+      for (int g2 = 1; g2 < 8; ++g2) e = max(e, emax_s[g2 * 128 + threadIdx.x]);
+      col_emax[threadIdx.x] = e;
+    }
+    __syncthreads();
+    __shared__ int col_bad[128];
+    col_bad[threadIdx.x] = 0;
+    long long* ipart = reinterpret_cast<long long*>(&part[0][0]);  // [8][128]
+    __syncthreads();
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const int ce = col_emax[8 * cg + t];
+      long long acc = 0;
+      bool bad = false;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t u = bits(i, t);
+        const uint32_t ex = (u >> 7) & 0xFFu, mant = u & 0x7Fu;
+        const long long M = ex ? (long long)(mant | 0x80u) : (long long)mant;
+        const int sh = (ex ? (int)ex : 1) - ce + 48;
+        if (M != 0 && sh < 0) bad = true;
+        const long long term = (sh >= 0) ? (M << sh) : 0;
+        acc += (u & 0x8000u) ? -term : term;
+      }
+      ipart[rg * 128 + 8 * cg + t] = acc;
+      if (bad) col_bad[8 * cg + t] = 1;
+    }
     __syncthreads();
     {
-      int c = threadIdx.x;
-      double s = 0.0;
+      const int c = threadIdx.x;
+      long long S = 0;
 #pragma unroll
-      for (int g = 0; g < 8; ++g) s += part[g][c];
-      float mean = (float)(s * (1.0 / 128.0));
+      for (int g2 = 0; g2 < 8; ++g2) S += ipart[g2 * 128 + c];
+      float mean = ldexpf(__ll2float_rn(S), col_emax[c] - 189);
+      if (col_bad[c] || (mean != 0.0f && fabsf(mean) < 1.17549435e-38f)) {
+        // fp64 sum with a compensation term (same rounding as a correctly
+        // rounded sum whenever the correction captures the error)
+        double sd = 0.0, comp = 0.0;
+        for (int r = 0; r < 128; ++r) {
+          const double v = (double)__bfloat162float(
+              q[(((size_t)b * a.Nq + (size_t)blk * 128 + r) * a.Hq + h) * 128 + c]);
+          const double t2 = sd + v;
+          comp += (fabs(sd) >= fabs(v)) ? ((sd - t2) + v) : ((v - t2) + sd);
+          sd = t2;
+        }
+        mean = (float)((sd + comp) * (1.0 / 128.0));
+      }
       qb[c] = mean;
       a.qbar[((size_t)bh * nblk + blk) * 128 + c] = mean;
     }
     __syncthreads();
     unsigned m = __float_as_uint(fabsf(qb[threadIdx.x]));
-    for (int i = 0; i < 16; ++i) {
-      size_t n = (size_t)blk * 128 + rg + 8 * i;
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-          q + (((size_t)b * a.Nq + n) * a.Hq + h) * 128 + 8 * cg));
-      uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        float d0 = __fsub_rn(bf16_lo(w[t]), qb[8 * cg + 2 * t]);
-        float d1 = __fsub_rn(bf16_hi(w[t]), qb[8 * cg + 2 * t + 1]);
-        m = max(m, __float_as_uint(fabsf(d0)));
-        m = max(m, __float_as_uint(fabsf(d1)));
+    for (int i = 0; i < 16; ++i)
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const float x = __uint_as_float(bits(i, t) << 16);
+        m = max(m, __float_as_uint(fabsf(__fsub_rn(x, qb[8 * cg + t]))));
       }
-    }
     m = block_max_u32(m, red);
     if (threadIdx.x == 0 && m) atomicMax(&a.amax[0], m);
     return;

@@ -149,8 +149,10 @@ mpfa_status mpfa_quantize_qkv_noalloc(const void *q_bf16, const void *k_bf16,
 /*
  * Prefill forward (MpFA abstract; FlashAttention-2 tiling and online softmax
  * per the explainer): O = softmax(s_q s_k S / sqrt(d)) V with S from the
- * block-scaled FP4 product plus the rank-one term, P stored as E4M3(2^8 p),
- * KV tiles of 128 keys in ascending order, N_q = N_k = N (causal: key j
+ * block-scaled FP4 product plus the rank-one term, P stored as E4M3(2^4 p)
+ * with p = 2^(t - m) against the row's reference max m (set by the first
+ * KV tile, moved to a tile's max only when that max exceeds m by more than
+ * 4 in log2 units), KV tiles of 128 keys in ascending order, N_q = N_k = N (causal: key j
  * visible to query i iff j <= i).
  *   q/k/v from mpfa_quantize_qkv; qbar NULL iff compensate == 0.
  *   o_bf16 [B][N][Hq][d]; lse [B][Hq][N] natural-log sum-exp of the scaled
@@ -186,6 +188,14 @@ mpfa_status mpfa_decode(const void *q_bf16, const mpfa_nvfp4 *k_cache, const mpf
                         int compensate, int T, int kv_chunk, void *o_bf16, float *lse,
                         mpfa_nvfp4 *q_quant_out, mpfa_rank1 *qbar_quant_out, int *used_chunk,
                         void *workspace, size_t ws_bytes, mpfa_stream_t stream);
+
+/* Failure-path self-test: enqueues a one-thread kernel that waits, with the
+ * same bounded barrier wait every kernel uses, on an on-chip barrier that
+ * nothing arrives on.  After limit_ns nanoseconds (1 .. 2e9) the wait gives up
+ * and records MPFA_ERR_TIMEOUT in the device status word, which
+ * mpfa_get_error then reports; the CUDA context stays usable.  No fault, no
+ * hang. */
+mpfa_status mpfa_selftest_wait_timeout(unsigned long long limit_ns, mpfa_stream_t stream);
 
 /* Synchronizes the stream, then returns and clears the device status word
  * (MPFA_ERR_TIMEOUT after an expired on-chip wait), or MPFA_ERR_CUDA if the

@@ -40,7 +40,8 @@ D = 128            # head dimension the method is specified for
 QBLOCK = 128       # rows per query block of the rank-one smoothing (prefill)
 NVFP4_QMAX = 6.0 * 448.0
 FP8_QMAX = 448.0
-P_SHIFT = 8        # P is stored as E4M3(2^8 p)
+P_SHIFT = 4        # P is stored as E4M3(2^4 p)
+RESCALE_TAU = 4.0  # the row's reference max moves only when a tile max exceeds it by > 4
 
 
 def build(force: bool = False) -> str:
@@ -76,7 +77,7 @@ def _L():
             "orc_fp8_dequant": (None, [P, i64, P]),
             "orc_block_means": (None, [P, i64, i32, i64, i32, P, P, i32]),
             "orc_attn_online": (None, [P, P, P, P, i64, i64, i32, f64, f64, i32, i64, i64,
-                                       i32, P, i64, P, P, i32]),
+                                       i32, f64, f64, P, i64, P, P, i32]),
             "orc_attn_exact": (None, [P, P, P, i64, i64, i32, f64, i32, i64, P, i64, P, P,
                                       i32]),
             "orc_e2m1_encode_array": (None, [P, i64, P]),
@@ -331,9 +332,11 @@ def score_scale_log2(s_q: float, s_k: float, d: int = D) -> float:
 
 
 def attn_online(q, qadd, k, v, *, score_scale, out_scale, causal, kv_len=None, chunk=0,
-                round_p=True, rows=None, nthreads=0):
+                round_p=True, p_shift=P_SHIFT, tau=RESCALE_TAU, rows=None, nthreads=0):
     """Tiled online-softmax attention of one head (see orc_attn_online).
-    q, qadd [nq,d] fp64 (qadd may be None), k, v [nk,d] fp64."""
+    q, qadd [nq,d] fp64 (qadd may be None), k, v [nk,d] fp64.  P is stored as
+    E4M3(2^p_shift p); the row's reference max moves only when a tile's max
+    exceeds it by more than tau (tau = 0: the exact running max)."""
     q = np.ascontiguousarray(q, np.float64)
     k = np.ascontiguousarray(k, np.float64)
     v = np.ascontiguousarray(v, np.float64)
@@ -346,7 +349,7 @@ def attn_online(q, qadd, k, v, *, score_scale, out_scale, causal, kv_len=None, c
     _L().orc_attn_online(_p(q), None if qa is None else _p(qa), _p(k), _p(v), nq, nk, d,
                          float(score_scale), float(out_scale), int(bool(causal)),
                          nk if kv_len is None else int(kv_len), int(chunk), int(bool(round_p)),
-                         _p(rows), rows.size, _p(o), _p(lse), nthreads)
+                         float(p_shift), float(tau), _p(rows), rows.size, _p(o), _p(lse), nthreads)
     return o, lse
 
 

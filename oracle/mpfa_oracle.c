@@ -35,9 +35,12 @@
  *    the block's rows; Q' = fp32(Q - qbar); Q' and qbar are quantized to
  *    NVFP4 with one shared tensor scale; the score is
  *    S = s_q s_k (deq(Q')deq(K)^T + 1 deq(qbar) deq(K)^T).
- *  - P is stored as E4M3(2^8 p) with p = 2^(t - m_running); the running sum
- *    adds the decoded rounded codes [SHR]; KV tiles of 128 keys are visited in
- *    ascending order; the output is s_v acc / l, LSE = ln2 (m + log2(l) - 8).
+ *  - P is stored as E4M3(2^s p) with p = 2^(t - m) and s = 4, where m is the
+ *    reference max of the row: set by the first tile and moved to a tile's
+ *    max only when that max exceeds m by more than tau = 4 (log2 units), so
+ *    p <= 2^tau and 2^s p <= 256 stays in E4M3 range.  The running sum adds
+ *    the decoded rounded codes [SHR]; KV tiles of 128 keys are visited in
+ *    ascending order; the output is s_v acc / l, LSE = ln2 (m + log2(l) - s).
  *
  * Build: plain C11, no fast-math, no FP contraction (gcc -O2 -std=c11
  * -ffp-contract=off), so every float operation below rounds once, as written.
@@ -321,12 +324,13 @@ void orc_block_mean(const float *x, int g, int64_t ld, int d, float *qbar, float
  *   t_ij = S_ij * score_scale (log2 domain); masked keys are -inf:
  *        causal: key j > query i;  any: key j >= kv_len.
  *   Keys are split into chunks of `chunk` keys (0: one chunk); each chunk is
- *   visited in tiles of 128 keys in ascending order with its own running max
- *   m and sum l.  Per tile:
- *        m' = max(m, max_j t_ij),  alpha = 2^(m - m'),  p_ij = 2^(t_ij - m')
- *        P_ij = round_p ? E4M3(2^8 p_ij) : 2^8 p_ij
+ *   visited in tiles of 128 keys in ascending order with its own reference
+ *   max m and sum l.  Per tile, with M = max_j t_ij:
+ *        m' = M if m = -inf or M > m + tau, else m;  alpha = 2^(m - m')
+ *        p_ij = 2^(t_ij - m'),  P_ij = round_p ? E4M3(2^s p_ij) : 2^s p_ij
  *        l = alpha l + sum_j P_ij,  acc = alpha acc + sum_j P_ij v_j
- *   Chunk result: o_s = out_scale * acc / l, lse_s = ln2 (m + log2(l) - 8).
+ *   (tau = 0 is the FlashAttention-2 running max.)
+ *   Chunk result: o_s = out_scale * acc / l, lse_s = ln2 (m + log2(l) - s).
  *   Chunks combine by weights w_s = e^(lse_s - max lse):
  *        o = sum_s w_s o_s / sum_s w_s,  lse = max lse + ln(sum_s w_s).
  *   A row with no visible key gets o = 0, lse = -inf.
@@ -339,6 +343,7 @@ typedef struct {
     int causal;
     int64_t kv_len, chunk;
     int round_p;
+    double p_shift, tau;
     const int64_t *rows;
     double *o, *lse;
 } orc_attn_ctx;
@@ -383,13 +388,13 @@ static void orc_attn_row(int64_t ri, void *vctx)
                 if (t[j - ts] > tmax)
                     tmax = t[j - ts];
             }
-            double mn = m > tmax ? m : tmax;
+            double mn = (m == -INFINITY || tmax > m + c->tau) ? tmax : m;
             double alpha = (m == -INFINITY) ? 0.0 : exp2(m - mn);
             l *= alpha;
             for (int x = 0; x < d; x++)
                 acc[x] *= alpha;
             for (int64_t j = ts; j < te; j++) {
-                double p = ldexp(exp2(t[j - ts] - mn), 8);
+                double p = exp2(t[j - ts] - mn + c->p_shift);
                 if (c->round_p)
                     p = orc_e4m3_value(orc_e4m3_encode(p));
                 l += p;
@@ -401,7 +406,7 @@ static void orc_attn_row(int64_t ri, void *vctx)
         }
         for (int x = 0; x < d; x++)
             os[nsplit * d + x] = c->out_scale * acc[x] / l;
-        ls[nsplit] = M_LN2 * (m + log2(l) - 8.0);
+        ls[nsplit] = M_LN2 * (m + log2(l) - c->p_shift);
         if (ls[nsplit] > lse_max)
             lse_max = ls[nsplit];
         nsplit++;
@@ -431,11 +436,12 @@ static void orc_attn_row(int64_t ri, void *vctx)
 
 void orc_attn_online(const double *q, const double *qadd, const double *k, const double *v,
                      int64_t nq, int64_t nk, int d, double score_scale, double out_scale,
-                     int causal, int64_t kv_len, int64_t chunk, int round_p,
-                     const int64_t *rows, int64_t nrows, double *o, double *lse, int nthreads)
+                     int causal, int64_t kv_len, int64_t chunk, int round_p, double p_shift,
+                     double tau, const int64_t *rows, int64_t nrows, double *o, double *lse,
+                     int nthreads)
 {
     orc_attn_ctx c = {q, qadd, k, v, nq, nk, d, score_scale, out_scale, causal,
-                      kv_len, chunk, round_p, rows, o, lse};
+                      kv_len, chunk, round_p, p_shift, tau, rows, o, lse};
     orc_parallel_for(nrows, nthreads, orc_attn_row, &c);
 }
 

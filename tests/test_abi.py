@@ -62,3 +62,46 @@ def test_workspace_size_queries(lib):
     n0 = lib.mpfa_quantize_workspace_size(1, 256, 2, 0)
     n1 = lib.mpfa_quantize_workspace_size(1, 256, 2, 1)
     assert n1 - n0 == 2 * 2 * 128 * 4
+
+
+def _fake(addr):
+    return ctypes.c_void_p(addr)
+
+
+def test_host_validation_rejects_bad_shapes_and_pointers(lib):
+    """Every host-checkable fault returns before any CUDA call (these run
+    with no GPU: a call that passed validation would fail with MPFA_ERR_CUDA)."""
+    class NV(ctypes.Structure):
+        _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                    ("tensor_scale", ctypes.c_void_p)]
+
+    class F8(ctypes.Structure):
+        _fields_ = [("codes", ctypes.c_void_p), ("tensor_scale", ctypes.c_void_p)]
+
+    ok = 0x10000
+    q = NV(ok, ok, ok)
+    k = NV(ok, ok, ok)
+    v = F8(ok, ok)
+    f = lib.mpfa_prefill
+    f.restype = ctypes.c_int
+    R = ctypes.byref
+    # N not a multiple of 128
+    assert f(R(q), None, R(k), R(v), 1, 100, 4, 2, 128, 1, 0, 0, _fake(ok), None, None) == 1
+    # Hq % Hkv != 0
+    assert f(R(q), None, R(k), R(v), 1, 128, 5, 2, 128, 1, 0, 0, _fake(ok), None, None) == 1
+    # misaligned output
+    assert f(R(q), None, R(k), R(v), 1, 128, 4, 2, 128, 1, 0, 0, _fake(ok + 2), None, None) == 1
+    # compensation without its terms, and T out of range
+    assert f(R(q), None, R(k), R(v), 1, 128, 4, 2, 128, 1, 1, 2, _fake(ok), None, None) == 1
+    assert f(R(q), None, R(k), R(v), 1, 128, 4, 2, 128, 1, 1, 3, _fake(ok), None, None) == 2
+    d = lib.mpfa_decode
+    d.restype = ctypes.c_int
+    used = ctypes.c_int(0)
+    # kv_chunk not a multiple of 128; Lmax not a multiple of 128
+    assert d(_fake(ok), R(k), R(v), _fake(ok), 2, 8, 2, 128, 256, 1, 2, 100, _fake(ok), None,
+             None, None, R(used), _fake(ok), 1 << 20, None) == 1
+    assert d(_fake(ok), R(k), R(v), _fake(ok), 2, 8, 2, 128, 200, 1, 2, 0, _fake(ok), None,
+             None, None, R(used), _fake(ok), 1 << 20, None) == 1
+    # more than 16 query heads per KV head
+    assert d(_fake(ok), R(k), R(v), _fake(ok), 2, 64, 2, 128, 256, 1, 2, 0, _fake(ok), None,
+             None, None, R(used), _fake(ok), 1 << 20, None) == 2

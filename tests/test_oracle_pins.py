@@ -253,21 +253,64 @@ def test_qadd_is_added_to_every_score():
     np.testing.assert_allclose(l1, l2, atol=1e-10)
 
 
+P_SHIFT_READING = 4      # P stored as E4M3(2^4 p)
+TAU_READING = 4.0        # reference max moves when a tile max exceeds it by > 4
+
+
+def _e4m3(x):
+    return torch.from_numpy(np.asarray(x, np.float64)).to(torch.float8_e4m3fn).double().numpy()
+
+
 @pytest.mark.parametrize("n", [16, 64, 128])
 def test_single_tile_rounded_p_direct_formula(n):
-    """One KV tile: P8 = E4M3(2^8 2^(t - max t)) (torch's e4m3 cast),
-    O = sum P8 v / sum P8, LSE = ln2 (max t + log2 sum P8 - 8)."""
+    """One KV tile: P8 = E4M3(2^4 2^(t - max t)) (torch's e4m3 cast),
+    O = sum P8 v / sum P8, LSE = ln2 (max t + log2 sum P8 - 4)."""
+    assert orc.P_SHIFT == P_SHIFT_READING and orc.RESCALE_TAU == TAU_READING
     q, k, v = _rand_qkv(n, seed=100 + n, scale=1.3)
     o1, l1 = orc.attn_online(q, None, k, v, score_scale=LOG2E_RSQRT_D, out_scale=1.0,
                              causal=False, round_p=True)
     t = (q @ k.T) * LOG2E_RSQRT_D
     m = t.max(axis=1, keepdims=True)
-    p = np.exp2(t - m) * 256.0
-    p8 = torch.from_numpy(p).to(torch.float8_e4m3fn).double().numpy()
+    p8 = _e4m3(np.exp2(t - m) * 2.0 ** P_SHIFT_READING)
     o2 = (p8 @ v) / p8.sum(axis=1, keepdims=True)
-    l2 = math.log(2) * (m[:, 0] + np.log2(p8.sum(axis=1)) - 8)
+    l2 = math.log(2) * (m[:, 0] + np.log2(p8.sum(axis=1)) - P_SHIFT_READING)
     np.testing.assert_allclose(o1, o2, rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(l1, l2, atol=1e-12)
+
+
+@pytest.mark.parametrize("delta", [-3.0, 0.5, 3.9, 4.1, 7.0])
+def test_two_tile_reference_max_rule(delta):
+    """Two KV tiles whose maxima differ by delta (log2 units): the row's
+    reference max stays at tile 0's max while delta <= 4 (P of tile 1 then
+    reaches up to 2^(4+delta)), and moves to tile 1's max with the rescale
+    alpha = 2^-delta once delta > 4.  Checked against a direct formula."""
+    rng = np.random.default_rng(int(delta * 10) + 50)
+    t0 = rng.uniform(-6, 0, 128)
+    t0[5] = 0.0                                   # tile 0 max = 0
+    t1 = rng.uniform(-6, 0, 128) + delta
+    t1[77] = delta                                # tile 1 max = delta
+    tt = np.concatenate([t0, t1])
+    q = np.zeros((1, 128)); q[0, 0] = 1.0
+    k = np.zeros((256, 128)); k[:, 0] = tt        # score_scale 1: t_j = k_j[0]
+    v = rng.standard_normal((256, 128))
+    o1, l1 = orc.attn_online(q, None, k, v, score_scale=1.0, out_scale=1.0, causal=False)
+    s = 2.0 ** P_SHIFT_READING
+    if delta <= TAU_READING:
+        p8 = _e4m3(np.exp2(tt - 0.0) * s)
+        o2 = p8 @ v / p8.sum()
+        l2 = math.log(2) * (0.0 + math.log2(p8.sum()) - P_SHIFT_READING)
+        if delta > 0:
+            assert p8[128:].max() > s                # P above 2^s: the stale max is kept
+    else:
+        p0 = _e4m3(np.exp2(t0) * s)
+        p1 = _e4m3(np.exp2(t1 - delta) * s)
+        alpha = 2.0 ** -delta
+        acc = alpha * (p0 @ v[:128]) + p1 @ v[128:]
+        ell = alpha * p0.sum() + p1.sum()
+        o2 = acc / ell
+        l2 = math.log(2) * (delta + math.log2(ell) - P_SHIFT_READING)
+    np.testing.assert_allclose(o1[0], o2, rtol=1e-12, atol=1e-13)
+    assert abs(l1[0] - l2) < 1e-12
 
 
 def test_shared_rounding_rows_sum_to_one():
