@@ -110,6 +110,26 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest x over all ranks (x itself without a process group).  The
+    tensor lives on `device` for NCCL and on the host for gloo."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    on = "cpu" if dist.get_backend() == "gloo" or device is None else device
+    t = torch.tensor([float(x)], dtype=torch.float64, device=on)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(units_per_rank: float, ms_local: float, world: int, device=None):
+    """Whole-job rate of replicas that each process `units_per_rank` units:
+    the units of all ranks over the slowest rank's time.  Returns (rate in
+    units/s, the max-over-ranks ms)."""
+    ms = max_over_ranks(ms_local, device)
+    return world * units_per_rank / (ms * 1e-3), ms
+
+
 # ----------------------------------------------------------------------------
 # CPU oracle on a bounded sample (cpu_baseline and the reference arm)
 # ----------------------------------------------------------------------------
@@ -242,13 +262,9 @@ def run_gpu(args):
     step_ms = [e[0].elapsed_time(e[2]) for e in evs]
     quant_ms = [e[0].elapsed_time(e[1]) for e in evs]
     pre_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    ms = statistics.mean(step_ms)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
     flops = FLOP_PER_PAIR * cfg.pairs
-    value = ws * flops / (ms * 1e-3) / 1e12
+    rate, ms = aggregate_rate(flops, statistics.mean(step_ms), ws, dev)
+    value = rate / 1e12
 
     # prefill roofline: FP4 QK^T + FP8 PV against the measured bf16 peak times
     # the nominal dense ratios (FP4 = 6x, FP8 = 2x bf16)
@@ -318,13 +334,14 @@ def run_decode(mp, dev, stream, peaks, flush, args):
         mp.decode(q, cache, seqlens, out=out, lse=lse, workspace=ws_d)
         evs[i][1].record(stream)
     torch.cuda.synchronize()
-    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    ms_local = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     tokens = int(seqlens.long().sum().item())
     nbytes = tokens * cfg.Hkv * KV_BYTES_PER_TOKEN
-    gbs = nbytes / (ms * 1e-3) / 1e9
+    gbs = nbytes / (ms_local * 1e-3) / 1e9          # this replica's kernel rate (roofline)
+    job, ms = aggregate_rate(nbytes, ms_local, _dist()[0], dev)
     del cache
     return {"workload": cfg.name, "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "L": cfg.Lmax,
-            "value": gbs, "unit": "GB/s", "ms": ms, "chunk": res["chunk"],
+            "value": job / 1e9, "unit": "GB/s", "ms": ms, "chunk": res["chunk"],
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm"], "traffic": None,
                          "algorithmic_bytes": nbytes},
@@ -364,10 +381,11 @@ def run_e2e(mp, dev, stream, Q, K, V, args):
         step()
     t1.record(stream)
     torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1) / n
+    ws = _dist()[0]
     flops = FLOP_PER_PAIR * cfg.pairs
+    rate, ms = aggregate_rate(flops, t0.elapsed_time(t1) / n, ws, dev)
     h2d = (Q.numel() + K.numel() + V.numel()) * 2
-    return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+    return {"value": rate / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": Q.numel() * 2}
 
 

@@ -1,0 +1,59 @@
+"""bench.py's multi-rank logic on the host: world-size-2 gloo process groups
+(one process per rank, as torchrun launches them) check the max-over-ranks
+time and the whole-job rate of independent replicas, and that the reference
+arm runs on rank 0 only."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as tmp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms_local = 10.0 + 5.0 * rank                  # rank 1 is the slow one
+        mx = bench.max_over_ranks(ms_local)
+        rate, ms = bench.aggregate_rate(1e9, ms_local, world)
+        with open(os.path.join(out_dir, f"r{rank}.txt"), "w") as f:
+            f.write(f"{mx} {rate} {ms}\n")
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_aggregate_gloo(tmp_path):
+    world = 2
+    tmp.spawn(_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True)
+    rows = [open(tmp_path / f"r{r}.txt").read().split() for r in range(world)]
+    for mx, rate, ms in rows:
+        assert float(mx) == 15.0 and float(ms) == 15.0
+        # 2 replicas x 1e9 units in the slowest rank's 15 ms
+        assert float(rate) == pytest.approx(2e9 / 15e-3)
+
+
+def test_max_over_ranks_without_group():
+    assert bench.max_over_ranks(3.5) == 3.5
+    rate, ms = bench.aggregate_rate(100.0, 2.0, 1)
+    assert ms == 2.0 and rate == pytest.approx(5e4)
+
+
+def test_reference_arm_other_ranks_do_no_work(monkeypatch, capsys):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+
+    class Args:
+        steps, warmup, gpus = 1, 3, 2
+    assert bench.run_reference(Args()) is None
+    assert capsys.readouterr().out == ""
