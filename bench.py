@@ -66,6 +66,11 @@ class Clocks:
         self.proc = None
 
     def start(self):
+        """Start sampling; returns once the first sample has arrived (or after
+        a few seconds), so that the timed region that follows is covered."""
+        import threading
+        self.lines = []
+        first = threading.Event()
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
@@ -73,19 +78,31 @@ class Clocks:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return
+
+        def reader(proc=self.proc):
+            for line in proc.stdout:
+                self.lines.append(line)
+                first.set()
+            first.set()
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+        first.wait(5.0)
+        self.skip = len(self.lines)     # samples taken before the timed region
 
     def stop(self):
         if self.proc is None:
             return None
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
+            self.proc.wait()
+        self.thread.join(timeout=5)
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
+        for line in self.lines[self.skip:]:
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -287,7 +304,8 @@ def run_gpu(args):
     if rank == 0 and not args.no_cpu_baseline and args.only is None:
         try:
             Qc, Kc, Vc = Q.cpu(), K.cpu(), V.cpu()
-            v, dt, desc, thr = oracle_sample(Qc, Kc, Vc)
+            v, dt, desc, thr = oracle_sample(Qc, Kc, Vc, rows_per_head=384,
+                                             heads=tuple((0, h) for h in range(cfg.Hq)))
             cpu = {"value": v, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
                    "sample": desc, "seconds": dt}
         except Exception as ex:  # pragma: no cover - reported, not fatal
@@ -328,12 +346,15 @@ def run_decode(mp, dev, stream, peaks, flush, args):
     torch.cuda.synchronize()
     n = max(args.steps, 5)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    clocks = Clocks(dev.index)
+    clocks.start()
     for i in range(n):
         flush.zero_()
         evs[i][0].record(stream)
         mp.decode(q, cache, seqlens, out=out, lse=lse, workspace=ws_d)
         evs[i][1].record(stream)
     torch.cuda.synchronize()
+    clk = clocks.stop()
     ms_local = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     tokens = int(seqlens.long().sum().item())
     nbytes = tokens * cfg.Hkv * KV_BYTES_PER_TOKEN
@@ -345,7 +366,7 @@ def run_decode(mp, dev, stream, peaks, flush, args):
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm"], "traffic": None,
                          "algorithmic_bytes": nbytes},
-            "gpu_launches": 4 * n}
+            "gpu_launches": 4 * n, "clocks": clk}
 
 
 def run_e2e(mp, dev, stream, Q, K, V, args):
@@ -392,7 +413,7 @@ def run_e2e(mp, dev, stream, Q, K, V, args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

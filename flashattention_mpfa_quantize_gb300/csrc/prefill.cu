@@ -4,19 +4,23 @@
 // rank-one smoothing term (the T NVFP4 terms of the query-block mean, the
 // same row for all 128 rows) issued as extra MMAs into the same score
 // accumulator, an online softmax (FlashAttention-2 section of the
-// "FlashAttention压到4位" explainer), P converted to FP8 E4M3 in place in
-// tensor memory and multiplied by FP8 V on the tensor core.  The running sum
-// l is itself a tensor-core product of the rounded P codes with a ones tile,
-// so the denominator consumes exactly the codes the PV product consumes (the
-// explainer's Direct-P section states that rule).
+// "FlashAttention压到4位" explainer), P converted to FP8 E4M3 in tensor
+// memory and multiplied by FP8 V on the tensor core.  The running sum l comes
+// out of the same MMA: each V stage is followed in shared memory by a tile of
+// E4M3 ones that the PV product reads as 16 extra columns (N = 144), so the
+// denominator consumes exactly the codes the numerator consumes (the
+// explainer's Direct-P section states that rule) at no extra instruction.
 //
 // One CTA computes one 128-row query tile of one (batch, head):
 //   warp 8    TMA producer: Q tile once, then K / K-scale tiles through a
 //             ring of kKStages stages and V tiles through kVStages stages.
-//   warp 9    MMA issuer: block scales into TMEM (tcgen05.cp), QK^T and the
+//   warp 9    QK issuer: block scales into TMEM (tcgen05.cp), QK^T and the
 //             rank-one MMAs into score bank j % 2; once the softmax has read
-//             S_j and published P_j it issues PV_j and the row-sum MMA, then
-//             QK_{j+2} into the freed bank.
+//             S_j it issues QK_{j+2} into the freed bank.
+//   warp 10   PV issuer: once the softmax has published P_j, PV_j (with the
+//             row sum).  Two issuing threads on two schedulers: each tcgen05
+//             instruction costs a thread on the order of a hundred cycles
+//             while the softmax warps load the scheduler it shares.
 //   warps 0-7 softmax + correction + epilogue in two warpgroups: thread
 //             (row r, half h) owns keys 64h..64h+63 of query row r (TMEM lane
 //             r), so two warps share each scheduler.  The two halves of a row
@@ -24,10 +28,12 @@
 //             stores its 16 columns of E4M3 P over the scores, rescales its
 //             64 columns of O when the running max moves, and writes its half
 //             of the output row.
-// Tensor memory (512 columns): S0 [0,128) S1 [128,256) O [256,384)
-// P0 [384,416) P1 [416,448) L [448,464) scale factors [464,512).  P has its
-// own columns so the scores of tile j+2 can be computed into bank j % 2 as
-// soon as the softmax has read tile j, while PV_j still reads P_j.
+// Tensor memory (512 columns): S0 [0,128) S1 [128,256) O [256,384) and the
+// row sum l at 384 (columns [384,400) all hold l), P0 [416,448) P1 [448,480),
+// block scales: Q [400,408), K slot 0 [408,416), rank-one terms
+// [480,480+8T), K slots 1-2 [496,512).  P has its own columns so the scores
+// of tile j+2 can be computed into bank j % 2 as soon as the softmax has read
+// tile j, while PV_j still reads P_j.
 #include <cmath>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -45,31 +51,35 @@ namespace {
 constexpr int kKStages = 4;   // K tiles: released once QK has read them
 constexpr int kVStages = 3;   // V tiles: released once PV has read them
 constexpr int kSfSlots = 3;   // TMEM block-scale slots for K (slot j % 3)
-constexpr int kThreads = 320;
-constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr int kThreads = 352;
+constexpr int kWarpTma = 8, kWarpMma = 9, kWarpPv = 10;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kTmemCols = 512;
 
-constexpr uint32_t kColS0 = 0, kColO = 256, kColP0 = 384, kColL = 448, kColSfQ = 464,
-                   kColSfQb = 472, kColSfK = 488;
+constexpr uint32_t kColS0 = 0, kColO = 256, kColL = 384, kColP0 = 416, kColSfQ = 400,
+                   kColSfQb = 480;
+// K block-scale slot i (8 columns each, 4-aligned as the MMA requires)
+__device__ __forceinline__ uint32_t col_sf_k(int i) { return i == 0 ? 408u : 488u + 8u * i; }
 
 // shared memory layout (offsets from a 1024-byte aligned base)
 constexpr uint32_t kOffQ = 0;                           // 8 KB
 constexpr uint32_t kOffQb = kOffQ + 8192;               // 2 x 8 KB
 constexpr uint32_t kOffK = kOffQb + 2 * 8192;            // kKStages x 8 KB
-constexpr uint32_t kOffV = kOffK + kKStages * 8192;      // kVStages x 16 KB
-constexpr uint32_t kOffQs = kOffV + kVStages * 16384;    // 1 KB
-constexpr uint32_t kOffQbs = kOffQs + 1024;              // 2 x 1 KB
-constexpr uint32_t kOffKs = kOffQbs + 2048;              // kKStages x 1 KB
-constexpr uint32_t kOffOnes = kOffKs + kKStages * 1024;  // 2 KB
-constexpr uint32_t kOffRed = kOffOnes + 2048;          // 2 x 2 x 128 floats (row maxima)
+// V stage s: 16 KB of V at kOffV + 32 KB * s, then 16 KB of E4M3 ones (the
+// second 128-byte atom of the N = 144 operand, kVOnesLbo bytes further on)
+constexpr uint32_t kVStageBytes = 32768, kVOnesLbo = 16384;
+constexpr uint32_t kOffV = kOffK + kKStages * 8192;           // kVStages x 32 KB
+constexpr uint32_t kOffQs = kOffV + kVStages * kVStageBytes;  // 1 KB
+constexpr uint32_t kOffQbs = kOffQs + 1024;                   // 2 x 1 KB
+constexpr uint32_t kOffKs = kOffQbs + 2048;                   // kKStages x 1 KB
+constexpr uint32_t kOffRed = kOffKs + kKStages * 1024;  // 2 x 2 x 128 floats (row maxima)
 constexpr uint32_t kOffBar = kOffRed + 2048;
 constexpr uint32_t kNumBars = 9 + 2 * kKStages + 2 * kVStages;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemUsed = kOffMisc + 64;
-// Request more than half an SM's shared memory so a single CTA owns the
-// SM and its 512 TMEM columns.
-constexpr uint32_t kSmemBytes = 160 * 1024;
+// More than half an SM's shared memory, so a single CTA owns the SM and its
+// 512 TMEM columns.
+constexpr uint32_t kSmemBytes = 168 * 1024;
 static_assert(kSmemUsed + 1024 <= kSmemBytes, "shared memory layout overflow");
 
 // barrier indices
@@ -133,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarPReady0 + 1), kSoftmaxThreads);
     mbar_init(bar(kBarODone0), 1);
     mbar_init(bar(kBarODone0 + 1), 1);
-    mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarDrain), 2);   // one commit from each issuer
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(bar(kBarKFull0 + s), 1);
       mbar_init(bar(kBarKEmpty0 + s), 1);
@@ -182,7 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             !mbar_wait(bar(kBarVEmpty0 + s), ((j / kVStages) - 1) & 1, a.err, abort_flag))
           return false;
         mbar_expect_tx(bar(kBarVFull0 + s), 16384);
-        tma_load_2d(sbase + kOffV + s * 16384, &map_v, 0, kvrow0 + j * 128, bar(kBarVFull0 + s));
+        tma_load_2d(sbase + kOffV + s * kVStageBytes, &map_v, 0, kvrow0 + j * 128,
+                    bar(kBarVFull0 + s));
         v_issued = j + 1;
         return true;
       };
@@ -198,11 +209,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(bar(kBarVFull0 + j % kVStages), (j / kVStages) & 1, a.err, nullptr);
     }
   } else if (warp == kWarpMma) {
-    // ---------------- MMA issuer ----------------
+    // ---------------- QK issuer ----------------
     if (lane == 0) {
       const uint32_t id_qk = idesc_nvfp4(128, 128);
-      const uint32_t id_pv = idesc_fp8(128, 128, 0, 1);
-      const uint32_t id_l = idesc_fp8(128, 16, 0, 0);
       bool ok = mbar_wait(bar(kBarQFull), 0, a.err, abort_flag) &&
                 mbar_wait(bar(kBarQbReady), 0, a.err, abort_flag);
       if (ok) {
@@ -216,15 +225,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem + kColSfQb + 8 * t + 4 * kc,
                 smem_desc(sbase + kOffQbs + 1024 * t + 512 * kc, 128, 128, kSwizzleNone));
       }
-      const uint64_t ones = smem_desc(sbase + kOffOnes, 128, 256, kSwizzleNone);
       // QK_j (and the rank-one MMAs) into score bank j % 2
       auto issue_qk = [&](int j) -> bool {
         const int s = j % kKStages, bk = j & 1;
         if (!mbar_wait(bar(kBarKFull0 + s), (j / kKStages) & 1, a.err, abort_flag)) return false;
         tc_fence_after();
         // slot j % 3: its last reader, QK_{j-3}, completed before the softmax
-        // of tile j-1 read its scores, which this issue waited for
-        const uint32_t sfk = tmem + kColSfK + 8 * (j % kSfSlots);
+        // of tile j-2 read its scores, which this issue waited for
+        const uint32_t sfk = tmem + col_sf_k(j % kSfSlots);
         for (int kc = 0; kc < 2; ++kc)
           tmem_cp_32x128b_x4(sfk + 4 * kc,
                              smem_desc(sbase + kOffKs + 1024 * s + 512 * kc, 128, 128, kSwizzleNone));
@@ -243,31 +251,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j + kKStages < nkv) tc_commit(bar(kBarKEmpty0 + s));
         return true;
       };
-      // PV_j and the row-sum MMA (P from P bank j % 2, V from stage j % kVStages)
-      auto issue_pv = [&](int j) -> bool {
+      if (ok) ok = issue_qk(0) && (nkv < 2 || issue_qk(1));
+      for (int j = 0; ok && j + 2 < nkv; ++j) {
+        // the softmax has read S_j: bank j % 2 is free
+        if (!mbar_wait(bar(kBarPReady0 + (j & 1)), (j >> 1) & 1, a.err, abort_flag)) break;
+        if (!issue_qk(j + 2)) break;
+      }
+      // drain this thread's tensor-core work before the CTA releases TMEM
+      tc_commit(bar(kBarDrain));
+      mbar_wait(bar(kBarDrain), 0, a.err, nullptr);
+    }
+  } else if (warp == kWarpPv) {
+    // ---------------- PV issuer ----------------
+    if (lane == 0) {
+      const uint32_t id_pv = idesc_fp8(128, 144, 0, 1);   // 128 V columns + 16 ones
+      for (int j = 0; j < nkv; ++j) {
         const int bp = j & 1, sp = j % kVStages;
-        if (!mbar_wait(bar(kBarVFull0 + sp), (j / kVStages) & 1, a.err, abort_flag)) return false;
+        // the softmax has published P_j in P bank j % 2
+        if (!mbar_wait(bar(kBarPReady0 + bp), (j >> 1) & 1, a.err, abort_flag)) break;
+        if (!mbar_wait(bar(kBarVFull0 + sp), (j / kVStages) & 1, a.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t pcol = tmem + kColP0 + 32 * bp;
-        const uint32_t vaddr = sbase + kOffV + sp * 16384;
+        const uint32_t vaddr = sbase + kOffV + sp * kVStageBytes;
         for (int kk = 0; kk < 4; ++kk)
           mma_fp8_ts(tmem + kColO, pcol + 8 * kk,
-                     smem_desc(vaddr + 4096 * kk, 16, 1024, kSwizzle128B), id_pv,
+                     smem_desc(vaddr + 4096 * kk, kVOnesLbo, 1024, kSwizzle128B), id_pv,
                      (j > 0 || kk > 0) ? 1u : 0u);
-        for (int kk = 0; kk < 4; ++kk)
-          mma_fp8_ts(tmem + kColL, pcol + 8 * kk, ones, id_l, (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(bar(kBarODone0 + bp));
         if (j + kVStages < nkv) tc_commit(bar(kBarVEmpty0 + sp));
-        return true;
-      };
-      if (ok) ok = issue_qk(0) && (nkv < 2 || issue_qk(1));
-      for (int j = 0; ok && j < nkv; ++j) {
-        // softmax(j) has read S_j (bank j % 2 is free) and written P_j
-        if (!mbar_wait(bar(kBarPReady0 + (j & 1)), (j >> 1) & 1, a.err, abort_flag)) break;
-        if (!issue_pv(j)) break;
-        if (j + 2 < nkv && !issue_qk(j + 2)) break;
       }
-      // drain the tensor pipe before the CTA releases TMEM
       tc_commit(bar(kBarDrain));
       mbar_wait(bar(kBarDrain), 0, a.err, nullptr);
     }
@@ -295,9 +307,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         reinterpret_cast<uint32_t*>(smem + kOffQbs + 1024 * t)[row] = w0;
         reinterpret_cast<uint32_t*>(smem + kOffQbs + 1024 * t + 512)[row] = w1;
       }
-      // ones tile (E4M3 1.0 = 0x38) for the row-sum MMA
-      reinterpret_cast<uint4*>(smem + kOffOnes)[row] =
-          make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
+    }
+    // the ones atoms beside the V stages (E4M3 1.0 = 0x38; every byte equal,
+    // so the 128-byte swizzle leaves them unchanged)
+    for (int s = 0; s < kVStages; ++s) {
+      uint4* ones = reinterpret_cast<uint4*>(smem + kOffV + s * kVStageBytes + kVOnesLbo);
+      for (int i = threadIdx.x; i < (int)(kVOnesLbo / 16); i += kSoftmaxThreads)
+        ones[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
     }
     fence_proxy_async_smem();
     mbar_arrive(bar(kBarQbReady));
@@ -364,8 +380,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  ex2(fmaf(__uint_as_float(sr[c][4 * w + 1]), cs, bias)),
                                  ex2(fmaf(__uint_as_float(sr[c][4 * w + 2]), cs, bias)),
                                  ex2(fmaf(__uint_as_float(sr[c][4 * w + 3]), cs, bias)));
-      // P bank j % 2 was last read by PV_{j-2}, which completed before S_j
-      // did: the MMA warp issues QK_j after PV_{j-2} and S_j's commit tracks it.
+      // P bank j % 2 was last read by PV_{j-2}: wait for it to complete.
+      // ODone[bk] cannot be a phase further on: PV_j needs this tile's P.
+      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar(kBarODone0 + bk), ((j - 2) >> 1) & 1,
+                                                        a.err, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
       tmem_st16(tmem + lane_off + kColP0 + 32 * bk + 16 * half, pw);
       // correction: O (this half's 64 columns) and L scale by alpha once
       // PV_{j-1} has landed
