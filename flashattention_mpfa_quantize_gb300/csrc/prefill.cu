@@ -15,19 +15,19 @@
 //   warp 8    TMA producer: Q tile once, then K / K-scale tiles through a
 //             ring of kKStages stages and V tiles through kVStages stages.
 //   warp 9    QK issuer: block scales into TMEM (tcgen05.cp), QK^T and the
-//             rank-one MMAs into score bank j % 2; once the softmax has read
-//             S_j it issues QK_{j+2} into the freed bank.
+//             rank-one MMAs into score bank j % 2, QK_{j+2} as soon as the
+//             softmax has loaded S_j into registers.
 //   warp 10   PV issuer: once the softmax has published P_j, PV_j (with the
 //             row sum).  Two issuing threads on two schedulers: each tcgen05
 //             instruction costs a thread on the order of a hundred cycles
 //             while the softmax warps load the scheduler it shares.
-//   warps 0-7 softmax + correction + epilogue in two warpgroups: thread
-//             (row r, half h) owns keys 64h..64h+63 of query row r (TMEM lane
-//             r), so two warps share each scheduler.  The two halves of a row
-//             exchange their partial maxima through shared memory; each
-//             stores its 16 columns of E4M3 P over the scores, rescales its
-//             64 columns of O when the running max moves, and writes its half
-//             of the output row.
+//   warps 0-7 softmax + correction + epilogue.  Warp w owns TMEM lanes
+//             32(w%4)..32(w%4)+31 (query rows) for the KV tiles of parity
+//             w/4: thread = one query row, all 128 keys of its tiles.  The two
+//             warps on a scheduler thus alternate tiles, so one's
+//             exponentials overlap the other's loads, maxima and stores; the
+//             only exchange is the row's reference max, handed from the
+//             owner of tile j to the owner of tile j+1 through shared memory.
 // Tensor memory (512 columns): S0 [0,128) S1 [128,256) O [256,384) and the
 // row sum l at 384 (columns [384,400) all hold l), P0 [416,448) P1 [448,480),
 // block scales: Q [400,408), K slot 0 [408,416), rank-one terms
@@ -48,18 +48,34 @@ bool make_map_2d_u8(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint
 
 namespace {
 
-constexpr int kKStages = 4;   // K tiles: released once QK has read them
+constexpr int kKStages = 4;   // K tiles: released once the softmax has loaded S
 constexpr int kVStages = 3;   // V tiles: released once PV has read them
 constexpr int kSfSlots = 3;   // TMEM block-scale slots for K (slot j % 3)
 constexpr int kThreads = 352;
 constexpr int kWarpTma = 8, kWarpMma = 9, kWarpPv = 10;
 constexpr int kSoftmaxThreads = 256;
+constexpr int kTileThreads = 128;   // softmax threads that own one KV tile
 constexpr int kTmemCols = 512;
 
 constexpr uint32_t kColS0 = 0, kColO = 256, kColL = 384, kColP0 = 416, kColSfQ = 400,
                    kColSfQb = 480;
 // K block-scale slot i (8 columns each, 4-aligned as the MMA requires)
 __device__ __forceinline__ uint32_t col_sf_k(int i) { return i == 0 ? 408u : 488u + 8u * i; }
+
+// barrier indices
+enum : int {
+  kBarQFull = 0,
+  kBarQbReady = 1,
+  kBarSFull0 = 2,                      // +bank: scores of tile j in bank j % 2
+  kBarPReady0 = 4,                     // +bank: P_j published in P bank j % 2
+  kBarDrain = 6,
+  kBarSRead0 = 7,                      // +K stage: S_j (K stage j % 4) loaded by the softmax
+  kBarKFull0 = kBarSRead0 + kKStages,  // +K stage
+  kBarVFull0 = kBarKFull0 + kKStages,  // +V stage
+  kBarODone0 = kBarVFull0 + kVStages,  // +V stage: PV_j (V stage j % 3) completed
+  kBarMax0 = kBarODone0 + kVStages,    // +2*quadrant+parity: reference max handed to that parity
+  kNumBars = kBarMax0 + 8,
+};
 
 // shared memory layout (offsets from a 1024-byte aligned base)
 constexpr uint32_t kOffQ = 0;                           // 8 KB
@@ -72,29 +88,14 @@ constexpr uint32_t kOffV = kOffK + kKStages * 8192;           // kVStages x 32 K
 constexpr uint32_t kOffQs = kOffV + kVStages * kVStageBytes;  // 1 KB
 constexpr uint32_t kOffQbs = kOffQs + 1024;                   // 2 x 1 KB
 constexpr uint32_t kOffKs = kOffQbs + 2048;                   // kKStages x 1 KB
-constexpr uint32_t kOffRed = kOffKs + kKStages * 1024;  // 2 x 2 x 128 floats (row maxima)
-constexpr uint32_t kOffBar = kOffRed + 2048;
-constexpr uint32_t kNumBars = 9 + 2 * kKStages + 2 * kVStages;
+constexpr uint32_t kOffMax = kOffKs + kKStages * 1024;        // 128 floats: reference max per row
+constexpr uint32_t kOffBar = kOffMax + 512;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemUsed = kOffMisc + 64;
 // More than half an SM's shared memory, so a single CTA owns the SM and its
 // 512 TMEM columns.
 constexpr uint32_t kSmemBytes = 168 * 1024;
 static_assert(kSmemUsed + 1024 <= kSmemBytes, "shared memory layout overflow");
-
-// barrier indices
-enum : int {
-  kBarQFull = 0,
-  kBarQbReady = 1,
-  kBarSFull0 = 2,   // +bank: scores of tile j in bank j % 2
-  kBarPReady0 = 4,  // +bank: softmax has read S_j and written P_j
-  kBarODone0 = 6,   // +bank: PV_j (reading P bank j % 2) has completed
-  kBarDrain = 8,
-  kBarKFull0 = 9,                          // +K stage
-  kBarKEmpty0 = 9 + kKStages,              // +K stage
-  kBarVFull0 = 9 + 2 * kKStages,           // +V stage
-  kBarVEmpty0 = 9 + 2 * kKStages + kVStages,  // +V stage
-};
 
 struct Params {
   PrefillArgs a;
@@ -137,21 +138,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     mbar_init(bar(kBarQFull), 1);
     mbar_init(bar(kBarQbReady), kSoftmaxThreads);
-    mbar_init(bar(kBarSFull0), 1);
-    mbar_init(bar(kBarSFull0 + 1), 1);
-    mbar_init(bar(kBarPReady0), kSoftmaxThreads);
-    mbar_init(bar(kBarPReady0 + 1), kSoftmaxThreads);
-    mbar_init(bar(kBarODone0), 1);
-    mbar_init(bar(kBarODone0 + 1), 1);
+    for (int b2 = 0; b2 < 2; ++b2) {
+      mbar_init(bar(kBarSFull0 + b2), 1);
+      mbar_init(bar(kBarPReady0 + b2), kTileThreads);
+    }
     mbar_init(bar(kBarDrain), 2);   // one commit from each issuer
     for (int s = 0; s < kKStages; ++s) {
+      mbar_init(bar(kBarSRead0 + s), kTileThreads);
       mbar_init(bar(kBarKFull0 + s), 1);
-      mbar_init(bar(kBarKEmpty0 + s), 1);
     }
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(bar(kBarVFull0 + s), 1);
-      mbar_init(bar(kBarVEmpty0 + s), 1);
+      mbar_init(bar(kBarODone0 + s), 1);
     }
+    for (int i = 0; i < 8; ++i) mbar_init(bar(kBarMax0 + i), 32);
     fence_barrier_init();
   }
   if (warp == kWarpMma) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -176,8 +176,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int k_issued = 0, v_issued = 0;
       auto load_k = [&](int j) -> bool {
         const int s = j % kKStages;
+        // stage s held K_{j-4}: free once the softmax has loaded S_{j-4}
         if (j >= kKStages &&
-            !mbar_wait(bar(kBarKEmpty0 + s), ((j / kKStages) - 1) & 1, a.err, abort_flag))
+            !mbar_wait(bar(kBarSRead0 + s), ((j / kKStages) - 1) & 1, a.err, abort_flag))
           return false;
         const int row = kvrow0 + j * 128;
         mbar_expect_tx(bar(kBarKFull0 + s), 8192 + 1024);
@@ -188,8 +189,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto load_v = [&](int j) -> bool {
         const int s = j % kVStages;
+        // stage s held V_{j-3}: free once PV_{j-3} has completed
         if (j >= kVStages &&
-            !mbar_wait(bar(kBarVEmpty0 + s), ((j / kVStages) - 1) & 1, a.err, abort_flag))
+            !mbar_wait(bar(kBarODone0 + s), ((j / kVStages) - 1) & 1, a.err, abort_flag))
           return false;
         mbar_expect_tx(bar(kBarVFull0 + s), 16384);
         tma_load_2d(sbase + kOffV + s * kVStageBytes, &map_v, 0, kvrow0 + j * 128,
@@ -230,8 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = j % kKStages, bk = j & 1;
         if (!mbar_wait(bar(kBarKFull0 + s), (j / kKStages) & 1, a.err, abort_flag)) return false;
         tc_fence_after();
-        // slot j % 3: its last reader, QK_{j-3}, completed before the softmax
-        // of tile j-2 read its scores, which this issue waited for
+        // slot j % 3: its last reader, QK_{j-3}, completed before QK_{j-2},
+        // whose scores the softmax has loaded (this issue waited for that)
         const uint32_t sfk = tmem + col_sf_k(j % kSfSlots);
         for (int kc = 0; kc < 2; ++kc)
           tmem_cp_32x128b_x4(sfk + 4 * kc,
@@ -248,14 +250,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                          smem_desc(kaddr + 32 * kc, 16, 512, kSwizzle64B), id_qk,
                          tmem + kColSfQb + 8 * t + 4 * kc, sfk + 4 * kc, 1u);
         tc_commit(bar(kBarSFull0 + bk));
-        if (j + kKStages < nkv) tc_commit(bar(kBarKEmpty0 + s));
         return true;
       };
       if (ok) ok = issue_qk(0) && (nkv < 2 || issue_qk(1));
-      for (int j = 0; ok && j + 2 < nkv; ++j) {
-        // the softmax has read S_j: bank j % 2 is free
-        if (!mbar_wait(bar(kBarPReady0 + (j & 1)), (j >> 1) & 1, a.err, abort_flag)) break;
-        if (!issue_qk(j + 2)) break;
+      for (int j = 2; ok && j < nkv; ++j) {
+        // the softmax has loaded S_{j-2}: bank j % 2 is free.  SRead for
+        // stage (j-2) % 4 cannot be a phase further on: that needs S_{j+2}.
+        if (!mbar_wait(bar(kBarSRead0 + (j - 2) % kKStages), ((j - 2) / kKStages) & 1, a.err,
+                       abort_flag))
+          break;
+        if (!issue_qk(j)) break;
       }
       // drain this thread's tensor-core work before the CTA releases TMEM
       tc_commit(bar(kBarDrain));
@@ -277,15 +281,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_fp8_ts(tmem + kColO, pcol + 8 * kk,
                      smem_desc(vaddr + 4096 * kk, kVOnesLbo, 1024, kSwizzle128B), id_pv,
                      (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(bar(kBarODone0 + bp));
-        if (j + kVStages < nkv) tc_commit(bar(kBarVEmpty0 + sp));
+        tc_commit(bar(kBarODone0 + sp));
       }
       tc_commit(bar(kBarDrain));
       mbar_wait(bar(kBarDrain), 0, a.err, nullptr);
     }
   } else {
     // ---------------- softmax / correction / epilogue ----------------
-    const int half = warp >> 2;              // 0: keys 0..63, 1: keys 64..127
+    const int half = warp >> 2;              // prologue split; afterwards the tile parity
     const int row = threadIdx.x & 127;       // query row = TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     // Rank-one operand tiles: every row holds the block's term t (same 64
@@ -318,88 +321,98 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async_smem();
     mbar_arrive(bar(kBarQbReady));
 
-    float* red = reinterpret_cast<float*>(smem + kOffRed);  // [2 buffers][2 halves][128 rows]
-    const int pair_bar = 1 + (warp & 3);                     // warps w and w + 4
+    // Tiles j = par, par + 2, ... of this warp; the owner of tile j hands
+    // the row's reference max m_j to the owner of tile j+1 (bar kBarMax0 +
+    // 2*quadrant + receiving parity; one hand-over per phase, and a phase
+    // cannot run ahead because the next hand-over needs the reply).
+    const int par = half, quad = warp & 3;
+    float* mrow = reinterpret_cast<float*>(smem + kOffMax);
+    const uint32_t bar_in = bar(kBarMax0 + 2 * quad + par);
+    const uint32_t bar_out = bar(kBarMax0 + 2 * quad + (par ^ 1));
     const float cs = __fmul_rn(__fmul_rn(*a.s_q, *a.s_k), p.log2e_rsqrt_d);
     float m = -INFINITY;
     bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      const int bk = j & 1;
-      if (!__all_sync(0xffffffffu,
-                      mbar_wait(bar(kBarSFull0 + bk), (j >> 1) & 1, a.err, abort_flag))) {
+    for (int j = par; j < nkv; j += 2) {
+      const int bk = par;   // == j & 1
+      const int it = j >> 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarSFull0 + bk), it & 1, a.err, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
       const uint32_t sS = tmem + lane_off + kColS0 + 128 * bk;
-      uint32_t sr[2][32];
-      tmem_ld32(sS + 64 * half, sr[0]);
-      tmem_ld32(sS + 64 * half + 32, sr[1]);
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(sS + 32 * c, sr[c]);
       tmem_ld_wait();
+      // S_j is in registers: bank j % 2 and K stage j % 4 may be reused
+      tc_fence_before();
+      mbar_arrive(bar(kBarSRead0 + j % kKStages));
       if (a.causal && j == qt) {  // diagonal tile: key > row is masked
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (64 * half + 32 * c + i > row) sr[c][i] = 0xFF800000u;  // -inf
+            if (32 * c + i > row) sr[c][i] = 0xFF800000u;  // -inf
       }
-      // partial max over this thread's 64 keys (a tree of 3-input max)
-      float pm[11];
+      // tile max over the row's 128 keys (3-input max tree)
+      float pm[16];
 #pragma unroll
-      for (int k = 0; k < 10; ++k) {
-        const int e = 6 * k;
+      for (int k = 0; k < 16; ++k) {
+        const int e = 8 * k;
         pm[k] = fmax3(fmax3(__uint_as_float(sr[e >> 5][e & 31]),
-                            __uint_as_float(sr[(e + 1) >> 5][(e + 1) & 31]),
-                            __uint_as_float(sr[(e + 2) >> 5][(e + 2) & 31])),
-                      __uint_as_float(sr[(e + 3) >> 5][(e + 3) & 31]),
-                      fmaxf(__uint_as_float(sr[(e + 4) >> 5][(e + 4) & 31]),
-                            __uint_as_float(sr[(e + 5) >> 5][(e + 5) & 31])));
+                            __uint_as_float(sr[e >> 5][(e + 1) & 31]),
+                            __uint_as_float(sr[e >> 5][(e + 2) & 31])),
+                      fmax3(__uint_as_float(sr[e >> 5][(e + 3) & 31]),
+                            __uint_as_float(sr[e >> 5][(e + 4) & 31]),
+                            __uint_as_float(sr[e >> 5][(e + 5) & 31])),
+                      fmaxf(__uint_as_float(sr[e >> 5][(e + 6) & 31]),
+                            __uint_as_float(sr[e >> 5][(e + 7) & 31])));
       }
-      pm[10] = fmax3(fmax3(__uint_as_float(sr[1][28]), __uint_as_float(sr[1][29]),
-                           __uint_as_float(sr[1][30])),
-                     __uint_as_float(sr[1][31]), -INFINITY);
-      const float lmax = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]),
-                               fmax3(fmax3(pm[6], pm[7], pm[8]), pm[9], pm[10]));
-      float* rb = red + 256 * bk;
-      rb[128 * half + row] = lmax;
-      named_bar_sync(pair_bar, 64);
-      const float smax = fmaxf(lmax, rb[128 * (half ^ 1) + row]);
+      const float smax = fmax3(fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]),
+                                     fmax3(pm[6], pm[7], pm[8])),
+                               fmax3(pm[9], pm[10], pm[11]),
+                               fmax3(fmax3(pm[12], pm[13], pm[14]), pm[15], -INFINITY));
+      // reference max of the row after tile j-1, from that tile's owner
+      if (j > 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_in, ((j - 1) >> 1) & 1, a.err, abort_flag))) {
+          ok = false;
+          break;
+        }
+        m = mrow[row];
+      }
       // cs > 0, so max_i(S_i * cs) == (max_i S_i) * cs exactly.  The reference
       // max moves only when the tile max exceeds it by more than kRescaleTau,
       // so O and L rarely need a rescale once the first tiles are done.
       const float tmax = __fmul_rn(smax, cs);
       const float mn = (m == -INFINITY || tmax > m + kRescaleTau) ? tmax : m;
+      if (j + 1 < nkv) {
+        mrow[row] = mn;
+        mbar_arrive(bar_out);
+      }
       const float alpha = (m == -INFINITY) ? 0.0f : (mn == m ? 1.0f : ex2(m - mn));
       const float bias = kPShift - mn;  // P8 = E4M3(2^(t - m) * 2^kPShift)
-      uint32_t pw[16];
+      uint32_t pw[32];
 #pragma unroll
-      for (int c = 0; c < 2; ++c)
+      for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int w = 0; w < 8; ++w)
           pw[8 * c + w] = e4m3x4(ex2(fmaf(__uint_as_float(sr[c][4 * w]), cs, bias)),
                                  ex2(fmaf(__uint_as_float(sr[c][4 * w + 1]), cs, bias)),
                                  ex2(fmaf(__uint_as_float(sr[c][4 * w + 2]), cs, bias)),
                                  ex2(fmaf(__uint_as_float(sr[c][4 * w + 3]), cs, bias)));
-      // P bank j % 2 was last read by PV_{j-2}: wait for it to complete.
-      // ODone[bk] cannot be a phase further on: PV_j needs this tile's P.
-      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar(kBarODone0 + bk), ((j - 2) >> 1) & 1,
-                                                        a.err, abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      tmem_st16(tmem + lane_off + kColP0 + 32 * bk + 16 * half, pw);
-      // correction: O (this half's 64 columns) and L scale by alpha once
-      // PV_{j-1} has landed
+      // correction: O and L scale by alpha once PV_{j-1} has landed (PV_j is
+      // issued only after this tile's P is published)
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarODone0 + ((j - 1) & 1)),
-                                               ((j - 1) >> 1) & 1, a.err, abort_flag))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarODone0 + (j - 1) % kVStages),
+                                               ((j - 1) / kVStages) & 1, a.err, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t oO = tmem + lane_off + kColO + 64 * half;
-        for (int c = 0; c < 2; ++c) {
+        const uint32_t oO = tmem + lane_off + kColO;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
           tmem_ld32(oO + 32 * c, o);
           tmem_ld_wait();
@@ -407,22 +420,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
           tmem_st32(oO + 32 * c, o);
         }
-        if (half == 0) {
-          uint32_t l4[4];
-          tmem_ld4(tmem + lane_off + kColL, l4);
-          tmem_ld_wait();
-          l4[0] = __float_as_uint(__uint_as_float(l4[0]) * alpha);
-          tmem_st4(tmem + lane_off + kColL, l4);
-        }
+        uint32_t l4[4];
+        tmem_ld4(tmem + lane_off + kColL, l4);
+        tmem_ld_wait();
+        l4[0] = __float_as_uint(__uint_as_float(l4[0]) * alpha);
+        tmem_st4(tmem + lane_off + kColL, l4);
       }
+      // P bank j % 2 was last read by PV_{j-2}: wait for it to complete
+      // (its ODone phase cannot be overtaken: PV_{j+1} needs this P first).
+      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar(kBarODone0 + (j - 2) % kVStages),
+                                                        ((j - 2) / kVStages) & 1, a.err,
+                                                        abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_st32(tmem + lane_off + kColP0 + 32 * bk, pw);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(kBarPReady0 + bk));
       m = mn;
     }
-    if (ok && nkv > 0 &&
-        __all_sync(0xffffffffu, mbar_wait(bar(kBarODone0 + ((nkv - 1) & 1)), ((nkv - 1) >> 1) & 1,
-                                          a.err, abort_flag))) {
+    // epilogue: the owner of the last tile holds the final reference max
+    if (ok && nkv > 0 && par == ((nkv - 1) & 1) &&
+        __all_sync(0xffffffffu, mbar_wait(bar(kBarODone0 + (nkv - 1) % kVStages),
+                                          ((nkv - 1) / kVStages) & 1, a.err, abort_flag))) {
       tc_fence_after();
       uint32_t l4[4];
       tmem_ld4(tmem + lane_off + kColL, l4);
@@ -431,11 +453,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float sc = __fdiv_rn(*a.s_v, l);
       const size_t grow = (size_t)qt * 128 + row;
       uint4* out = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) +
-                                            (((size_t)b * a.N + grow) * a.Hq + h) * 128 +
-                                            64 * half);
-      for (int c = 0; c < 2; ++c) {
+                                            (((size_t)b * a.N + grow) * a.Hq + h) * 128);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_off + kColO + 64 * half + 32 * c, o);
+        tmem_ld32(tmem + lane_off + kColO + 32 * c, o);
         tmem_ld_wait();
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
@@ -449,9 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           out[4 * c + q4] = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
-      if (a.lse && half == 0)
-        a.lse[(size_t)bh * a.N + grow] =
-            0.69314718055994531f * (m + __log2f(l) - kPShift);
+      if (a.lse)
+        a.lse[(size_t)bh * a.N + grow] = 0.69314718055994531f * (m + __log2f(l) - kPShift);
     }
   }
 
