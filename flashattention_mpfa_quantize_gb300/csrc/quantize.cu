@@ -22,7 +22,9 @@
 namespace mpfa {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 128;        // quant_kernel
+constexpr int kStatsThreads = 512;   // stats_kernel: 32 row groups x 16 column groups
+constexpr int kRowGroups = kStatsThreads / 16, kRowsPerThread = 128 / kRowGroups;
 constexpr float kNvfp4Max = 2688.0f;  // 6 * 448
 constexpr float kFp8Max = 448.0f;
 
@@ -98,7 +100,7 @@ __device__ __forceinline__ unsigned block_max_u32(unsigned v, unsigned* red) {
   if (l == 0) red[w] = v;
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int i = 1; i < kThreads / 32; ++i) v = max(v, red[i]);
+    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) v = max(v, red[i]);
   }
   __syncthreads();
   return v;
@@ -109,8 +111,8 @@ __device__ __forceinline__ unsigned block_max_u32(unsigned v, unsigned* red) {
 __device__ void amax_bf16(const uint4* p, size_t n8, int b0, int nblk, unsigned* out,
                           unsigned* red) {
   unsigned m = 0;
-  for (size_t i = (size_t)(blockIdx.x - b0) * kThreads + threadIdx.x; i < n8;
-       i += (size_t)nblk * kThreads) {
+  for (size_t i = (size_t)(blockIdx.x - b0) * blockDim.x + threadIdx.x; i < n8;
+       i += (size_t)nblk * blockDim.x) {
     uint4 a = __ldg(p + i);
     m = __vmaxu2(m, a.x & 0x7FFF7FFFu);
     m = __vmaxu2(m, a.y & 0x7FFF7FFFu);
@@ -126,10 +128,12 @@ __device__ void amax_bf16(const uint4* p, size_t n8, int b0, int nblk, unsigned*
 // pass 1
 // ---------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(kThreads) stats_kernel(QuantArgs a, int nq_blocks,
-                                                         int nk_blocks, int nv_blocks) {
-  __shared__ unsigned red[kThreads / 32];
-  __shared__ double part[8][128];
+__global__ void __launch_bounds__(kStatsThreads, 2) stats_kernel(QuantArgs a, int nq_blocks,
+                                                                 int nk_blocks, int nv_blocks) {
+  __shared__ unsigned red[kStatsThreads / 32];
+  __shared__ long long ipart[kRowGroups][128];   // per row group: column partial sums (also emax)
+  __shared__ int col_emax[128];
+  __shared__ int col_bad[128];
   __shared__ float qb[128];
   int bid = blockIdx.x;
   if (bid < nq_blocks) {
@@ -138,105 +142,118 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(QuantArgs a, int nq_blo
       amax_bf16(reinterpret_cast<const uint4*>(a.q), n8, 0, nq_blocks, &a.amax[0], red);
       return;
     }
-    // One CTA per (b, h, 128-row block).  Each column sum is computed
-    // exactly in integers: a bf16 value is M * 2^(e - 134) (M < 256); scaled
-    // to units of 2^(emax - 182), where emax is the column's largest
-    // exponent, every term is an integer below 2^56 and 128 of them fit an
-    // int64.  The sum then rounds once to fp32 (exact scaling by 2^k), i.e.
-    // the mean is the fp32 rounding of the exact mean.  A column whose values
-    // span more than 2^48 (or whose mean would be subnormal) takes an fp64
-    // path with a compensation term instead.
-    int nblk = a.Nq / 128;
-    int blk = bid % nblk;
-    int bh = bid / nblk;
-    int h = bh % a.Hq, b = bh / a.Hq;
-    int cg = threadIdx.x & 15, rg = threadIdx.x >> 4;
+    // Persistent over the (b, h, 128-row block) units, the next unit's rows
+    // loaded while the current one is reduced.  Thread = kRowsPerThread rows
+    // (row group rg) x 8 columns (column group cg).  Each column sum is
+    // computed exactly in integers: a bf16 value is M * 2^(e - 134)
+    // (M < 256); scaled to units of 2^(emax - 182), where emax is the
+    // column's largest exponent, every term is an integer below 2^56 and 128
+    // of them fit an int64.  The sum then rounds once to fp32 (exact scaling
+    // by 2^k), i.e. the mean is the fp32 rounding of the exact mean.  A
+    // column whose values span more than 2^48 (or whose mean would be
+    // subnormal) takes an fp64 path with a compensation term instead.
+    const int nblk = a.Nq / 128;
+    const int units = a.B * a.Hq * nblk;
+    const int cg = threadIdx.x & 15, rg = threadIdx.x >> 4;
     const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(a.q);
-    uint32_t w[16][4];
+    auto load_unit = [&](int unit, uint32_t (&w)[kRowsPerThread][4]) {
+      const int blk = unit % nblk, bh = unit / nblk;
+      const int h = bh % a.Hq, b = bh / a.Hq;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      size_t n = (size_t)blk * 128 + rg + 8 * i;
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-          q + (((size_t)b * a.Nq + n) * a.Hq + h) * 128 + 8 * cg));
-      w[i][0] = v.x;
-      w[i][1] = v.y;
-      w[i][2] = v.z;
-      w[i][3] = v.w;
-    }
-    auto bits = [&](int i, int t) -> uint32_t {  // bf16 bits of row i, column t (0..7)
-      return (t & 1) ? (w[i][t >> 1] >> 16) : (w[i][t >> 1] & 0xFFFFu);
+      for (int i = 0; i < kRowsPerThread; ++i) {
+        size_t n = (size_t)blk * 128 + rg + kRowGroups * i;
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+            q + (((size_t)b * a.Nq + n) * a.Hq + h) * 128 + 8 * cg));
+        w[i][0] = v.x;
+        w[i][1] = v.y;
+        w[i][2] = v.z;
+        w[i][3] = v.w;
+      }
     };
-    int* emax_s = reinterpret_cast<int*>(&part[0][0]);  // [8][128] ints, reused below
+    unsigned m = 0;
+    uint32_t wn[kRowsPerThread][4];
+    if (bid < units) load_unit(bid, wn);
+    for (int unit = bid; unit < units; unit += nq_blocks) {
+      uint32_t w[kRowsPerThread][4];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      int e = 1;
+      for (int i = 0; i < kRowsPerThread; ++i)
 #pragma unroll
-      for (int i = 0; i < 16; ++i) e = max(e, (int)((bits(i, t) >> 7) & 0xFFu));
-      emax_s[rg * 128 + 8 * cg + t] = e;
-    }
-    __syncthreads();
-    __shared__ int col_emax[128];
-    {
-      int e = emax_s[threadIdx.x];
-#pragma unroll
-      for (int g2 = 1; g2 < 8; ++g2) e = max(e, emax_s[g2 * 128 + threadIdx.x]);
-      col_emax[threadIdx.x] = e;
-    }
-    __syncthreads();
-    __shared__ int col_bad[128];
-    col_bad[threadIdx.x] = 0;
-    long long* ipart = reinterpret_cast<long long*>(&part[0][0]);  // [8][128]
-    __syncthreads();
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      const int ce = col_emax[8 * cg + t];
-      long long acc = 0;
-      bool bad = false;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint32_t u = bits(i, t);
-        const uint32_t ex = (u >> 7) & 0xFFu, mant = u & 0x7Fu;
-        const long long M = ex ? (long long)(mant | 0x80u) : (long long)mant;
-        const int sh = (ex ? (int)ex : 1) - ce + 48;
-        if (M != 0 && sh < 0) bad = true;
-        const long long term = (sh >= 0) ? (M << sh) : 0;
-        acc += (u & 0x8000u) ? -term : term;
-      }
-      ipart[rg * 128 + 8 * cg + t] = acc;
-      if (bad) col_bad[8 * cg + t] = 1;
-    }
-    __syncthreads();
-    {
-      const int c = threadIdx.x;
-      long long S = 0;
-#pragma unroll
-      for (int g2 = 0; g2 < 8; ++g2) S += ipart[g2 * 128 + c];
-      float mean = ldexpf(__ll2float_rn(S), col_emax[c] - 189);
-      if (col_bad[c] || (mean != 0.0f && fabsf(mean) < 1.17549435e-38f)) {
-        // fp64 sum with a compensation term (same rounding as a correctly
-        // rounded sum whenever the correction captures the error)
-        double sd = 0.0, comp = 0.0;
-        for (int r = 0; r < 128; ++r) {
-          const double v = (double)__bfloat162float(
-              q[(((size_t)b * a.Nq + (size_t)blk * 128 + r) * a.Hq + h) * 128 + c]);
-          const double t2 = sd + v;
-          comp += (fabs(sd) >= fabs(v)) ? ((sd - t2) + v) : ((v - t2) + sd);
-          sd = t2;
-        }
-        mean = (float)((sd + comp) * (1.0 / 128.0));
-      }
-      qb[c] = mean;
-      a.qbar[((size_t)bh * nblk + blk) * 128 + c] = mean;
-    }
-    __syncthreads();
-    unsigned m = __float_as_uint(fabsf(qb[threadIdx.x]));
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
+        for (int k = 0; k < 4; ++k) w[i][k] = wn[i][k];
+      if (unit + nq_blocks < units) load_unit(unit + nq_blocks, wn);
+      const int blk = unit % nblk, bh = unit / nblk;
+      const int h = bh % a.Hq, b = bh / a.Hq;
+      auto bits = [&](int i, int t) -> uint32_t {  // bf16 bits of row i, column t (0..7)
+        return (t & 1) ? (w[i][t >> 1] >> 16) : (w[i][t >> 1] & 0xFFFFu);
+      };
+      int* emax_s = reinterpret_cast<int*>(&ipart[0][0]);  // [kRowGroups][128] ints
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
-        const float x = __uint_as_float(bits(i, t) << 16);
-        m = max(m, __float_as_uint(fabsf(__fsub_rn(x, qb[8 * cg + t]))));
+        int e = 1;
+#pragma unroll
+        for (int i = 0; i < kRowsPerThread; ++i) e = max(e, (int)((bits(i, t) >> 7) & 0xFFu));
+        emax_s[rg * 128 + 8 * cg + t] = e;
       }
+      __syncthreads();
+      if (threadIdx.x < 128) {
+        int e = emax_s[threadIdx.x];
+#pragma unroll
+        for (int g2 = 1; g2 < kRowGroups; ++g2) e = max(e, emax_s[g2 * 128 + threadIdx.x]);
+        col_emax[threadIdx.x] = e;
+        col_bad[threadIdx.x] = 0;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int ce = col_emax[8 * cg + t];
+        long long acc = 0;
+        bool bad = false;
+#pragma unroll
+        for (int i = 0; i < kRowsPerThread; ++i) {
+          const uint32_t u = bits(i, t);
+          const uint32_t ex = (u >> 7) & 0xFFu, mant = u & 0x7Fu;
+          const long long M = ex ? (long long)(mant | 0x80u) : (long long)mant;
+          const int sh = (ex ? (int)ex : 1) - ce + 48;
+          if (M != 0 && sh < 0) bad = true;
+          const long long term = (sh >= 0) ? (M << sh) : 0;
+          acc += (u & 0x8000u) ? -term : term;
+        }
+        ipart[rg][8 * cg + t] = acc;
+        if (bad) col_bad[8 * cg + t] = 1;
+      }
+      __syncthreads();
+      if (threadIdx.x < 128) {
+        const int c = threadIdx.x;
+        long long S = 0;
+#pragma unroll
+        for (int g2 = 0; g2 < kRowGroups; ++g2) S += ipart[g2][c];
+        float mean = ldexpf(__ll2float_rn(S), col_emax[c] - 189);
+        if (col_bad[c] || (mean != 0.0f && fabsf(mean) < 1.17549435e-38f)) {
+          // fp64 sum with a compensation term (same rounding as a correctly
+          // rounded sum whenever the correction captures the error)
+          double sd = 0.0, comp = 0.0;
+          for (int r = 0; r < 128; ++r) {
+            const double v = (double)__bfloat162float(
+                q[(((size_t)b * a.Nq + (size_t)blk * 128 + r) * a.Hq + h) * 128 + c]);
+            const double t2 = sd + v;
+            comp += (fabs(sd) >= fabs(v)) ? ((sd - t2) + v) : ((v - t2) + sd);
+            sd = t2;
+          }
+          mean = (float)((sd + comp) * (1.0 / 128.0));
+        }
+        qb[c] = mean;
+        a.qbar[((size_t)bh * nblk + blk) * 128 + c] = mean;
+        m = max(m, __float_as_uint(fabsf(mean)));
+      }
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < kRowsPerThread; ++i)
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const float x = __uint_as_float(bits(i, t) << 16);
+          m = max(m, __float_as_uint(fabsf(__fsub_rn(x, qb[8 * cg + t]))));
+        }
+      __syncthreads();   // qb and ipart are rewritten by the next unit
+    }
     m = block_max_u32(m, red);
     if (threadIdx.x == 0 && m) atomicMax(&a.amax[0], m);
     return;
@@ -404,18 +421,20 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int sms = num_sms();
   auto amax_blocks = [&](size_t elems) {
-    size_t need = (elems / 8 + kThreads - 1) / kThreads;
+    size_t need = (elems / 8 + kStatsThreads - 1) / kStatsThreads;
     size_t cap = (size_t)sms * 8;
     return (int)(need < cap ? (need ? need : 1) : cap);
   };
   int nq = 0, nk = 0, nv = 0;
-  if (a.q)
-    nq = a.compensate ? a.B * a.Hq * (a.Nq / 128)
+  if (a.q) {
+    const int units = a.B * a.Hq * (a.Nq / 128);
+    nq = a.compensate ? (units < 2 * sms ? units : 2 * sms)   // persistent, 2 per SM
                       : amax_blocks((size_t)a.B * a.Nq * a.Hq * 128);
+  }
   if (a.k) nk = amax_blocks((size_t)a.B * a.Nk * a.Hkv * 128);
   if (a.v) nv = amax_blocks((size_t)a.B * a.Nk * a.Hkv * 128);
   if (nq + nk + nv > 0) {
-    stats_kernel<<<nq + nk + nv, kThreads, 0, stream>>>(a, nq, nk, nv);
+    stats_kernel<<<nq + nk + nv, kStatsThreads, 0, stream>>>(a, nq, nk, nv);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
