@@ -49,8 +49,8 @@ constexpr uint32_t kOffQ = kOffKs + kStages * 1024;     // (1 + 2) x 1 KB: q', q
 constexpr uint32_t kOffQs = kOffQ + 3 * 1024;           // (1 + 2) x 1 KB scale atoms
 constexpr uint32_t kOffP = kOffQs + 3 * 1024;           // 2 x 2 KB: P^T (16 rows x 128 B)
 constexpr uint32_t kOffOnes = kOffP + 2 * 2048;         // 4 KB ones (128 rows x 32 B)
-constexpr uint32_t kOffRed = kOffOnes + 4096;           // 4 warps x 16 floats
-constexpr uint32_t kOffBar = kOffRed + 4 * 16 * 4;
+constexpr uint32_t kOffRed = kOffOnes + 4096;           // 4 warps x 16 floats, 4 vote words
+constexpr uint32_t kOffBar = kOffRed + 4 * 16 * 4 + 16;   // + 4 vote words
 constexpr uint32_t kNumBars = 8 + 3 * kStages + 2;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemUsed = kOffMisc + 64;
@@ -306,8 +306,9 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
       };
       for (int j = 0; ok && j < ntiles; ++j) {
         const int s = j % kStages, bkk = j & 1;
+        // bank j % 2 was last read by the softmax of tile j-2, which published
+        // P_{j-2} before this thread issued PV_{j-2} (previous iteration)
         if (!mbar_wait(bar(kBarKFull0 + s), (j / kStages) & 1, a.err, abort_flag)) break;
-        if (j >= 2 && !mbar_wait(bar(kBarODone), (j - 2) & 1, a.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t sfk = tmem + kColSfK + 8 * s;
         for (int kc = 0; kc < 2; ++kc)
@@ -409,27 +410,46 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
       }
       const int key = k0 + j * 128 + t;
       const bool valid = key < k1;
-      // block max per query row over the 128 keys
       float v[kMaxG];
 #pragma unroll
-      for (int n = 0; n < kMaxG; ++n) {
-        v[n] = valid ? __uint_as_float(sr[n]) : -INFINITY;
-        float mx = v[n];
+      for (int n = 0; n < kMaxG; ++n) v[n] = valid ? __uint_as_float(sr[n]) : -INFINITY;
+      // The reference max of head n moves only if some key of this tile has
+      // S * cs > m + kRescaleTau; the tile max over the 128 keys (shuffles and
+      // shared memory) is needed only then.  Vote first: bit n set if any key
+      // of the CTA moves head n.
+      uint32_t move = 0;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (lane == 0) red[warp * 16 + n] = mx;
-      }
+      for (int n = 0; n < kMaxG; ++n)
+        if (n < g && (m[n] == -INFINITY ? v[n] != -INFINITY : __fmul_rn(v[n], cs) > m[n] + kRescaleTau))
+          move |= 1u << n;
+      move = __reduce_or_sync(0xffffffffu, move);
+      if (lane == 0) reinterpret_cast<uint32_t*>(red)[64 + warp] = move;
       named_bar_sync(1, 128);
+      move = reinterpret_cast<uint32_t*>(red)[64] | reinterpret_cast<uint32_t*>(red)[65] |
+             reinterpret_cast<uint32_t*>(red)[66] | reinterpret_cast<uint32_t*>(red)[67];
       float alpha[kMaxG];
-      bool any_change = false;
 #pragma unroll
-      for (int n = 0; n < kMaxG; ++n) {
-        const float smax = fmaxf(fmaxf(red[n], red[16 + n]), fmaxf(red[32 + n], red[48 + n]));
-        const float tmax = __fmul_rn(smax, cs);
-        const float mn = (m[n] == -INFINITY || tmax > m[n] + kRescaleTau) ? tmax : m[n];
-        alpha[n] = (m[n] == -INFINITY) ? 0.0f : (mn == m[n] ? 1.0f : ex2(m[n] - mn));
-        any_change |= (n < g) && (alpha[n] != 1.0f);
-        m[n] = mn;
+      for (int n = 0; n < kMaxG; ++n) alpha[n] = 1.0f;
+      bool any_change = false;
+      if (move) {
+        // block max per query row over the 128 keys
+#pragma unroll
+        for (int n = 0; n < kMaxG; ++n) {
+          float mx = v[n];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          if (lane == 0) red[warp * 16 + n] = mx;
+        }
+        named_bar_sync(1, 128);
+#pragma unroll
+        for (int n = 0; n < kMaxG; ++n) {
+          const float smax = fmaxf(fmaxf(red[n], red[16 + n]), fmaxf(red[32 + n], red[48 + n]));
+          const float tmax = __fmul_rn(smax, cs);
+          const float mn = (m[n] == -INFINITY || tmax > m[n] + kRescaleTau) ? tmax : m[n];
+          alpha[n] = (m[n] == -INFINITY) ? 0.0f : (mn == m[n] ? 1.0f : ex2(m[n] - mn));
+          any_change |= (n < g) && (alpha[n] != 1.0f);
+          m[n] = mn;
+        }
       }
       // P^T: row n, column key (128-byte rows, 128-byte swizzle).  Buffer
       // j % 2 was last read by PV_{j-2}; its own barrier completes once per
