@@ -42,6 +42,11 @@ PREFILL_CFG = mi.PREFILL["llama8b_n16k_causal"]
 DECODE_CFG = mi.DECODE["decode_b64_l32k"]
 FLOP_PER_PAIR = 512
 KV_BYTES_PER_TOKEN = 64 + 8 + 128   # K codes + K block scales + V codes, per KV head
+# prefill_kernel inputs and outputs per launch on the 16K workload: Q codes +
+# block scales, rank-one terms, K codes + scales, V codes, O (bf16) and LSE
+PREFILL_ALGO_BYTES = (PREFILL_CFG.B * PREFILL_CFG.N * (PREFILL_CFG.Hq * (64 + 8 + 128 * 2 + 4)
+                                                       + PREFILL_CFG.Hkv * (64 + 8 + 128))
+                      + PREFILL_CFG.B * PREFILL_CFG.Hq * (PREFILL_CFG.N // 128) * 2 * 72)
 
 
 def _peaks():
@@ -118,6 +123,32 @@ class Clocks:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+def measured_traffic(kernel: str):
+    """DRAM bytes per launch (read + write) of `kernel` from the ncu table in
+    profiles/traffic.md, or None when the kernel's sources have changed since
+    the counters were taken (sha256 of the listed files)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(path):
+        return None
+    csrc = os.path.join(ROOT, "flashattention_mpfa_quantize_gb300", "csrc")
+    for line in open(path):
+        f = [x.strip() for x in line.strip().strip("|").split("|")]
+        if len(f) < 6 or f[0] != kernel:
+            continue
+        h = hashlib.sha256()
+        try:
+            for src in f[1].split():
+                with open(os.path.join(csrc, src), "rb") as fh:
+                    h.update(fh.read())
+        except OSError:
+            return None
+        if h.hexdigest()[:16] != f[2]:
+            return None
+        return int(f[4]) + int(f[5])
+    return None
 
 
 def _dist():
@@ -292,7 +323,9 @@ def run_gpu(args):
     peak_eff = (f4 + f8) / t_roof / 1e12
     achieved = flops / (pre * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_eff, "unit": "TFLOP/s",
-                "frac": achieved / peak_eff, "traffic": None,
+                "frac": achieved / peak_eff, "traffic": measured_traffic("prefill_kernel"),
+                "traffic_unit": "bytes per launch (ncu dram read + write)",
+                "algorithmic_bytes": PREFILL_ALGO_BYTES,
                 "kernel": "prefill_kernel", "peak_source": peaks["source"] + " bf16 burst x "
                 "nominal FP4 (6x) / FP8 (2x) ratios, harmonic mix for equal FP4 and FP8 FLOPs",
                 "quantize_ms": statistics.mean(quant_ms), "prefill_ms": pre}
@@ -364,8 +397,10 @@ def run_decode(mp, dev, stream, peaks, flush, args):
     return {"workload": cfg.name, "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "L": cfg.Lmax,
             "value": job / 1e9, "unit": "GB/s", "ms": ms, "chunk": res["chunk"],
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
-                         "frac": gbs / peaks["hbm"], "traffic": None,
-                         "algorithmic_bytes": nbytes},
+                         "frac": gbs / peaks["hbm"],
+                         "traffic": measured_traffic("split_kernel") if not args.decode_batch else None,
+                         "traffic_unit": "bytes per launch (ncu dram read + write)",
+                         "algorithmic_bytes": nbytes, "kernel": "split_kernel"},
             "gpu_launches": 4 * n, "clocks": clk}
 
 

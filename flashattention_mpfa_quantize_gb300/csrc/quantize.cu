@@ -1,7 +1,8 @@
 // quantize.cu -- online NVFP4 quantization of Q and K and FP8 quantization
-// of V (MpFA abstract: "NVFP4 for QK and FP8 for PV"; formats per the FP4
-// section of the "FlashAttention压到4位" explainer: E2M1 codes, one E4M3 scale
-// per 16 elements, one FP32 tensor scale), plus the rank-one smoothing of Q
+// of V (MpFA abstract: the QK operands in NVFP4, the PV operands in FP8;
+// formats per the FP4 section of the "FlashAttention压到4位" explainer: E2M1
+// codes, one E4M3 scale per 16 elements, one FP32 tensor scale), plus the
+// rank-one smoothing of Q
 // (block mean removed before quantization, the mean kept as T NVFP4 terms).
 //
 // Two HBM-streaming passes, because every tensor scale depends on the whole

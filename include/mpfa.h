@@ -103,8 +103,9 @@ const char *mpfa_status_string(mpfa_status s);
 size_t mpfa_quantize_workspace_size(int B, int Nq, int Hq, int compensate);
 
 /*
- * Online quantization of one attention layer's inputs (MpFA abstract:
- * "NVFP4 for QK and FP8 for PV"; formats per the FP4 explainer section).
+ * Online quantization of one attention layer's inputs (MpFA abstract: the QK
+ * operands in NVFP4, the PV operands in FP8; formats per the FP4 explainer
+ * section).
  *
  *   q_bf16 [B][Nq][Hq][d], k_bf16 / v_bf16 [B][Nk][Hkv][d]  bf16, device.
  *   Any of q/k/v may be NULL to skip it (its output must then be NULL too);
