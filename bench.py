@@ -405,8 +405,11 @@ def run_decode(mp, dev, stream, peaks, flush, args):
 
 
 def run_e2e(mp, dev, stream, Q, K, V, args):
-    """Same step through the public API with pinned host buffers: H2D of the
-    bf16 inputs, quantize, prefill, D2H of O, all inside the timed region."""
+    """Same step through the public API with pinned host buffers: every step
+    copies its bf16 Q/K/V from the host, quantizes, runs the prefill and
+    copies its O back to the host, all inside the timed region.  The copies
+    run on two copy streams with two device buffer sets, so the upload of
+    step i+1 and the download of step i-1 overlap the compute of step i."""
     cfg = PREFILL_CFG
     hq = torch.empty(Q.shape, dtype=Q.dtype, pin_memory=True)
     hk = torch.empty(K.shape, dtype=K.dtype, pin_memory=True)
@@ -414,27 +417,55 @@ def run_e2e(mp, dev, stream, Q, K, V, args):
     hq.copy_(Q)
     hk.copy_(K)
     hv.copy_(V)
-    ho = torch.empty(Q.shape, dtype=torch.bfloat16, pin_memory=True)
-    dq, dk, dv = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
-    o = torch.empty_like(Q)
+    ho = [torch.empty(Q.shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
+    dq = [torch.empty_like(Q) for _ in range(2)]
+    dk = [torch.empty_like(K) for _ in range(2)]
+    dv = [torch.empty_like(V) for _ in range(2)]
+    o = [torch.empty_like(Q) for _ in range(2)]
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    in_ready = [ev(), ev()]      # inputs of buffer b uploaded
+    in_free = [None, None]       # quantize of buffer b done (inputs consumed)
+    out_ready = [ev(), ev()]     # O of buffer b computed
+    out_free = [None, None]      # O of buffer b downloaded
 
-    def step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        z = mp.quantize_qkv(dq, dk, dv, compensate=True, T=2)
-        mp.prefill(z, causal=cfg.causal, out=o, want_lse=False)
-        ho.copy_(o, non_blocking=True)
+    def step(i):
+        b = i & 1
+        with torch.cuda.stream(up):
+            if in_free[b] is not None:
+                up.wait_event(in_free[b])
+            dq[b].copy_(hq, non_blocking=True)
+            dk[b].copy_(hk, non_blocking=True)
+            dv[b].copy_(hv, non_blocking=True)
+            in_ready[b].record(up)
+        stream.wait_event(in_ready[b])
+        if out_free[b] is not None:
+            stream.wait_event(out_free[b])
+        z = mp.quantize_qkv(dq[b], dk[b], dv[b], compensate=True, T=2)
+        e = ev()
+        e.record(stream)
+        in_free[b] = e
+        mp.prefill(z, causal=cfg.causal, out=o[b], want_lse=False)
+        out_ready[b].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(out_ready[b])
+            ho[b].copy_(o[b], non_blocking=True)
+            f = ev()
+            f.record(down)
+            out_free[b] = f
 
-    for _ in range(2):
-        step()
+    for i in range(2):
+        step(i)
     torch.cuda.synchronize()
     n = max(args.steps, 3)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for _ in range(n):
-        step()
+    up.wait_event(t0)
+    for i in range(n):
+        step(i)
+    stream.wait_event(out_free[(n - 1) & 1])
+    stream.wait_event(out_free[n & 1])
     t1.record(stream)
     torch.cuda.synchronize()
     ws = _dist()[0]
@@ -442,7 +473,8 @@ def run_e2e(mp, dev, stream, Q, K, V, args):
     rate, ms = aggregate_rate(flops, t0.elapsed_time(t1) / n, ws, dev)
     h2d = (Q.numel() + K.numel() + V.numel()) * 2
     return {"value": rate / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": Q.numel() * 2}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": Q.numel() * 2,
+            "pipelining": "two buffer sets; H2D of step i+1 and D2H of step i-1 overlap step i"}
 
 
 def main():

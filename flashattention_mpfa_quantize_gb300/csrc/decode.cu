@@ -587,16 +587,52 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
 
 }  // namespace
 
+// Resident split CTAs per SM, from the kernel's registers and shared memory
+// against the SM's register file and shared-memory capacity (1 KB of each
+// CTA's shared memory is reserved by the system).
+static int split_ctas_per_sm() {
+  static int occ = 0;
+  if (!occ) {
+    int dev = 0, smem_sm = 0, regs_sm = 0;
+    cudaFuncAttributes fa{};
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) ==
+            cudaSuccess &&
+        cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) ==
+            cudaSuccess &&
+        cudaFuncGetAttributes(&fa, split_kernel) == cudaSuccess && fa.numRegs > 0) {
+      const int by_smem = smem_sm / (int)(kSmemBytes + fa.sharedSizeBytes + 1024);
+      const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
+      const int by_regs = regs_sm / (regs_warp * (kThreads / 32));
+      occ = by_smem < by_regs ? by_smem : by_regs;
+    }
+    if (occ < 1) occ = 1;
+  }
+  return occ;
+}
+
+// Chunk (keys per split) for B x Hkv units of Lmax keys: the split count that
+// minimises  waves x (128-key tiles per CTA + a fixed per-CTA cost), where a
+// wave is one CTA in every resident slot.  The fixed cost (query codes,
+// TMEM allocation, pipeline fill and drain, partial results) is taken as 4
+// tiles' time.
 int decode_default_chunk(int B, int Hkv, int Lmax, int num_sms) {
+  constexpr long long kCtaCostTiles = 4;
   const long long units = (long long)B * Hkv;
-  const long long target = 16LL * num_sms;
-  long long nsplit = (target + units - 1) / units;
-  const long long max_split = (Lmax + 127) / 128;
-  if (nsplit < 1) nsplit = 1;
-  if (nsplit > max_split) nsplit = max_split;
-  long long chunk = (Lmax + nsplit - 1) / nsplit;
-  chunk = (chunk + 127) / 128 * 128;
-  return (int)chunk;
+  const long long slots = (long long)split_ctas_per_sm() * num_sms;
+  const long long tiles = (Lmax + 127) / 128;
+  long long best_n = 1, best_cost = -1;
+  for (long long n = 1; n <= tiles; ++n) {
+    const long long per_cta = (tiles + n - 1) / n;
+    if (n > 1 && (tiles + per_cta - 1) / per_cta < n) continue;  // same chunk as a smaller n
+    const long long waves = (units * n + slots - 1) / slots;
+    const long long cost = waves * (per_cta + kCtaCostTiles);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_n = n;
+    }
+  }
+  return (int)(((tiles + best_n - 1) / best_n) * 128);
 }
 
 size_t decode_workspace_bytes(int B, int Hq, int Hkv, int nsplit) {
