@@ -284,35 +284,59 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(QuantArgs a) {
   const int part = blockIdx.y;
 
   if (part == 0 && a.q) {
+    // One warp per (b, h, 128-row block): 4 rows per step (8 lanes per row,
+    // one 16-element NVFP4 block per lane), the block means of the lane's 16
+    // columns held in registers, the next step's rows loaded before the
+    // current ones are coded.
     float s = tensor_scale(a.amax[0], kNvfp4Max);
     if (blockIdx.x == 0 && threadIdx.x == 0) *a.s_q = s;
     const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(a.q);
-    size_t rows = (size_t)a.B * a.Hq * a.Nq;
-    int nblk = a.Nq / 128;
-    for (size_t u = gwarp; u < rows / 4; u += warps_total) {
-      size_t r = u * 4 + ri;  // output row (b, h, n)
-      size_t n = r % a.Nq;
-      size_t bh = r / a.Nq;
-      size_t h = bh % a.Hq, b = bh / a.Hq;
-      float x[16];
-      load16_bf16(q + ((b * a.Nq + n) * a.Hq + h) * 128 + 16 * j, x);
+    const int nblk = a.Nq / 128;
+    const size_t units = (size_t)a.B * a.Hq * nblk;
+    for (size_t unit = gwarp; unit < units; unit += warps_total) {
+      const size_t bh = unit / nblk, blk = unit % nblk;
+      const size_t h = bh % a.Hq, b = bh / a.Hq;
+      float m[16];
       if (a.compensate) {
-        const float4* qb =
-            reinterpret_cast<const float4*>(a.qbar + (bh * nblk + n / 128) * 128 + 16 * j);
+        const float4* qb = reinterpret_cast<const float4*>(a.qbar + unit * 128 + 16 * j);
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-          float4 m = qb[t];
-          x[4 * t] = __fsub_rn(x[4 * t], m.x);
-          x[4 * t + 1] = __fsub_rn(x[4 * t + 1], m.y);
-          x[4 * t + 2] = __fsub_rn(x[4 * t + 2], m.z);
-          x[4 * t + 3] = __fsub_rn(x[4 * t + 3], m.w);
+          const float4 v = qb[t];
+          m[4 * t] = v.x;
+          m[4 * t + 1] = v.y;
+          m[4 * t + 2] = v.z;
+          m[4 * t + 3] = v.w;
         }
       }
-      uint2 codes;
-      uint32_t sb;
-      nvfp4_block(x, s, codes, sb);
-      *reinterpret_cast<uint2*>(a.qc + r * 64 + 8 * j) = codes;
-      store_scales_tiled(a.qs, r, j, sb);
+      auto src = [&](int step) {
+        const size_t n = blk * 128 + 4 * step + ri;
+        return reinterpret_cast<const uint4*>(q + ((b * a.Nq + n) * a.Hq + h) * 128 + 16 * j);
+      };
+      uint4 n0 = __ldg(src(0)), n1 = __ldg(src(0) + 1);
+#pragma unroll 1
+      for (int step = 0; step < 32; ++step) {
+        const uint32_t w[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+        if (step + 1 < 32) {
+          n0 = __ldg(src(step + 1));
+          n1 = __ldg(src(step + 1) + 1);
+        }
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          x[2 * i] = bf16_lo(w[i]);
+          x[2 * i + 1] = bf16_hi(w[i]);
+        }
+        if (a.compensate) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) x[i] = __fsub_rn(x[i], m[i]);
+        }
+        const size_t r = bh * a.Nq + blk * 128 + 4 * step + ri;  // output row (b, h, n)
+        uint2 codes;
+        uint32_t sb;
+        nvfp4_block(x, s, codes, sb);
+        *reinterpret_cast<uint2*>(a.qc + r * 64 + 8 * j) = codes;
+        store_scales_tiled(a.qs, r, j, sb);
+      }
     }
     return;
   }
