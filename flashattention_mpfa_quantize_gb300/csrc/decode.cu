@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
       for (int j = 0; j < ntiles; ++j) {
         const int s = j % kStages;
         if (j >= kStages &&
-            !mbar_wait(bar(kBarKvEmpty0 + s), ((j / kStages) - 1) & 1, a.err, abort_flag))
+            !mbar_wait_tf(bar(kBarKvEmpty0 + s), ((j / kStages) - 1) & 1, a.err, abort_flag))
           break;
         const int row = row0 + j * 128;
         mbar_expect_tx(bar(kBarKFull0 + s), 8192 + 1024);
@@ -268,8 +268,8 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
       }
       for (int j = issued - kStages > 0 ? issued - kStages : 0; j < issued; ++j) {
         const int s = j % kStages;
-        mbar_wait(bar(kBarKFull0 + s), (j / kStages) & 1, a.err, nullptr);
-        mbar_wait(bar(kBarVFull0 + s), (j / kStages) & 1, a.err, nullptr);
+        mbar_wait_tf(bar(kBarKFull0 + s), (j / kStages) & 1, a.err, nullptr);
+        mbar_wait_tf(bar(kBarVFull0 + s), (j / kStages) & 1, a.err, nullptr);
       }
     }
   } else if (warp == 5) {
@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
       const uint32_t id_qk = idesc_nvfp4(128, 16);
       const uint32_t id_pv = idesc_fp8(128, 16, 1, 0);
       const uint32_t id_l = idesc_fp8(128, 16, 0, 0);
-      bool ok = mbar_wait(bar(kBarQReady), 0, a.err, abort_flag);
+      bool ok = mbar_wait_tf(bar(kBarQReady), 0, a.err, abort_flag);
       if (ok) {
         tc_fence_after();
         for (int o = 0; o < 1 + T; ++o)
@@ -287,8 +287,8 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
       }
       auto issue_pv = [&](int jp) -> bool {
         const int bp = jp & 1, sp = jp % kStages;
-        if (!mbar_wait(bar(kBarPReady0 + bp), (jp >> 1) & 1, a.err, abort_flag)) return false;
-        if (!mbar_wait(bar(kBarVFull0 + sp), (jp / kStages) & 1, a.err, abort_flag)) return false;
+        if (!mbar_wait_tf(bar(kBarPReady0 + bp), (jp >> 1) & 1, a.err, abort_flag)) return false;
+        if (!mbar_wait_tf(bar(kBarVFull0 + sp), (jp / kStages) & 1, a.err, abort_flag)) return false;
         tc_fence_after();
         const uint32_t paddr = sbase + kOffP + 2048 * bp;
         const uint32_t vaddr = sbase + kOffV + 16384 * sp;
@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
         const int s = j % kStages, bkk = j & 1;
         // bank j % 2 was last read by the softmax of tile j-2, which published
         // P_{j-2} before this thread issued PV_{j-2} (previous iteration)
-        if (!mbar_wait(bar(kBarKFull0 + s), (j / kStages) & 1, a.err, abort_flag)) break;
+        if (!mbar_wait_tf(bar(kBarKFull0 + s), (j / kStages) & 1, a.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t sfk = tmem + kColSfK + 8 * s;
         for (int kc = 0; kc < 2; ++kc)
@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
       }
       if (ok) issue_pv(ntiles - 1);
       tc_commit(bar(kBarDrain));
-      mbar_wait(bar(kBarDrain), 0, a.err, nullptr);
+      mbar_wait_tf(bar(kBarDrain), 0, a.err, nullptr);
     }
   } else {
     // ---------------- softmax: thread = key (TMEM lane) ----------------
@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       const int bkk = j & 1;
-      if (!named_bar_and(2, 128, mbar_wait(bar(kBarSFull0 + bkk), (j >> 1) & 1, a.err, abort_flag))) {
+      if (!named_bar_and(2, 128, mbar_wait_tf(bar(kBarSFull0 + bkk), (j >> 1) & 1, a.err, abort_flag))) {
         ok = false;
         break;
       }
@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
       // P^T: row n, column key (128-byte rows, 128-byte swizzle).  Buffer
       // j % 2 was last read by PV_{j-2}; its own barrier completes once per
       // two tiles, so the parity cannot run two phases ahead of this wait.
-      if (j >= 2 && !named_bar_and(2, 128, mbar_wait(bar(kBarPFree0 + bkk), ((j >> 1) - 1) & 1,
+      if (j >= 2 && !named_bar_and(2, 128, mbar_wait_tf(bar(kBarPFree0 + bkk), ((j >> 1) - 1) & 1,
                                                      a.err, abort_flag))) {
         ok = false;
         break;
@@ -470,7 +470,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
       fence_proxy_async_smem();
       // correction of O^T and L (columns n < g) once PV_{j-1} has landed
       if (j > 0 && any_change) {
-        if (!named_bar_and(2, 128, mbar_wait(bar(kBarODone), (j - 1) & 1, a.err, abort_flag))) {
+        if (!named_bar_and(2, 128, mbar_wait_tf(bar(kBarODone), (j - 1) & 1, a.err, abort_flag))) {
           ok = false;
           break;
         }
@@ -515,7 +515,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
       mbar_arrive(bar(kBarPReady0 + bkk));
       named_bar_sync(1, 128);  // red[] is reused by the next tile
     }
-    if (ok && named_bar_and(2, 128, mbar_wait(bar(kBarODone), (ntiles - 1) & 1, a.err, abort_flag))) {
+    if (ok && named_bar_and(2, 128, mbar_wait_tf(bar(kBarODone), (ntiles - 1) & 1, a.err, abort_flag))) {
       tc_fence_after();
       uint32_t o16[16], l16[16];
       {
