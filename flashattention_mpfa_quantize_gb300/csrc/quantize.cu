@@ -8,7 +8,7 @@
 // Two HBM-streaming passes, because every tensor scale depends on the whole
 // tensor:
 //   stats_kernel : amax of K and V; for Q either amax(Q) or, with the
-//                  smoothing, the fp32 block means qbar (exact integer sums) and
+//                  smoothing, the fp32 block means qbar (exact column sums) and
 //                  max(amax(Q - qbar), amax(qbar)).
 //   quant_kernel : codes and scales of Q (or Q - qbar), of the qbar terms,
 //                  of K and of V; the tensor scales.
@@ -132,10 +132,10 @@ __device__ void amax_bf16(const uint4* p, size_t n8, int b0, int nblk, unsigned*
 __global__ void __launch_bounds__(kStatsThreads, 2) stats_kernel(QuantArgs a, int nq_blocks,
                                                                  int nk_blocks, int nv_blocks) {
   __shared__ unsigned red[kStatsThreads / 32];
-  __shared__ long long ipart[kRowGroups][128];   // per row group: column partial sums (also emax)
-  __shared__ int col_emax[128];
+  // per warp (16) x column (128): column partials of the two sums, max, min
+  __shared__ float part[4][kStatsThreads / 32][128];
+  __shared__ float col_c0[128];
   __shared__ int col_bad[128];
-  __shared__ float qb[128];
   int bid = blockIdx.x;
   if (bid < nq_blocks) {
     if (!a.compensate) {
@@ -145,17 +145,26 @@ __global__ void __launch_bounds__(kStatsThreads, 2) stats_kernel(QuantArgs a, in
     }
     // Persistent over the (b, h, 128-row block) units, the next unit's rows
     // loaded while the current one is reduced.  Thread = kRowsPerThread rows
-    // (row group rg) x 8 columns (column group cg).  Each column sum is
-    // computed exactly in integers: a bf16 value is M * 2^(e - 134)
-    // (M < 256); scaled to units of 2^(emax - 182), where emax is the
-    // column's largest exponent, every term is an integer below 2^56 and 128
-    // of them fit an int64.  The sum then rounds once to fp32 (exact scaling
-    // by 2^k), i.e. the mean is the fp32 rounding of the exact mean.  A
-    // column whose values span more than 2^48 (or whose mean would be
-    // subnormal) takes an fp64 path with a compensation term instead.
+    // (row group rg) x 8 columns (column group cg); the two row groups of a
+    // warp hold the same columns.
+    //
+    // Each column sum is exact, in two fp32 sums.  With E the largest
+    // biased exponent of the column (at least 1) and u = 2^(E - 143) (the
+    // bf16 spacing 9 binades below the largest value), every x splits
+    // exactly into hi = x rounded to a multiple of u (adding and subtracting
+    // C = 1.5 * 2^23 * u) and lo = x - hi, |lo| <= u / 2.  Any partial sum
+    // of the his is a multiple of u below 2^24 u, and, when no nonzero value
+    // lies more than 26 binades below E, any partial sum of the los is a
+    // multiple of 2^(E - 160) below 2^24 times that: both are exact in fp32
+    // in any order, and one fp32 addition rounds hi + lo correctly.  The
+    // mean is that sum times 2^-7 (computed in fp64 if it is subnormal).  A
+    // column with a wider spread, or with E > 247, takes an fp64 path with a
+    // compensation term instead.  max |x - qbar| over a column is reached at
+    // its largest or smallest x, since fp32(x - qbar) is monotonic in x.
     const int nblk = a.Nq / 128;
     const int units = a.B * a.Hq * nblk;
     const int cg = threadIdx.x & 15, rg = threadIdx.x >> 4;
+    const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(a.q);
     auto load_unit = [&](int unit, uint32_t (&w)[kRowsPerThread][4]) {
       const int blk = unit % nblk, bh = unit / nblk;
@@ -183,52 +192,89 @@ __global__ void __launch_bounds__(kStatsThreads, 2) stats_kernel(QuantArgs a, in
       if (unit + nq_blocks < units) load_unit(unit + nq_blocks, wn);
       const int blk = unit % nblk, bh = unit / nblk;
       const int h = bh % a.Hq, b = bh / a.Hq;
-      auto bits = [&](int i, int t) -> uint32_t {  // bf16 bits of row i, column t (0..7)
-        return (t & 1) ? (w[i][t >> 1] >> 16) : (w[i][t >> 1] & 0xFFFFu);
-      };
-      int* emax_s = reinterpret_cast<int*>(&ipart[0][0]);  // [kRowGroups][128] ints
+      // column max |x| and min (|x| - 1) (zero -> 0xFFFF) on bf16 bit patterns,
+      // two columns per 32-bit word
+      uint32_t* pmax = reinterpret_cast<uint32_t*>(&part[0][0][0]);
+      uint32_t* pmin = reinterpret_cast<uint32_t*>(&part[1][0][0]);
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        int e = 1;
-#pragma unroll
-        for (int i = 0; i < kRowsPerThread; ++i) e = max(e, (int)((bits(i, t) >> 7) & 0xFFu));
-        emax_s[rg * 128 + 8 * cg + t] = e;
-      }
-      __syncthreads();
-      if (threadIdx.x < 128) {
-        int e = emax_s[threadIdx.x];
-#pragma unroll
-        for (int g2 = 1; g2 < kRowGroups; ++g2) e = max(e, emax_s[g2 * 128 + threadIdx.x]);
-        col_emax[threadIdx.x] = e;
-        col_bad[threadIdx.x] = 0;
-      }
-      __syncthreads();
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int ce = col_emax[8 * cg + t];
-        long long acc = 0;
-        bool bad = false;
+      for (int k = 0; k < 4; ++k) {
+        uint32_t mx = 0, mn = 0xFFFFFFFFu;
 #pragma unroll
         for (int i = 0; i < kRowsPerThread; ++i) {
-          const uint32_t u = bits(i, t);
-          const uint32_t ex = (u >> 7) & 0xFFu, mant = u & 0x7Fu;
-          const long long M = ex ? (long long)(mant | 0x80u) : (long long)mant;
-          const int sh = (ex ? (int)ex : 1) - ce + 48;
-          if (M != 0 && sh < 0) bad = true;
-          const long long term = (sh >= 0) ? (M << sh) : 0;
-          acc += (u & 0x8000u) ? -term : term;
+          const uint32_t mag = w[i][k] & 0x7FFF7FFFu;
+          mx = __vmaxu2(mx, mag);
+          mn = __vminu2(mn, __vsub2(mag, 0x00010001u));
         }
-        ipart[rg][8 * cg + t] = acc;
-        if (bad) col_bad[8 * cg + t] = 1;
+        mx = __vmaxu2(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        mn = __vminu2(mn, __shfl_xor_sync(0xffffffffu, mn, 16));
+        if (lane < 16) {
+          const int c = 8 * cg + 2 * k;
+          pmax[wid * 128 + c] = mx & 0xFFFFu;
+          pmax[wid * 128 + c + 1] = mx >> 16;
+          pmin[wid * 128 + c] = mn & 0xFFFFu;
+          pmin[wid * 128 + c + 1] = mn >> 16;
+        }
       }
       __syncthreads();
       if (threadIdx.x < 128) {
         const int c = threadIdx.x;
-        long long S = 0;
+        uint32_t mx = 0, mn = 0xFFFFu;
 #pragma unroll
-        for (int g2 = 0; g2 < kRowGroups; ++g2) S += ipart[g2][c];
-        float mean = ldexpf(__ll2float_rn(S), col_emax[c] - 189);
-        if (col_bad[c] || (mean != 0.0f && fabsf(mean) < 1.17549435e-38f)) {
+        for (int g2 = 0; g2 < kStatsThreads / 32; ++g2) {
+          mx = max(mx, pmax[g2 * 128 + c]);
+          mn = min(mn, pmin[g2 * 128 + c]);
+        }
+        const int E = max((int)(mx >> 7), 1);
+        const bool any = mn != 0xFFFFu;
+        const int Emin = max((int)((mn + 1) >> 7), 1);
+        const bool bad = E > 247 || (any && Emin < E - 26);
+        col_bad[c] = bad;
+        col_c0[c] = bad ? 0.0f : __uint_as_float(((uint32_t)(E + 7) << 23) | 0x400000u);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int c = 8 * cg + t;
+        const float C = col_c0[c];
+        float s0 = 0.0f, s1 = 0.0f, xmx = -INFINITY, xmn = INFINITY;
+#pragma unroll
+        for (int i = 0; i < kRowsPerThread; ++i) {
+          const uint32_t wv = w[i][t >> 1];
+          const float x = __uint_as_float((t & 1) ? (wv & 0xFFFF0000u) : (wv << 16));
+          const float hi = __fsub_rn(__fadd_rn(x, C), C);
+          s0 = __fadd_rn(s0, hi);
+          s1 = __fadd_rn(s1, __fsub_rn(x, hi));
+          xmx = fmaxf(xmx, x);
+          xmn = fminf(xmn, x);
+        }
+        s0 = __fadd_rn(s0, __shfl_xor_sync(0xffffffffu, s0, 16));
+        s1 = __fadd_rn(s1, __shfl_xor_sync(0xffffffffu, s1, 16));
+        xmx = fmaxf(xmx, __shfl_xor_sync(0xffffffffu, xmx, 16));
+        xmn = fminf(xmn, __shfl_xor_sync(0xffffffffu, xmn, 16));
+        if (lane < 16) {
+          part[0][wid][c] = s0;
+          part[1][wid][c] = s1;
+          part[2][wid][c] = xmx;
+          part[3][wid][c] = xmn;
+        }
+      }
+      __syncthreads();
+      if (threadIdx.x < 128) {
+        const int c = threadIdx.x;
+        float s0 = 0.0f, s1 = 0.0f, xmx = -INFINITY, xmn = INFINITY;
+#pragma unroll
+        for (int g2 = 0; g2 < kStatsThreads / 32; ++g2) {
+          s0 = __fadd_rn(s0, part[0][g2][c]);
+          s1 = __fadd_rn(s1, part[1][g2][c]);
+          xmx = fmaxf(xmx, part[2][g2][c]);
+          xmn = fminf(xmn, part[3][g2][c]);
+        }
+        float mean;
+        if (!col_bad[c]) {
+          mean = __fmul_rn(__fadd_rn(s0, s1), 0.0078125f);
+          if (mean != 0.0f && fabsf(mean) < 1.17549435e-38f)
+            mean = __double2float_rn(((double)s0 + (double)s1) * 0.0078125);
+        } else {
           // fp64 sum with a compensation term (same rounding as a correctly
           // rounded sum whenever the correction captures the error)
           double sd = 0.0, comp = 0.0;
@@ -241,19 +287,12 @@ __global__ void __launch_bounds__(kStatsThreads, 2) stats_kernel(QuantArgs a, in
           }
           mean = (float)((sd + comp) * (1.0 / 128.0));
         }
-        qb[c] = mean;
         a.qbar[((size_t)bh * nblk + blk) * 128 + c] = mean;
         m = max(m, __float_as_uint(fabsf(mean)));
+        m = max(m, __float_as_uint(fabsf(__fsub_rn(xmx, mean))));
+        m = max(m, __float_as_uint(fabsf(__fsub_rn(xmn, mean))));
       }
-      __syncthreads();
-#pragma unroll
-      for (int i = 0; i < kRowsPerThread; ++i)
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const float x = __uint_as_float(bits(i, t) << 16);
-          m = max(m, __float_as_uint(fabsf(__fsub_rn(x, qb[8 * cg + t]))));
-        }
-      __syncthreads();   // qb and ipart are rewritten by the next unit
+      __syncthreads();   // part and col_* are rewritten by the next unit
     }
     m = block_max_u32(m, red);
     if (threadIdx.x == 0 && m) atomicMax(&a.amax[0], m);

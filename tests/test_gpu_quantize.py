@@ -79,3 +79,54 @@ def test_quantize_kv_only_cache():
     np.testing.assert_array_equal(
         tiled_to_rows(qz["k"]["scales"].cpu().numpy(), 3 * 2 * 256), ref["k"]["ks"].reshape(-1, 8))
     np.testing.assert_array_equal(qz["v"]["codes"].cpu().numpy(), ref["v"]["vc"])
+
+
+def _edge_column_q(rng, n_blocks=2, Hq=2, big=False):
+    """Q [1, 128 n_blocks, Hq, 128] bf16 whose columns exercise every path of
+    the exact block mean: ordinary values, cancellation, a spread of more
+    than 26 binades, tiny and subnormal values (subnormal means), an all-zero
+    column, one nonzero value, an exact tie, and (big=True) values near the
+    bf16 maximum."""
+    x = rng.standard_normal((n_blocks * 128, Hq, 128)).astype(np.float32)
+    r = np.arange(n_blocks * 128)
+    x[:, :, 8] = np.where(r % 4 == 0, 100.0, np.where(r % 4 == 2, -100.0, 1e-3))[:, None] * (
+        1.0 + np.where(r % 2 == 1, 1.0, 0.0)[:, None] * x[:, :, 8])
+    x[:, :, 9] = x[:, :, 9] * np.exp2(rng.integers(-22, 22, (n_blocks * 128, Hq)))
+    x[:, :, 10] = 1e-37 * x[:, :, 10]
+    x[:, :, 11] = 3e-39 * x[:, :, 11]            # bf16 subnormals
+    x[:, :, 12] = 0.0
+    x[:, :, 13] = 0.0
+    x[::128, :, 13] = -2.5
+    x[:, :, 14] = 1.0
+    x[::128, :, 14] = 1.0 + 2.0 ** -7               # the exact mean lies on a tie
+    x[:, :, 15] = np.exp2(-10.0) * (1.0 + (r % 128)[:, None] / 128.0)
+    x[5::128, :, 15] = 192.0                        # 17 binades above the rest
+    x[:, :, 17] = np.where(r % 3 == 0, 1.0, -np.exp2(-26.0))[:, None]   # spread 26
+    x[:, :, 18] = np.where(r % 3 == 0, 1.0, np.exp2(-27.0))[:, None]    # spread 27
+    if big:
+        x[:, :, 16] = 2.5e38 * (0.5 + 0.5 * np.abs(x[:, :, 16]) / (1 + np.abs(x[:, :, 16])))
+    return torch.from_numpy(x[None]).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("big", [False, True])
+def test_quantize_block_means_edge_columns(big):
+    """The fp32 block means the kernels leave in the workspace equal the
+    oracle's correctly rounded means bit for bit, and the codes and tensor
+    scales that follow from them match too."""
+    import flashattention_mpfa_quantize_gb300 as mp
+    import oracle as orc
+    rng = np.random.default_rng(11)
+    Q = _edge_column_q(rng, big=big)
+    K = torch.from_numpy(rng.standard_normal((1, 256, 1, 128)).astype(np.float32)).to(torch.bfloat16)
+    dev = torch.device("cuda:0")
+    qz = mp.quantize_qkv(Q.to(dev), K.to(dev), K.to(dev), compensate=True, T=2)
+    torch.cuda.synchronize()
+    assert mp.get_error() == 0
+    B, N, Hq = 1, Q.shape[1], Q.shape[2]
+    ws = qz["_workspace"][256:256 + B * Hq * (N // 128) * 128 * 4].cpu().numpy().view(np.float32)
+    got = ws.reshape(Hq, N // 128, 128)
+    xs = Q.float().numpy()[0]
+    for h in range(Hq):
+        want, _ = orc.block_means(xs[:, h, :], 128)
+        np.testing.assert_array_equal(got[h].view(np.uint32), want.view(np.uint32))
+    _check(qz, oracle_quantize(Q, K, K, True, 2), True)
