@@ -57,6 +57,21 @@ __device__ __forceinline__ float e2m1_value(uint32_t c) {
   return (c & 8u) ? -mag : mag;
 }
 
+// x / d rounded to nearest even, for many x sharing one divisor d with
+// y = RN(1/d) (Markstein's one-step correction, IBM J. Res. Dev. 34(1),
+// 1990: q0 = RN(x y) is within an ulp of x / d, the residual x - d q0 comes
+// from one fma, and RN(q0 + r y) is the correctly rounded quotient in
+// binary32 when no intermediate leaves the normal range).  Callers keep d in
+// [2^-90, 2^100]: then every quotient a code depends on (|x / d| >= 2^-10
+// for E4M3, >= 1/4 for E2M1) has normal intermediates, and smaller ones
+// keep their sign and stay below the first decision point.
+constexpr float kDivLo = 0x1p-90f;
+constexpr float kDivHi = 0x1p100f;
+__device__ __forceinline__ float div_rn(float x, float d, float y) {
+  const float q0 = __fmul_rn(x, y);
+  return __fmaf_rn(__fmaf_rn(-d, q0, x), y, q0);
+}
+
 // One NVFP4 block of 16 fp32 values with tensor scale s: eight code bytes
 // (element 2i in the low nibble of byte i) and the E4M3 block scale.
 __device__ __forceinline__ void nvfp4_block(const float (&x)[16], float s, uint2& codes,
@@ -68,14 +83,26 @@ __device__ __forceinline__ void nvfp4_block(const float (&x)[16], float s, uint2
   sb = e4m3_pos(t);
   uint32_t w0 = 0, w1 = 0;
   if (sb != 0) {
-    float denom = __fmul_rn(e4m3_value(sb), s);
+    const float denom = __fmul_rn(e4m3_value(sb), s);
+    if (denom >= kDivLo && denom <= kDivHi && bamax <= 3.40282347e38f) {
+      const float y = __frcp_rn(denom);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      uint32_t byte = e2m1x2(__fdiv_rn(x[2 * i], denom), __fdiv_rn(x[2 * i + 1], denom));
-      if (i < 4)
-        w0 |= byte << (8 * i);
-      else
-        w1 |= byte << (8 * (i - 4));
+      for (int i = 0; i < 8; ++i) {
+        uint32_t byte = e2m1x2(div_rn(x[2 * i], denom, y), div_rn(x[2 * i + 1], denom, y));
+        if (i < 4)
+          w0 |= byte << (8 * i);
+        else
+          w1 |= byte << (8 * (i - 4));
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint32_t byte = e2m1x2(__fdiv_rn(x[2 * i], denom), __fdiv_rn(x[2 * i + 1], denom));
+        if (i < 4)
+          w0 |= byte << (8 * i);
+        else
+          w1 |= byte << (8 * (i - 4));
+      }
     }
   }
   codes = make_uint2(w0, w1);
@@ -437,6 +464,8 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(QuantArgs a) {
   if (part == 3 && a.v) {
     float s = tensor_scale(a.amax[2], kFp8Max);
     if (blockIdx.x == 0 && threadIdx.x == 0) *a.s_v = s;
+    const bool fast = s >= kDivLo && s <= kDivHi;
+    const float ys = __frcp_rn(s);
     const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(a.v);
     size_t units = (size_t)a.B * a.Hkv * a.Nk * 8;  // 16-element units
     size_t tid = (size_t)blockIdx.x * kThreads + threadIdx.x;
@@ -449,12 +478,25 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(QuantArgs a) {
       float x[16];
       load16_bf16(v + ((b * a.Nk + n) * a.Hkv + h) * 128 + 16 * jj, x);
       uint32_t w[4];
+      float xm = 0.0f;
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        w[t] = e4m3_signed(__fdiv_rn(x[4 * t], s)) |
-               (e4m3_signed(__fdiv_rn(x[4 * t + 1], s)) << 8) |
-               (e4m3_signed(__fdiv_rn(x[4 * t + 2], s)) << 16) |
-               (e4m3_signed(__fdiv_rn(x[4 * t + 3], s)) << 24);
+      for (int i = 0; i < 16; ++i) xm = fmaxf(xm, fabsf(x[i]));
+      if (fast && xm <= 3.40282347e38f) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          w[t] = e4m3_signed(div_rn(x[4 * t], s, ys)) |
+                 (e4m3_signed(div_rn(x[4 * t + 1], s, ys)) << 8) |
+                 (e4m3_signed(div_rn(x[4 * t + 2], s, ys)) << 16) |
+                 (e4m3_signed(div_rn(x[4 * t + 3], s, ys)) << 24);
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          w[t] = e4m3_signed(__fdiv_rn(x[4 * t], s)) |
+                 (e4m3_signed(__fdiv_rn(x[4 * t + 1], s)) << 8) |
+                 (e4m3_signed(__fdiv_rn(x[4 * t + 2], s)) << 16) |
+                 (e4m3_signed(__fdiv_rn(x[4 * t + 3], s)) << 24);
+        }
       }
       *reinterpret_cast<uint4*>(a.vc + r * 128 + 16 * jj) = make_uint4(w[0], w[1], w[2], w[3]);
     }
