@@ -24,8 +24,8 @@ namespace mpfa {
 namespace {
 
 constexpr int kThreads = 128;        // quant_kernel
-constexpr int kStatsThreads = 512;   // stats_kernel: 32 row groups x 16 column groups
-constexpr int kRowGroups = kStatsThreads / 16, kRowsPerThread = 128 / kRowGroups;
+constexpr int kStatsThreads = 256;   // stats_kernel: 8 warps, one 16-column slice each
+constexpr int kStatsCtasPerSm = 2;
 constexpr float kNvfp4Max = 2688.0f;  // 6 * 448
 constexpr float kFp8Max = 448.0f;
 
@@ -156,13 +156,11 @@ __device__ void amax_bf16(const uint4* p, size_t n8, int b0, int nblk, unsigned*
 // pass 1
 // ---------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(kStatsThreads, 2) stats_kernel(QuantArgs a, int nq_blocks,
-                                                                 int nk_blocks, int nv_blocks) {
+__global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm)
+    stats_kernel(QuantArgs a, int nq_blocks, int nk_blocks, int nv_blocks) {
   __shared__ unsigned red[kStatsThreads / 32];
-  // per warp (16) x column (128): column partials of the two sums, max, min
-  __shared__ float part[4][kStatsThreads / 32][128];
-  __shared__ float col_c0[128];
-  __shared__ int col_bad[128];
+  // per warp: the 32 lanes' column partials, transposed through shared memory
+  __shared__ float xpose[kStatsThreads / 32][32][33];
   int bid = blockIdx.x;
   if (bid < nq_blocks) {
     if (!a.compensate) {
@@ -171,9 +169,10 @@ __global__ void __launch_bounds__(kStatsThreads, 2) stats_kernel(QuantArgs a, in
       return;
     }
     // Persistent over the (b, h, 128-row block) units, the next unit's rows
-    // loaded while the current one is reduced.  Thread = kRowsPerThread rows
-    // (row group rg) x 8 columns (column group cg); the two row groups of a
-    // warp hold the same columns.
+    // loaded while the current one is reduced.  Warp w owns columns
+    // 16w..16w+15 of the unit for all 128 rows (lane: 16-byte column group
+    // 2w + (lane & 1), rows lane/2 + 16k), so every column reduction stays
+    // inside the warp.
     //
     // Each column sum is exact, in two fp32 sums.  With E the largest
     // biased exponent of the column (at least 1) and u = 2^(E - 143) (the
@@ -190,114 +189,107 @@ __global__ void __launch_bounds__(kStatsThreads, 2) stats_kernel(QuantArgs a, in
     // its largest or smallest x, since fp32(x - qbar) is monotonic in x.
     const int nblk = a.Nq / 128;
     const int units = a.B * a.Hq * nblk;
-    const int cg = threadIdx.x & 15, rg = threadIdx.x >> 4;
     const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cg = 2 * wid + (lane & 1);      // 16-byte column group (8 columns)
+    const int rr = lane >> 1;                 // row within each group of 16
     const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(a.q);
-    auto load_unit = [&](int unit, uint32_t (&w)[kRowsPerThread][4]) {
+    auto load_unit = [&](int unit, uint4 (&w)[8]) {
       const int blk = unit % nblk, bh = unit / nblk;
       const int h = bh % a.Hq, b = bh / a.Hq;
 #pragma unroll
-      for (int i = 0; i < kRowsPerThread; ++i) {
-        size_t n = (size_t)blk * 128 + rg + kRowGroups * i;
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+      for (int k = 0; k < 8; ++k) {
+        const size_t n = (size_t)blk * 128 + rr + 16 * k;
+        w[k] = __ldg(reinterpret_cast<const uint4*>(
             q + (((size_t)b * a.Nq + n) * a.Hq + h) * 128 + 8 * cg));
-        w[i][0] = v.x;
-        w[i][1] = v.y;
-        w[i][2] = v.z;
-        w[i][3] = v.w;
       }
     };
+    auto word = [](const uint4& v, int j) -> uint32_t {
+      return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+    };
+    float (*xp)[33] = xpose[wid];
     unsigned m = 0;
-    uint32_t wn[kRowsPerThread][4];
+    uint4 wn[8];
     if (bid < units) load_unit(bid, wn);
     for (int unit = bid; unit < units; unit += nq_blocks) {
-      uint32_t w[kRowsPerThread][4];
+      uint4 w[8];
 #pragma unroll
-      for (int i = 0; i < kRowsPerThread; ++i)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) w[i][k] = wn[i][k];
+      for (int k = 0; k < 8; ++k) w[k] = wn[k];
       if (unit + nq_blocks < units) load_unit(unit + nq_blocks, wn);
       const int blk = unit % nblk, bh = unit / nblk;
       const int h = bh % a.Hq, b = bh / a.Hq;
-      // column max |x| and min (|x| - 1) (zero -> 0xFFFF) on bf16 bit patterns,
-      // two columns per 32-bit word
-      uint32_t* pmax = reinterpret_cast<uint32_t*>(&part[0][0][0]);
-      uint32_t* pmin = reinterpret_cast<uint32_t*>(&part[1][0][0]);
+      // column max |x| and min (|x| - 1) (zero -> 0xFFFF) on bf16 bit
+      // patterns, two columns per 32-bit word, over the 16 lanes of the
+      // column group
+      float C[8];
+      bool bad[8];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int j = 0; j < 4; ++j) {
         uint32_t mx = 0, mn = 0xFFFFFFFFu;
 #pragma unroll
-        for (int i = 0; i < kRowsPerThread; ++i) {
-          const uint32_t mag = w[i][k] & 0x7FFF7FFFu;
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t mag = word(w[k], j) & 0x7FFF7FFFu;
           mx = __vmaxu2(mx, mag);
           mn = __vminu2(mn, __vsub2(mag, 0x00010001u));
         }
-        mx = __vmaxu2(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        mn = __vminu2(mn, __shfl_xor_sync(0xffffffffu, mn, 16));
-        if (lane < 16) {
-          const int c = 8 * cg + 2 * k;
-          pmax[wid * 128 + c] = mx & 0xFFFFu;
-          pmax[wid * 128 + c + 1] = mx >> 16;
-          pmin[wid * 128 + c] = mn & 0xFFFFu;
-          pmin[wid * 128 + c + 1] = mn >> 16;
-        }
-      }
-      __syncthreads();
-      if (threadIdx.x < 128) {
-        const int c = threadIdx.x;
-        uint32_t mx = 0, mn = 0xFFFFu;
 #pragma unroll
-        for (int g2 = 0; g2 < kStatsThreads / 32; ++g2) {
-          mx = max(mx, pmax[g2 * 128 + c]);
-          mn = min(mn, pmin[g2 * 128 + c]);
+        for (int o = 2; o < 32; o <<= 1) {
+          mx = __vmaxu2(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          mn = __vminu2(mn, __shfl_xor_sync(0xffffffffu, mn, o));
         }
-        const int E = max((int)(mx >> 7), 1);
-        const bool any = mn != 0xFFFFu;
-        const int Emin = max((int)((mn + 1) >> 7), 1);
-        const bool bad = E > 247 || (any && Emin < E - 26);
-        col_bad[c] = bad;
-        col_c0[c] = bad ? 0.0f : __uint_as_float(((uint32_t)(E + 7) << 23) | 0x400000u);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const uint32_t cmx = e ? mx >> 16 : mx & 0xFFFFu, cmn = e ? mn >> 16 : mn & 0xFFFFu;
+          const int E = max((int)(cmx >> 7), 1);
+          const int Emin = max((int)((cmn + 1) >> 7), 1);
+          bad[2 * j + e] = E > 247 || (cmn != 0xFFFFu && Emin < E - 26);
+          C[2 * j + e] = bad[2 * j + e] ? 0.0f : __uint_as_float(((uint32_t)(E + 7) << 23) | 0x400000u);
+        }
       }
-      __syncthreads();
+      // per column: the two sums and the extremes over the lane's 8 rows,
+      // stored as lane-major partials [lane][quantity * 8 + column]
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
-        const int c = 8 * cg + t;
-        const float C = col_c0[c];
         float s0 = 0.0f, s1 = 0.0f, xmx = -INFINITY, xmn = INFINITY;
 #pragma unroll
-        for (int i = 0; i < kRowsPerThread; ++i) {
-          const uint32_t wv = w[i][t >> 1];
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t wv = word(w[k], t >> 1);
           const float x = __uint_as_float((t & 1) ? (wv & 0xFFFF0000u) : (wv << 16));
-          const float hi = __fsub_rn(__fadd_rn(x, C), C);
+          const float hi = __fsub_rn(__fadd_rn(x, C[t]), C[t]);
           s0 = __fadd_rn(s0, hi);
           s1 = __fadd_rn(s1, __fsub_rn(x, hi));
           xmx = fmaxf(xmx, x);
           xmn = fminf(xmn, x);
         }
-        s0 = __fadd_rn(s0, __shfl_xor_sync(0xffffffffu, s0, 16));
-        s1 = __fadd_rn(s1, __shfl_xor_sync(0xffffffffu, s1, 16));
-        xmx = fmaxf(xmx, __shfl_xor_sync(0xffffffffu, xmx, 16));
-        xmn = fminf(xmn, __shfl_xor_sync(0xffffffffu, xmn, 16));
-        if (lane < 16) {
-          part[0][wid][c] = s0;
-          part[1][wid][c] = s1;
-          part[2][wid][c] = xmx;
-          part[3][wid][c] = xmn;
+        xp[lane][t] = s0;
+        xp[lane][8 + t] = s1;
+        xp[lane][16 + t] = xmx;
+        xp[lane][24 + t] = xmn;
+      }
+      __syncwarp();
+      // lane L < 16 finishes column group 2w + (L & 1), column t = L >> 1:
+      // sums and extremes over the 16 lanes of that group
+      float s0 = 0.0f, s1 = 0.0f, xmx = -INFINITY, xmn = INFINITY;
+      const int gsel = lane & 1, tc = (lane >> 1) & 7;
+      if (lane < 16) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float* row = xp[2 * i + gsel];
+          s0 = __fadd_rn(s0, row[tc]);
+          s1 = __fadd_rn(s1, row[8 + tc]);
+          xmx = fmaxf(xmx, row[16 + tc]);
+          xmn = fminf(xmn, row[24 + tc]);
         }
       }
-      __syncthreads();
-      if (threadIdx.x < 128) {
-        const int c = threadIdx.x;
-        float s0 = 0.0f, s1 = 0.0f, xmx = -INFINITY, xmn = INFINITY;
+      __syncwarp();   // xpose is rewritten by the next unit
+      // the column's flag (lane L belongs to column group 2w + (L & 1) itself)
+      bool cbad = false;
 #pragma unroll
-        for (int g2 = 0; g2 < kStatsThreads / 32; ++g2) {
-          s0 = __fadd_rn(s0, part[0][g2][c]);
-          s1 = __fadd_rn(s1, part[1][g2][c]);
-          xmx = fmaxf(xmx, part[2][g2][c]);
-          xmn = fminf(xmn, part[3][g2][c]);
-        }
+      for (int t = 0; t < 8; ++t)
+        if (t == tc) cbad = bad[t];
+      if (lane < 16) {
+        const int c = 8 * (2 * wid + gsel) + tc;
         float mean;
-        if (!col_bad[c]) {
+        if (!cbad) {
           mean = __fmul_rn(__fadd_rn(s0, s1), 0.0078125f);
           if (mean != 0.0f && fabsf(mean) < 1.17549435e-38f)
             mean = __double2float_rn(((double)s0 + (double)s1) * 0.0078125);
@@ -319,7 +311,6 @@ __global__ void __launch_bounds__(kStatsThreads, 2) stats_kernel(QuantArgs a, in
         m = max(m, __float_as_uint(fabsf(__fsub_rn(xmx, mean))));
         m = max(m, __float_as_uint(fabsf(__fsub_rn(xmn, mean))));
       }
-      __syncthreads();   // part and col_* are rewritten by the next unit
     }
     m = block_max_u32(m, red);
     if (threadIdx.x == 0 && m) atomicMax(&a.amax[0], m);
@@ -534,7 +525,7 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
   int nq = 0, nk = 0, nv = 0;
   if (a.q) {
     const int units = a.B * a.Hq * (a.Nq / 128);
-    nq = a.compensate ? (units < 2 * sms ? units : 2 * sms)   // persistent, 2 per SM
+    nq = a.compensate ? (units < kStatsCtasPerSm * sms ? units : kStatsCtasPerSm * sms)  // persistent
                       : amax_blocks((size_t)a.B * a.Nq * a.Hq * 128);
   }
   if (a.k) nk = amax_blocks((size_t)a.B * a.Nk * a.Hkv * 128);
