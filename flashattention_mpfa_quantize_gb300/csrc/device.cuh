@@ -29,18 +29,16 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 // ---------------------------------------------------------------------------
 
 // Two E2M1 codes in one byte: y0 in the low nibble, y1 in the high nibble.
-// Magnitudes round to nearest, ties to even, saturating at 6 (the hardware
-// conversion of |y|); the sign bit is copied from y, so a negative value that
-// rounds to zero keeps its sign.
+// Round to nearest, ties to even, saturating at +-6, the sign kept (also
+// for a value that rounds to zero).  The signed hardware conversion does
+// exactly this: it gave the same codes as converting |y| and copying the
+// sign bit for every binary32 input except NaN, in both nibbles.
 __device__ __forceinline__ uint32_t e2m1x2(float y0, float y1) {
   uint16_t r;
   asm("{\n.reg .b8 t;\ncvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\ncvt.u16.u8 %0, t;\n}"
       : "=h"(r)
-      : "f"(fabsf(y1)), "f"(fabsf(y0)));
-  uint32_t b = r & 0xFFu;
-  b |= (__float_as_uint(y0) >> 31) << 3;
-  b |= (__float_as_uint(y1) >> 31) << 7;
-  return b;
+      : "f"(y1), "f"(y0));
+  return r & 0xFFu;
 }
 
 // E4M3 code of a non-negative value: round to nearest even, saturate at 448.
@@ -50,12 +48,9 @@ __device__ __forceinline__ uint32_t e4m3_pos(float t) {
   return r & 0xFFu;
 }
 
-// E4M3 code with the sign bit copied from y.
-__device__ __forceinline__ uint32_t e4m3_signed(float y) {
-  return e4m3_pos(fabsf(y)) | ((__float_as_uint(y) >> 31) << 7);
-}
-
-// Four E4M3 codes of non-negative values packed low byte first.
+// Four E4M3 codes packed low byte first: round to nearest even, saturating
+// at +-448, the sign kept (the signed hardware conversion matched |y| plus
+// the copied sign bit on every binary32 input except NaN).
 __device__ __forceinline__ uint32_t e4m3x4(float a0, float a1, float a2, float a3) {
   uint16_t lo, hi;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(a1), "f"(a0));

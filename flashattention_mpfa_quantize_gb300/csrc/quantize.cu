@@ -139,13 +139,27 @@ __device__ __forceinline__ unsigned block_max_u32(unsigned v, unsigned* red) {
 __device__ void amax_bf16(const uint4* p, size_t n8, int b0, int nblk, unsigned* out,
                           unsigned* red) {
   unsigned m = 0;
-  for (size_t i = (size_t)(blockIdx.x - b0) * blockDim.x + threadIdx.x; i < n8;
-       i += (size_t)nblk * blockDim.x) {
-    uint4 a = __ldg(p + i);
-    m = __vmaxu2(m, a.x & 0x7FFF7FFFu);
-    m = __vmaxu2(m, a.y & 0x7FFF7FFFu);
-    m = __vmaxu2(m, a.z & 0x7FFF7FFFu);
-    m = __vmaxu2(m, a.w & 0x7FFF7FFFu);
+  const size_t stride = (size_t)nblk * blockDim.x;
+  size_t i = (size_t)(blockIdx.x - b0) * blockDim.x + threadIdx.x;
+  // four independent loads in flight per thread
+  for (; i + 3 * stride < n8; i += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = __ldg(p + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      m = __vmaxu2(m, v[u].x & 0x7FFF7FFFu);
+      m = __vmaxu2(m, v[u].y & 0x7FFF7FFFu);
+      m = __vmaxu2(m, v[u].z & 0x7FFF7FFFu);
+      m = __vmaxu2(m, v[u].w & 0x7FFF7FFFu);
+    }
+  }
+  for (; i < n8; i += stride) {
+    uint4 v = __ldg(p + i);
+    m = __vmaxu2(m, v.x & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.y & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.z & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.w & 0x7FFF7FFFu);
   }
   m = max(m & 0xFFFFu, m >> 16);
   m = block_max_u32(m, red);
@@ -475,18 +489,14 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(QuantArgs a) {
       if (fast && xm <= 3.40282347e38f) {
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-          w[t] = e4m3_signed(div_rn(x[4 * t], s, ys)) |
-                 (e4m3_signed(div_rn(x[4 * t + 1], s, ys)) << 8) |
-                 (e4m3_signed(div_rn(x[4 * t + 2], s, ys)) << 16) |
-                 (e4m3_signed(div_rn(x[4 * t + 3], s, ys)) << 24);
+          w[t] = e4m3x4(div_rn(x[4 * t], s, ys), div_rn(x[4 * t + 1], s, ys),
+                        div_rn(x[4 * t + 2], s, ys), div_rn(x[4 * t + 3], s, ys));
         }
       } else {
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-          w[t] = e4m3_signed(__fdiv_rn(x[4 * t], s)) |
-                 (e4m3_signed(__fdiv_rn(x[4 * t + 1], s)) << 8) |
-                 (e4m3_signed(__fdiv_rn(x[4 * t + 2], s)) << 16) |
-                 (e4m3_signed(__fdiv_rn(x[4 * t + 3], s)) << 24);
+          w[t] = e4m3x4(__fdiv_rn(x[4 * t], s), __fdiv_rn(x[4 * t + 1], s),
+                        __fdiv_rn(x[4 * t + 2], s), __fdiv_rn(x[4 * t + 3], s));
         }
       }
       *reinterpret_cast<uint4*>(a.vc + r * 128 + 16 * jj) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -519,7 +529,7 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
   const int sms = num_sms();
   auto amax_blocks = [&](size_t elems) {
     size_t need = (elems / 8 + kStatsThreads - 1) / kStatsThreads;
-    size_t cap = (size_t)sms * 8;
+    size_t cap = (size_t)sms * kStatsCtasPerSm;   // one resident wave
     return (int)(need < cap ? (need ? need : 1) : cap);
   };
   int nq = 0, nk = 0, nv = 0;
