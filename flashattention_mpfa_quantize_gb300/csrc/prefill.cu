@@ -101,6 +101,7 @@ struct Params {
   PrefillArgs a;
   float log2e_rsqrt_d;  // fp32(log2(e) / sqrt(128))
   int q_tiles;
+  int wave;             // CTAs resident at once (one per SM)
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -166,6 +167,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&map_q);
       prefetch_tensormap(&map_k);
       prefetch_tensormap(&map_v);
+      // L2 prefetch of the query-side inputs of the CTA one wave later (one
+      // CTA per SM): its Q tile is otherwise a DRAM miss on its critical path
+      {
+        const unsigned nxt = blockIdx.x + (unsigned)p.wave;
+        if (nxt < gridDim.x) {
+          const int qt2 = p.q_tiles - 1 - (int)(nxt / bh_count);
+          const int bh2 = (int)(nxt % bh_count);
+          const size_t qrow2 = (size_t)bh2 * a.N + (size_t)qt2 * 128;
+          prefetch_l2_bulk(a.qc + qrow2 * 64, 8192);
+          prefetch_l2_bulk(a.qs + qrow2 * 8, 1024);
+          if (T > 0) {
+            const size_t qb2 = ((size_t)bh2 * (a.N / 128) + qt2) * a.T;
+            prefetch_l2_bulk(a.qbc + qb2 * 64, 64u * a.T);
+            prefetch_l2_line(a.qbs + qb2 * 8);
+          }
+        }
+      }
       const int qrow = (b * a.Hq + h) * a.N + qt * 128;
       mbar_expect_tx(bar(kBarQFull), 8192 + 1024);
       tma_load_2d(sbase + kOffQ, &map_q, 0, qrow, bar(kBarQFull));
@@ -505,6 +523,16 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.a = a;
   p.log2e_rsqrt_d = (float)(1.4426950408889634 / std::sqrt(128.0));
   p.q_tiles = a.N / 128;
+  {
+    static int sms = 0;
+    if (!sms) {
+      int dev = 0;
+      cudaGetDevice(&dev);
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (sms <= 0) sms = 148;
+    }
+    p.wave = sms;
+  }
   const unsigned grid = (unsigned)(p.q_tiles * a.B * a.Hq);
   if (grid == 0) return cudaSuccess;
   prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);

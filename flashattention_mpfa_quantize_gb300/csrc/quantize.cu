@@ -39,17 +39,6 @@ __device__ __forceinline__ size_t sf_offset(size_t row, int j) {
   return (row >> 7) * 1024 + (size_t)(j >> 2) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4;
 }
 
-__device__ __forceinline__ void load16_bf16(const __nv_bfloat16* p, float (&x)[16]) {
-  const uint4* p4 = reinterpret_cast<const uint4*>(p);
-  uint4 a = __ldg(p4), b = __ldg(p4 + 1);
-  uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    x[2 * i] = bf16_lo(w[i]);
-    x[2 * i + 1] = bf16_hi(w[i]);
-  }
-}
-
 // E2M1 value of a 4-bit code.
 __device__ __forceinline__ float e2m1_value(uint32_t c) {
   uint32_t e = (c >> 1) & 3u, m = c & 1u;
@@ -346,7 +335,7 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm)
 // ---------------------------------------------------------------------------
 
 // blockIdx.y: 0 = Q rows, 1 = qbar terms, 2 = K rows, 3 = V elements.
-__global__ void __launch_bounds__(kThreads) quant_kernel(QuantArgs a) {
+__global__ void __launch_bounds__(kThreads, 6) quant_kernel(QuantArgs a) {
   const int lane = threadIdx.x & 31;
   const int warps_total = gridDim.x * (kThreads / 32);
   const int gwarp = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
@@ -355,10 +344,10 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(QuantArgs a) {
   const int part = blockIdx.y;
 
   if (part == 0 && a.q) {
-    // One warp per (b, h, 128-row block): 4 rows per step (8 lanes per row,
-    // one 16-element NVFP4 block per lane), the block means of the lane's 16
-    // columns held in registers, the next step's rows loaded before the
-    // current ones are coded.
+    // One warp per (b, h, 128-row block): 8 rows per step (8 lanes per row,
+    // one 16-element NVFP4 block per lane, two rows per lane), the block
+    // means of the lane's 16 columns held in registers, the next step's rows
+    // loaded before the current ones are coded.
     float s = tensor_scale(a.amax[0], kNvfp4Max);
     if (blockIdx.x == 0 && threadIdx.x == 0) *a.s_q = s;
     const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(a.q);
@@ -379,34 +368,51 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(QuantArgs a) {
           m[4 * t + 3] = v.w;
         }
       }
-      auto src = [&](int step) {
-        const size_t n = blk * 128 + 4 * step + ri;
+      // rows 8 step + ri and 8 step + 4 + ri of the block (lane group ri)
+      auto src = [&](int row) {
+        const size_t n = blk * 128 + row;
         return reinterpret_cast<const uint4*>(q + ((b * a.Nq + n) * a.Hq + h) * 128 + 16 * j);
       };
-      uint4 n0 = __ldg(src(0)), n1 = __ldg(src(0) + 1);
+      uint4 nx[4];
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        nx[2 * h2] = __ldg(src(4 * h2 + ri));
+        nx[2 * h2 + 1] = __ldg(src(4 * h2 + ri) + 1);
+      }
 #pragma unroll 1
-      for (int step = 0; step < 32; ++step) {
-        const uint32_t w[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
-        if (step + 1 < 32) {
-          n0 = __ldg(src(step + 1));
-          n1 = __ldg(src(step + 1) + 1);
-        }
-        float x[16];
+      for (int step = 0; step < 16; ++step) {
+        uint4 cx[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          x[2 * i] = bf16_lo(w[i]);
-          x[2 * i + 1] = bf16_hi(w[i]);
-        }
-        if (a.compensate) {
+        for (int i = 0; i < 4; ++i) cx[i] = nx[i];
+        if (step + 1 < 16) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) x[i] = __fsub_rn(x[i], m[i]);
+          for (int h2 = 0; h2 < 2; ++h2) {
+            nx[2 * h2] = __ldg(src(8 * (step + 1) + 4 * h2 + ri));
+            nx[2 * h2 + 1] = __ldg(src(8 * (step + 1) + 4 * h2 + ri) + 1);
+          }
         }
-        const size_t r = bh * a.Nq + blk * 128 + 4 * step + ri;  // output row (b, h, n)
-        uint2 codes;
-        uint32_t sb;
-        nvfp4_block(x, s, codes, sb);
-        *reinterpret_cast<uint2*>(a.qc + r * 64 + 8 * j) = codes;
-        store_scales_tiled(a.qs, r, j, sb);
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const uint32_t w[8] = {cx[2 * h2].x,     cx[2 * h2].y,     cx[2 * h2].z,
+                                 cx[2 * h2].w,     cx[2 * h2 + 1].x, cx[2 * h2 + 1].y,
+                                 cx[2 * h2 + 1].z, cx[2 * h2 + 1].w};
+          float x[16];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            x[2 * i] = bf16_lo(w[i]);
+            x[2 * i + 1] = bf16_hi(w[i]);
+          }
+          if (a.compensate) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[i] = __fsub_rn(x[i], m[i]);
+          }
+          const size_t r = bh * a.Nq + blk * 128 + 8 * step + 4 * h2 + ri;  // output row
+          uint2 codes;
+          uint32_t sb;
+          nvfp4_block(x, s, codes, sb);
+          *reinterpret_cast<uint2*>(a.qc + r * 64 + 8 * j) = codes;
+          store_scales_tiled(a.qs, r, j, sb);
+        }
       }
     }
     return;
@@ -450,19 +456,52 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(QuantArgs a) {
     float s = tensor_scale(a.amax[1], kNvfp4Max);
     if (blockIdx.x == 0 && threadIdx.x == 0) *a.s_k = s;
     const __nv_bfloat16* k = reinterpret_cast<const __nv_bfloat16*>(a.k);
-    size_t rows = (size_t)a.B * a.Hkv * a.Nk;
-    for (size_t u = gwarp; u < rows / 4; u += warps_total) {
-      size_t r = u * 4 + ri;
-      size_t n = r % a.Nk;
-      size_t bh = r / a.Nk;
-      size_t h = bh % a.Hkv, b = bh / a.Hkv;
-      float x[16];
-      load16_bf16(k + ((b * a.Nk + n) * a.Hkv + h) * 128 + 16 * j, x);
-      uint2 codes;
-      uint32_t sb;
-      nvfp4_block(x, s, codes, sb);
-      *reinterpret_cast<uint2*>(a.kc + r * 64 + 8 * j) = codes;
-      store_scales_tiled(a.ks, r, j, sb);
+    // 8 rows per warp step (two per lane), the next step's rows loaded
+    // before the current ones are coded; rows is a multiple of 128
+    const size_t nu = (size_t)a.B * a.Hkv * a.Nk / 8;
+    auto src = [&](size_t r) {
+      const size_t n = r % a.Nk, bh = r / a.Nk;
+      const size_t h = bh % a.Hkv, b = bh / a.Hkv;
+      return reinterpret_cast<const uint4*>(k + ((b * a.Nk + n) * a.Hkv + h) * 128 + 16 * j);
+    };
+    uint4 nx[4];
+    size_t u = gwarp;
+    if (u < nu) {
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        nx[2 * h2] = __ldg(src(8 * u + 4 * h2 + ri));
+        nx[2 * h2 + 1] = __ldg(src(8 * u + 4 * h2 + ri) + 1);
+      }
+    }
+    for (; u < nu; u += warps_total) {
+      uint4 cx[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cx[i] = nx[i];
+      if (u + warps_total < nu) {
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          nx[2 * h2] = __ldg(src(8 * (u + warps_total) + 4 * h2 + ri));
+          nx[2 * h2 + 1] = __ldg(src(8 * (u + warps_total) + 4 * h2 + ri) + 1);
+        }
+      }
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const uint32_t w[8] = {cx[2 * h2].x,     cx[2 * h2].y,     cx[2 * h2].z,
+                               cx[2 * h2].w,     cx[2 * h2 + 1].x, cx[2 * h2 + 1].y,
+                               cx[2 * h2 + 1].z, cx[2 * h2 + 1].w};
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          x[2 * i] = bf16_lo(w[i]);
+          x[2 * i + 1] = bf16_hi(w[i]);
+        }
+        const size_t r = 8 * u + 4 * h2 + ri;
+        uint2 codes;
+        uint32_t sb;
+        nvfp4_block(x, s, codes, sb);
+        *reinterpret_cast<uint2*>(a.kc + r * 64 + 8 * j) = codes;
+        store_scales_tiled(a.ks, r, j, sb);
+      }
     }
     return;
   }
@@ -472,34 +511,62 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(QuantArgs a) {
     const bool fast = s >= kDivLo && s <= kDivHi;
     const float ys = __frcp_rn(s);
     const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(a.v);
-    size_t units = (size_t)a.B * a.Hkv * a.Nk * 8;  // 16-element units
-    size_t tid = (size_t)blockIdx.x * kThreads + threadIdx.x;
-    for (size_t e = tid; e < units; e += (size_t)gridDim.x * kThreads) {
-      size_t r = e >> 3;  // output row (b, h, n)
-      int jj = (int)(e & 7);
-      size_t n = r % a.Nk;
-      size_t bh = r / a.Nk;
-      size_t h = bh % a.Hkv, b = bh / a.Hkv;
+    // 16-element units, two per thread per step (e and e + stride), the
+    // next step's loaded before the current ones are coded
+    const size_t units = (size_t)a.B * a.Hkv * a.Nk * 8;
+    const size_t stride = (size_t)gridDim.x * kThreads;
+    auto src = [&](size_t e) {
+      const size_t r = e >> 3;  // output row (b, h, n)
+      const size_t n = r % a.Nk, bh = r / a.Nk;
+      const size_t h = bh % a.Hkv, b = bh / a.Hkv;
+      return reinterpret_cast<const uint4*>(v + ((b * a.Nk + n) * a.Hkv + h) * 128 +
+                                            16 * (int)(e & 7));
+    };
+    auto code = [&](const uint4& c0, const uint4& c1, size_t e) {
+      const uint32_t w8[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
       float x[16];
-      load16_bf16(v + ((b * a.Nk + n) * a.Hkv + h) * 128 + 16 * jj, x);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        x[2 * i] = bf16_lo(w8[i]);
+        x[2 * i + 1] = bf16_hi(w8[i]);
+      }
       uint32_t w[4];
       float xm = 0.0f;
 #pragma unroll
       for (int i = 0; i < 16; ++i) xm = fmaxf(xm, fabsf(x[i]));
       if (fast && xm <= 3.40282347e38f) {
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
+        for (int t = 0; t < 4; ++t)
           w[t] = e4m3x4(div_rn(x[4 * t], s, ys), div_rn(x[4 * t + 1], s, ys),
                         div_rn(x[4 * t + 2], s, ys), div_rn(x[4 * t + 3], s, ys));
-        }
       } else {
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
+        for (int t = 0; t < 4; ++t)
           w[t] = e4m3x4(__fdiv_rn(x[4 * t], s), __fdiv_rn(x[4 * t + 1], s),
                         __fdiv_rn(x[4 * t + 2], s), __fdiv_rn(x[4 * t + 3], s));
+      }
+      *reinterpret_cast<uint4*>(a.vc + (e >> 3) * 128 + 16 * (int)(e & 7)) =
+          make_uint4(w[0], w[1], w[2], w[3]);
+    };
+    uint4 nx[4];
+    size_t e = (size_t)blockIdx.x * kThreads + threadIdx.x;
+    auto load2 = [&](size_t e0) {
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        if (e0 + h2 * stride < units) {
+          nx[2 * h2] = __ldg(src(e0 + h2 * stride));
+          nx[2 * h2 + 1] = __ldg(src(e0 + h2 * stride) + 1);
         }
       }
-      *reinterpret_cast<uint4*>(a.vc + r * 128 + 16 * jj) = make_uint4(w[0], w[1], w[2], w[3]);
+    };
+    load2(e);
+    for (; e < units; e += 2 * stride) {
+      uint4 cx[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cx[i] = nx[i];
+      load2(e + 2 * stride);
+      code(cx[0], cx[1], e);
+      if (e + stride < units) code(cx[2], cx[3], e + stride);
     }
   }
 }
