@@ -353,7 +353,9 @@ __global__ void __launch_bounds__(kThreads, 6) quant_kernel(QuantArgs a) {
     const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(a.q);
     const int nblk = a.Nq / 128;
     const size_t units = (size_t)a.B * a.Hq * nblk;
-    for (size_t unit = gwarp; unit < units; unit += warps_total) {
+    // last units first: the stats pass read them last, so they may still be in L2
+    for (size_t it = gwarp; it < units; it += warps_total) {
+      const size_t unit = units - 1 - it;
       const size_t bh = unit / nblk, blk = unit % nblk;
       const size_t h = bh % a.Hq, b = bh / a.Hq;
       float m[16];
