@@ -378,6 +378,18 @@ def run_gpu(args):
                 "nominal FP4 (6x) / FP8 (2x) ratios, harmonic mix for equal FP4 and FP8 FLOPs",
                 "quantize_ms": statistics.mean(quant_ms), "prefill_ms": pre}
 
+    # diagnostics outside the timed region: the exp-unit bound (one ex2 per
+    # pair at 32 per clock per SM on this part) and the cost of the rank-one
+    # compensation (the same step with compensation off)
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    f_clk = (clk or {}).get("sm_mhz") or 2070.0
+    t_exp = cfg.pairs / (n_sm * 32 * f_clk * 1e6) * 1e3
+    roofline["exp_unit"] = {"bound_ms": t_exp, "frac": t_exp / pre, "sm_mhz": f_clk,
+                            "rate": "32 ex2 per clock per SM"}
+    roofline["compensation"] = compensation_cost(mp, Q, K, V, cfg, flush, stream,
+                                                 min(args.steps, 50),
+                                                 statistics.mean(quant_ms), pre)
+
     dec = run_decode(mp, dev, stream, peaks, flush, args) if args.only != "prefill" else {}
     e2e = run_e2e(mp, dev, stream, Q, K, V, args) if args.only is None else None
 
@@ -408,6 +420,40 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def compensation_cost(mp, Q, K, V, cfg, flush, stream, steps, quant_on_ms, pre_on_ms):
+    """Quantize and prefill times with the rank-one compensation off and with
+    one term, against the timed step's (compensation on, T=2)."""
+    def timed(compensate, T):
+        z = mp.quantize_qkv(Q, K, V, compensate=compensate, T=T)
+        ws = z["_workspace"]
+        o, lse = mp.prefill(z, causal=cfg.causal)
+        for _ in range(3):
+            flush.zero_()
+            z = mp.quantize_qkv(Q, K, V, compensate=compensate, T=T, workspace=ws)
+            mp.prefill(z, causal=cfg.causal, out=o, lse=lse)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+               for _ in range(max(steps, 1))]
+        for ev in evs:
+            flush.zero_()
+            ev[0].record(stream)
+            z = mp.quantize_qkv(Q, K, V, compensate=compensate, T=T, workspace=ws)
+            ev[1].record(stream)
+            mp.prefill(z, causal=cfg.causal, out=o, lse=lse)
+            ev[2].record(stream)
+        torch.cuda.synchronize()
+        return (statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
+                statistics.mean(e[1].elapsed_time(e[2]) for e in evs))
+    q_off, p_off = timed(False, 2)
+    q_1, p_1 = timed(True, 1)
+    return {"quantize_ms_off": q_off, "prefill_ms_off": p_off,
+            "quantize_ms_T1": q_1, "prefill_ms_T1": p_1,
+            "quantize_ms_T2": quant_on_ms, "prefill_ms_T2": pre_on_ms,
+            "prefill_overhead_pct_T1": 100.0 * (p_1 / p_off - 1.0),
+            "prefill_overhead_pct_T2": 100.0 * (pre_on_ms / p_off - 1.0),
+            "step_overhead_pct_T1": 100.0 * ((q_1 + p_1) / (q_off + p_off) - 1.0),
+            "step_overhead_pct_T2": 100.0 * ((quant_on_ms + pre_on_ms) / (q_off + p_off) - 1.0)}
 
 
 def run_decode(mp, dev, stream, peaks, flush, args):
