@@ -390,6 +390,9 @@ def run_gpu(args):
                                                  min(args.steps, 50),
                                                  statistics.mean(quant_ms), pre)
 
+    bf16 = bf16_sdpa_baseline(Q, K, V, cfg, flush, stream, min(args.steps, 20), flops,
+                              statistics.mean(step_ms), pre)
+
     dec = run_decode(mp, dev, stream, peaks, flush, args) if args.only != "prefill" else {}
     e2e = run_e2e(mp, dev, stream, Q, K, V, args) if args.only is None else None
 
@@ -414,12 +417,44 @@ def run_gpu(args):
                            "T": 2, "step": "mpfa_quantize_qkv + mpfa_prefill",
                            "l2": "flushed (512 MB write) before every step",
                            "parallelism": "replicas" if ws > 1 else "single"},
-                "roofline": roofline, "decode": dec, "e2e": e2e, "cpu_baseline": cpu,
+                "roofline": roofline, "bf16_sdpa": bf16, "decode": dec, "e2e": e2e,
+                "cpu_baseline": cpu,
                 "gpu_launches": args.steps * 3 + dec.get("gpu_launches", 0),
                 "clocks": clk, "wall_s": t_wall}
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def bf16_sdpa_baseline(Q, K, V, cfg, flush, stream, steps, flops, step_ms, pre_ms):
+    """Context, not part of the product: torch's fused bf16 attention (flash,
+    cuDNN or memory-efficient backend, whichever torch picks) on the same
+    unquantized inputs, timed the same way."""
+    try:
+        from torch.nn.attention import SDPBackend, sdpa_kernel
+        import torch.nn.functional as F
+        q, k, v = (t.transpose(1, 2) for t in (Q, K, V))   # [B, H, N, d] views
+        backends = [SDPBackend.FLASH_ATTENTION, SDPBackend.CUDNN_ATTENTION,
+                    SDPBackend.EFFICIENT_ATTENTION]
+        with sdpa_kernel(backends):
+            run = lambda: F.scaled_dot_product_attention(q, k, v, is_causal=cfg.causal,
+                                                         enable_gqa=cfg.Hq != cfg.Hkv)
+            for _ in range(3):
+                run()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(max(steps, 1))]
+            for a, b in evs:
+                flush.zero_()
+                a.record(stream)
+                run()
+                b.record(stream)
+            torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        return {"kernel": "torch scaled_dot_product_attention, bf16, fused backend",
+                "ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+                "speedup_of_step": ms / step_ms, "speedup_of_prefill_kernel": ms / pre_ms}
+    except Exception as ex:  # pragma: no cover - reported, not fatal
+        return {"unavailable": repr(ex)[:200]}
 
 
 def compensation_cost(mp, Q, K, V, cfg, flush, stream, steps, quant_on_ms, pre_on_ms):
