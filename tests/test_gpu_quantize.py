@@ -130,3 +130,29 @@ def test_quantize_block_means_edge_columns(big):
         want, _ = orc.block_means(xs[:, h, :], 128)
         np.testing.assert_array_equal(got[h].view(np.uint32), want.view(np.uint32))
     _check(qz, oracle_quantize(Q, K, K, True, 2), True)
+
+
+@pytest.mark.parametrize("scale", [1e-36, 1e-26, 1e31])
+def test_quantize_extreme_magnitudes(scale):
+    """Tensors scaled so that the block divisors fall outside [2^-90, 2^100]
+    (tiny and huge scales take the IEEE-division path, the others the
+    reciprocal-and-correction path, some blocks of each in one tensor):
+    codes, block scales and tensor scales stay bit-exact with the oracle."""
+    import flashattention_mpfa_quantize_gb300 as mp
+    cfg = mi.custom_prefill(1, 2, 1, 256, False, k_outliers=2, v_outlier_p=0.01, q_offset=True)
+    Q, K, V = mi.prefill_inputs(cfg, "cpu", 5)
+    # per-row magnitudes spread over 2^±10 around `scale` (bf16 subnormals
+    # for the smallest, far from overflow for the largest)
+    rng = np.random.default_rng(2)
+    def spread(t):
+        f = np.exp2(rng.integers(-10, 11, size=(1, t.shape[1], t.shape[2], 1))).astype(np.float32)
+        x = t.float().numpy() * f * np.float32(scale)
+        assert np.isfinite(x).all()
+        return torch.from_numpy(x).to(torch.bfloat16)
+    Q, K, V = spread(Q), spread(K), spread(V)
+    dev = torch.device("cuda:0")
+    for comp in (False, True):
+        qz = mp.quantize_qkv(Q.to(dev), K.to(dev), V.to(dev), compensate=comp, T=2)
+        torch.cuda.synchronize()
+        assert mp.get_error() == 0
+        _check(qz, oracle_quantize(Q, K, V, comp, 2), comp)
