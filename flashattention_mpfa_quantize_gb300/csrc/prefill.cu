@@ -13,10 +13,12 @@
 //
 // One CTA computes one 128-row query tile of one (batch, head):
 //   warp 8    TMA producer: Q tile once, then K / K-scale tiles through a
-//             ring of kKStages stages and V tiles through kVStages stages.
-//   warp 9    QK issuer: block scales into TMEM (tcgen05.cp), QK^T and the
-//             rank-one MMAs into score bank j % 2, QK_{j+2} as soon as the
-//             softmax has loaded S_j into registers.
+//             ring of kKStages stages and V tiles through kVStages stages;
+//             it also copies each K tile's block scales into TMEM
+//             (tcgen05.cp + commit), off the QK issuer's thread.
+//   warp 9    QK issuer: QK^T and the rank-one MMAs into score bank j % 2,
+//             QK_{j+2} as soon as the softmax has loaded S_j into registers
+//             and the scales of tile j+2 are in TMEM.
 //   warp 10   PV issuer: once the softmax has published P_j, PV_j (with the
 //             row sum).  Two issuing threads on two schedulers: each tcgen05
 //             instruction costs a thread on the order of a hundred cycles
@@ -74,7 +76,8 @@ enum : int {
   kBarVFull0 = kBarKFull0 + kKStages,  // +V stage
   kBarODone0 = kBarVFull0 + kVStages,  // +V stage: PV_j (V stage j % 3) completed
   kBarMax0 = kBarODone0 + kVStages,    // +2*quadrant+parity: reference max handed to that parity
-  kNumBars = kBarMax0 + 8,
+  kBarSfReady0 = kBarMax0 + 8,         // +slot: K block scales of tile j copied into slot j % 3
+  kNumBars = kBarSfReady0 + kSfSlots,
 };
 
 // shared memory layout (offsets from a 1024-byte aligned base)
@@ -153,6 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarODone0 + s), 1);
     }
     for (int i = 0; i < 8; ++i) mbar_init(bar(kBarMax0 + i), 32);
+    for (int i = 0; i < kSfSlots; ++i) mbar_init(bar(kBarSfReady0 + i), 1);
     fence_barrier_init();
   }
   if (warp == kWarpMma) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -217,12 +221,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         v_issued = j + 1;
         return true;
       };
-      bool lok = load_k(0) && (nkv < 2 || load_k(1));
-      for (int j = 0; lok && j < nkv; ++j) {
-        if (!load_v(j)) break;
-        if (j + 2 < nkv && !load_k(j + 2)) break;
+      // the K block scales of tile j into TMEM slot j % 3 (tcgen05.cp, then a
+      // commit to SfReady): the QK issuer's MMAs read them there.  Each
+      // tcgen05 instruction or barrier wait costs the issuing thread on the
+      // order of a hundred cycles, and the QK issuer's thread sets the pace.
+      int sf_issued = 0;
+      auto cp_sf = [&](int j) -> bool {
+        const int s = j % kKStages;
+        if (!mbar_wait(bar(kBarKFull0 + s), (j / kKStages) & 1, a.err, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t sfk = tmem + col_sf_k(j % kSfSlots);
+        for (int kc = 0; kc < 2; ++kc)
+          tmem_cp_32x128b_x4(sfk + 4 * kc,
+                             smem_desc(sbase + kOffKs + 1024 * s + 512 * kc, 128, 128, kSwizzleNone));
+        tc_commit(bar(kBarSfReady0 + j % kSfSlots));
+        sf_issued = j + 1;
+        return true;
+      };
+      // K_0..K_3, V_0, V_1 and the scales of tiles 0..2 up front; then, once
+      // the softmax has loaded S_i (so QK_i has completed and K stage i % 4
+      // is free): K_{i+4}, the scales of tile i+3 into slot i % 3, and V_{i+2}
+      // (whose stage PV_{i-1} releases).  SRead for stage i % 4 cannot be a
+      // phase further on: that needs S_{i+4}, whose scales come later here.
+      bool lok = true;
+      for (int j = 0; lok && j < nkv && j < kKStages; ++j) lok = load_k(j);
+      for (int j = 0; lok && j < nkv && j < 2; ++j) lok = load_v(j);
+      for (int j = 0; lok && j < nkv && j < kSfSlots; ++j) lok = cp_sf(j);
+      for (int i = 0; lok && i + 2 < nkv; ++i) {
+        if (!mbar_wait(bar(kBarSRead0 + i % kKStages), (i / kKStages) & 1, a.err, abort_flag))
+          break;
+        if (i + kKStages < nkv && !load_k(i + kKStages)) break;
+        if (i + kSfSlots < nkv && !cp_sf(i + kSfSlots)) break;
+        if (!load_v(i + 2)) break;
       }
-      // drain: every stage's last load must have landed before the CTA exits
+      // drain: the last scale copy completed and every stage's last load
+      // landed before the CTA exits
+      if (sf_issued > 0)
+        mbar_wait(bar(kBarSfReady0 + (sf_issued - 1) % kSfSlots), ((sf_issued - 1) / kSfSlots) & 1,
+                  a.err, nullptr);
       for (int j = k_issued - kKStages > 0 ? k_issued - kKStages : 0; j < k_issued; ++j)
         mbar_wait(bar(kBarKFull0 + j % kKStages), (j / kKStages) & 1, a.err, nullptr);
       for (int j = v_issued - kVStages > 0 ? v_issued - kVStages : 0; j < v_issued; ++j)
@@ -248,14 +284,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // QK_j (and the rank-one MMAs) into score bank j % 2
       auto issue_qk = [&](int j) -> bool {
         const int s = j % kKStages, bk = j & 1;
-        if (!mbar_wait(bar(kBarKFull0 + s), (j / kKStages) & 1, a.err, abort_flag)) return false;
+        // K_j's scales are in slot j % 3 (the producer copied them after K_j
+        // landed, so K_j is in shared memory too); the slot cannot be a phase
+        // further on: the next copy into it needs S_j
+        if (!mbar_wait(bar(kBarSfReady0 + j % kSfSlots), (j / kSfSlots) & 1, a.err, abort_flag))
+          return false;
         tc_fence_after();
-        // slot j % 3: its last reader, QK_{j-3}, completed before QK_{j-2},
-        // whose scores the softmax has loaded (this issue waited for that)
         const uint32_t sfk = tmem + col_sf_k(j % kSfSlots);
-        for (int kc = 0; kc < 2; ++kc)
-          tmem_cp_32x128b_x4(sfk + 4 * kc,
-                             smem_desc(sbase + kOffKs + 1024 * s + 512 * kc, 128, 128, kSwizzleNone));
         const uint32_t dS = tmem + kColS0 + 128 * bk;
         const uint32_t kaddr = sbase + kOffK + 8192 * s;
         for (int kc = 0; kc < 2; ++kc)
