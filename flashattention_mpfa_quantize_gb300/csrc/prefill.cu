@@ -281,6 +281,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem + kColSfQb + 8 * t + 4 * kc,
                 smem_desc(sbase + kOffQbs + 1024 * t + 512 * kc, 128, 128, kSwizzleNone));
       }
+      // shared-memory descriptors built once: the start address sits in the
+      // low field in 16-byte units, so a K stage or a rank-one term (8 KB)
+      // is +512 and the second 64-element K chunk (32 B) +2; every address
+      // stays below 2^18, inside that field
+      const uint64_t dq0 = smem_desc(sbase + kOffQ, 16, 512, kSwizzle64B);
+      const uint64_t dk0 = smem_desc(sbase + kOffK, 16, 512, kSwizzle64B);
+      const uint64_t dqb0 = smem_desc(sbase + kOffQb, 16, 512, kSwizzle64B);
       // QK_j (and the rank-one MMAs) into score bank j % 2
       auto issue_qk = [&](int j) -> bool {
         const int s = j % kKStages, bk = j & 1;
@@ -292,16 +299,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t sfk = tmem + col_sf_k(j % kSfSlots);
         const uint32_t dS = tmem + kColS0 + 128 * bk;
-        const uint32_t kaddr = sbase + kOffK + 8192 * s;
-        for (int kc = 0; kc < 2; ++kc)
-          mma_nvfp4_ss(dS, smem_desc(sbase + kOffQ + 32 * kc, 16, 512, kSwizzle64B),
-                       smem_desc(kaddr + 32 * kc, 16, 512, kSwizzle64B), id_qk,
-                       tmem + kColSfQ + 4 * kc, sfk + 4 * kc, kc > 0 ? 1u : 0u);
-        for (int t = 0; t < T; ++t)
-          for (int kc = 0; kc < 2; ++kc)
-            mma_nvfp4_ss(dS, smem_desc(sbase + kOffQb + 8192 * t + 32 * kc, 16, 512, kSwizzle64B),
-                         smem_desc(kaddr + 32 * kc, 16, 512, kSwizzle64B), id_qk,
-                         tmem + kColSfQb + 8 * t + 4 * kc, sfk + 4 * kc, 1u);
+        const uint64_t dk = dk0 + 512u * (uint32_t)s;
+        mma_nvfp4_ss(dS, dq0, dk, id_qk, tmem + kColSfQ, sfk, 0u);
+        mma_nvfp4_ss(dS, dq0 + 2u, dk + 2u, id_qk, tmem + kColSfQ + 4, sfk + 4, 1u);
+        if (T > 0) {
+          mma_nvfp4_ss(dS, dqb0, dk, id_qk, tmem + kColSfQb, sfk, 1u);
+          mma_nvfp4_ss(dS, dqb0 + 2u, dk + 2u, id_qk, tmem + kColSfQb + 4, sfk + 4, 1u);
+        }
+        if (T > 1) {
+          mma_nvfp4_ss(dS, dqb0 + 512u, dk, id_qk, tmem + kColSfQb + 8, sfk, 1u);
+          mma_nvfp4_ss(dS, dqb0 + 514u, dk + 2u, id_qk, tmem + kColSfQb + 12, sfk + 4, 1u);
+        }
         tc_commit(bar(kBarSFull0 + bk));
         return true;
       };
