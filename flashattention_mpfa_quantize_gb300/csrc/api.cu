@@ -120,6 +120,9 @@ mpfa_status mpfa_quantize_qkv(const void* q_bf16, const void* k_bf16, const void
   } else if (v_out) {
     return MPFA_ERR_INVALID_ARG;
   }
+  if ((q_bf16 && (uint64_t)B * Hq * Nq >= (1ull << 31)) ||
+      ((k_bf16 || v_bf16) && (uint64_t)B * Hkv * Nk >= (1ull << 31)))
+    return MPFA_ERR_INVALID_ARG;
   if (!ok_ptr(workspace) ||
       ws_bytes < mpfa::quant_workspace_bytes(B, q_bf16 ? Nq : 0, Hq, a.compensate))
     return MPFA_ERR_INVALID_ARG;
@@ -196,6 +199,7 @@ mpfa_status mpfa_decode(const void* q_bf16, const mpfa_nvfp4* k_cache, const mpf
       !ok_ptr(v_cache->codes) || !v_cache->tensor_scale)
     return MPFA_ERR_INVALID_ARG;
   if (Hq / Hkv > 16) return MPFA_ERR_UNSUPPORTED;
+  if ((uint64_t)B * Hkv * Lmax >= (1ull << 31)) return MPFA_ERR_INVALID_ARG;
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

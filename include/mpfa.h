@@ -114,7 +114,9 @@ size_t mpfa_quantize_workspace_size(int B, int Nq, int Hq, int compensate);
  *   qbar_out (compensate != 0): codes [B][Hq][Nq/128][T][64], scales [..][T][8].
  *   k_out:  codes [B][Hkv][Nk][64], scales tiled over B*Hkv*Nk rows.
  *   v_out:  codes [B][Hkv][Nk][128].
- *   Nq, Nk multiples of 128 (when the tensor is given), T in {1, 2}.
+ *   Nq, Nk multiples of 128 (when the tensor is given), T in {1, 2};
+ *   B*Hq*Nq and B*Hkv*Nk below 2^31 rows (the row index the kernels and the
+ *   tensor-memory-access coordinates use is 32-bit).
  *   Tensor scales are computed over each whole tensor argument.
  *   workspace: device buffer of at least mpfa_quantize_workspace_size bytes.
  */
@@ -173,7 +175,8 @@ size_t mpfa_decode_workspace_size(int B, int Hq, int Hkv, int d, int Lmax, int k
  * quantized KV cache.
  *   q_bf16 [B][Hq][d]; k_cache codes [B][Hkv][Lmax][64] + tiled scales,
  *   v_cache codes [B][Hkv][Lmax][128]; seqlens int32 [B] (device) with
- *   0 <= seqlens[b] <= Lmax.  Lmax multiple of 128.
+ *   0 <= seqlens[b] <= Lmax.  Lmax multiple of 128; B*Hkv*Lmax below 2^31
+ *   rows.
  *   The query is quantized inside the call (rank-one block = the Hq/Hkv
  *   heads of one KV head).  Keys [s*C, min(L, (s+1)*C)) form split s
  *   (C = kv_chunk, a multiple of 128; 0 = chosen by the library, returned in

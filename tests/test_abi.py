@@ -105,3 +105,16 @@ def test_host_validation_rejects_bad_shapes_and_pointers(lib):
     # more than 16 query heads per KV head
     assert d(_fake(ok), R(k), R(v), _fake(ok), 2, 64, 2, 128, 256, 1, 2, 0, _fake(ok), None,
              None, None, R(used), _fake(ok), 1 << 20, None) == 2
+    # 2^31 cache rows or more (B * Hkv * Lmax)
+    assert d(_fake(ok), R(k), R(v), _fake(ok), 4096, 8, 8, 128, 1 << 16, 1, 2, 0, _fake(ok),
+             None, None, None, R(used), _fake(ok), ctypes.c_size_t(1 << 50), None) == 1
+    # 2^31 rows or more in prefill
+    assert f(R(q), None, R(k), R(v), 1024, 1 << 21, 4, 2, 128, 1, 0, 0, _fake(ok), None,
+             None) == 1
+    # and in quantize (q rows; k/v rows)
+    qq = lib.mpfa_quantize_qkv
+    qq.restype = ctypes.c_int
+    assert qq(_fake(ok), None, None, 1024, 1 << 21, 0, 4, 2, 128, 0, 2, R(q), None, None, None,
+              _fake(ok), ctypes.c_size_t(1 << 50), None) == 1
+    assert qq(None, _fake(ok), _fake(ok), 1024, 0, 1 << 21, 4, 2, 128, 0, 2, None, None, R(k),
+              R(v), _fake(ok), ctypes.c_size_t(1 << 50), None) == 1
