@@ -13,16 +13,18 @@
 //
 // One CTA computes one 128-row query tile of one (batch, head):
 //   warp 8    TMA producer: Q tile once, then K / K-scale tiles through a
-//             ring of kKStages stages and V tiles through kVStages stages;
-//             it also copies each K tile's block scales into TMEM
-//             (tcgen05.cp + commit), off the QK issuer's thread.
-//   warp 9    QK issuer: QK^T and the rank-one MMAs into score bank j % 2,
-//             QK_{j+2} as soon as the softmax has loaded S_j into registers
-//             and the scales of tile j+2 are in TMEM.
+//             ring of kKStages stages and V tiles through kVStages stages.
+//   warps 9, 11  QK issuers, one per score bank (warp 9 the even tiles,
+//             warp 11 the odd ones), each with its own TMEM slot for K's
+//             block scales: tcgen05.cp of the scales, QK^T and the rank-one
+//             MMAs into bank j % 2, QK_{j+2} as soon as the softmax has
+//             loaded S_j into registers.  Neither thread's tiles wait behind
+//             the other's.
 //   warp 10   PV issuer: once the softmax has published P_j, PV_j (with the
-//             row sum).  Two issuing threads on two schedulers: each tcgen05
-//             instruction costs a thread on the order of a hundred cycles
-//             while the softmax warps load the scheduler it shares.
+//             row sum).  Each tcgen05 instruction costs its issuing thread on
+//             the order of a hundred cycles while the softmax warps load the
+//             scheduler it shares, hence three issuing threads on three
+//             schedulers.
 //   warps 0-7 softmax + correction + epilogue.  Warp w owns TMEM lanes
 //             32(w%4)..32(w%4)+31 (query rows) for the KV tiles of parity
 //             w/4: thread = one query row, all 128 keys of its tiles.  The two
@@ -33,7 +35,7 @@
 // Tensor memory (512 columns): S0 [0,128) S1 [128,256) O [256,384) and the
 // row sum l at 384 (columns [384,400) all hold l), P0 [416,448) P1 [448,480),
 // block scales: Q [400,408), K slot 0 [408,416), rank-one terms
-// [480,480+8T), K slots 1-2 [496,512).  P has its own columns so the scores
+// [480,480+8T), K slot 1 [496,504).  P has its own columns so the scores
 // of tile j+2 can be computed into bank j % 2 as soon as the softmax has read
 // tile j, while PV_j still reads P_j.
 #include <cmath>
@@ -52,17 +54,20 @@ namespace {
 
 constexpr int kKStages = 4;   // K tiles: released once the softmax has loaded S
 constexpr int kVStages = 3;   // V tiles: released once PV has read them
-constexpr int kSfSlots = 3;   // TMEM block-scale slots for K (slot j % 3)
-constexpr int kThreads = 352;
-constexpr int kWarpTma = 8, kWarpMma = 9, kWarpPv = 10;
+constexpr int kSfSlots = 2;   // TMEM block-scale slots for K: slot j % 2, one per QK issuer
+constexpr int kThreads = 384;
+// QK issuers: warp 9 for the even tiles (score bank 0, scale slot 0), warp 11
+// for the odd ones (bank 1, slot 1)
+constexpr int kWarpTma = 8, kWarpMma = 9, kWarpPv = 10, kWarpMma2 = 11;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kTileThreads = 128;   // softmax threads that own one KV tile
 constexpr int kTmemCols = 512;
 
 constexpr uint32_t kColS0 = 0, kColO = 256, kColL = 384, kColP0 = 416, kColSfQ = 400,
                    kColSfQb = 480;
-// K block-scale slot i (8 columns each, 4-aligned as the MMA requires)
-__device__ __forceinline__ uint32_t col_sf_k(int i) { return i == 0 ? 408u : 488u + 8u * i; }
+// K block-scale slot i of QK issuer i (8 columns each, 4-aligned as the MMA
+// requires)
+__device__ __forceinline__ uint32_t col_sf_k(int i) { return i == 0 ? 408u : 496u; }
 
 // barrier indices
 enum : int {
@@ -76,8 +81,8 @@ enum : int {
   kBarVFull0 = kBarKFull0 + kKStages,  // +V stage
   kBarODone0 = kBarVFull0 + kVStages,  // +V stage: PV_j (V stage j % 3) completed
   kBarMax0 = kBarODone0 + kVStages,    // +2*quadrant+parity: reference max handed to that parity
-  kBarSfReady0 = kBarMax0 + 8,         // +slot: K block scales of tile j copied into slot j % 3
-  kNumBars = kBarSfReady0 + kSfSlots,
+  kBarQSf = kBarMax0 + 8,              // Q and rank-one block scales copied into TMEM
+  kNumBars = kBarQSf + 1,
 };
 
 // shared memory layout (offsets from a 1024-byte aligned base)
@@ -146,7 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarSFull0 + b2), 1);
       mbar_init(bar(kBarPReady0 + b2), kTileThreads);
     }
-    mbar_init(bar(kBarDrain), 2);   // one commit from each issuer
+    mbar_init(bar(kBarDrain), 3);   // one commit from each issuing thread
+    mbar_init(bar(kBarQSf), 1);
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(bar(kBarSRead0 + s), kTileThreads);
       mbar_init(bar(kBarKFull0 + s), 1);
@@ -156,7 +162,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarODone0 + s), 1);
     }
     for (int i = 0; i < 8; ++i) mbar_init(bar(kBarMax0 + i), 32);
-    for (int i = 0; i < kSfSlots; ++i) mbar_init(bar(kBarSfReady0 + i), 1);
     fence_barrier_init();
   }
   if (warp == kWarpMma) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -221,65 +226,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         v_issued = j + 1;
         return true;
       };
-      // the K block scales of tile j into TMEM slot j % 3 (tcgen05.cp, then a
-      // commit to SfReady): the QK issuer's MMAs read them there.  Each
-      // tcgen05 instruction or barrier wait costs the issuing thread on the
-      // order of a hundred cycles, and the QK issuer's thread sets the pace.
-      int sf_issued = 0;
-      auto cp_sf = [&](int j) -> bool {
-        const int s = j % kKStages;
-        if (!mbar_wait(bar(kBarKFull0 + s), (j / kKStages) & 1, a.err, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t sfk = tmem + col_sf_k(j % kSfSlots);
-        for (int kc = 0; kc < 2; ++kc)
-          tmem_cp_32x128b_x4(sfk + 4 * kc,
-                             smem_desc(sbase + kOffKs + 1024 * s + 512 * kc, 128, 128, kSwizzleNone));
-        tc_commit(bar(kBarSfReady0 + j % kSfSlots));
-        sf_issued = j + 1;
-        return true;
-      };
-      // K_0..K_3, V_0, V_1 and the scales of tiles 0..2 up front; then, once
-      // the softmax has loaded S_i (so QK_i has completed and K stage i % 4
-      // is free): K_{i+4}, the scales of tile i+3 into slot i % 3, and V_{i+2}
-      // (whose stage PV_{i-1} releases).  SRead for stage i % 4 cannot be a
-      // phase further on: that needs S_{i+4}, whose scales come later here.
-      bool lok = true;
-      for (int j = 0; lok && j < nkv && j < kKStages; ++j) lok = load_k(j);
-      for (int j = 0; lok && j < nkv && j < 2; ++j) lok = load_v(j);
-      for (int j = 0; lok && j < nkv && j < kSfSlots; ++j) lok = cp_sf(j);
-      for (int i = 0; lok && i + 2 < nkv; ++i) {
-        if (!mbar_wait(bar(kBarSRead0 + i % kKStages), (i / kKStages) & 1, a.err, abort_flag))
-          break;
-        if (i + kKStages < nkv && !load_k(i + kKStages)) break;
-        if (i + kSfSlots < nkv && !cp_sf(i + kSfSlots)) break;
-        if (!load_v(i + 2)) break;
+      bool lok = load_k(0) && (nkv < 2 || load_k(1));
+      for (int j = 0; lok && j < nkv; ++j) {
+        if (!load_v(j)) break;
+        if (j + 2 < nkv && !load_k(j + 2)) break;
       }
-      // drain: the last scale copy completed and every stage's last load
-      // landed before the CTA exits
-      if (sf_issued > 0)
-        mbar_wait(bar(kBarSfReady0 + (sf_issued - 1) % kSfSlots), ((sf_issued - 1) / kSfSlots) & 1,
-                  a.err, nullptr);
+      // drain: every stage's last load must have landed before the CTA exits
       for (int j = k_issued - kKStages > 0 ? k_issued - kKStages : 0; j < k_issued; ++j)
         mbar_wait(bar(kBarKFull0 + j % kKStages), (j / kKStages) & 1, a.err, nullptr);
       for (int j = v_issued - kVStages > 0 ? v_issued - kVStages : 0; j < v_issued; ++j)
         mbar_wait(bar(kBarVFull0 + j % kVStages), (j / kVStages) & 1, a.err, nullptr);
     }
-  } else if (warp == kWarpMma) {
-    // ---------------- QK issuer ----------------
+  } else if (warp == kWarpMma || warp == kWarpMma2) {
+    // ---------------- QK issuers ----------------
+    // One thread per score bank, each issuing every other tile with its own
+    // K scale slot: each accumulator and slot has a single issuing thread,
+    // and neither thread's tiles wait behind the other's.
     if (lane == 0) {
+      const int par = warp == kWarpMma ? 0 : 1;
       const uint32_t id_qk = idesc_nvfp4(128, 128);
-      bool ok = mbar_wait(bar(kBarQFull), 0, a.err, abort_flag) &&
-                mbar_wait(bar(kBarQbReady), 0, a.err, abort_flag);
-      if (ok) {
-        tc_fence_after();
-        for (int kc = 0; kc < 2; ++kc)
-          tmem_cp_32x128b_x4(tmem + kColSfQ + 4 * kc,
-                             smem_desc(sbase + kOffQs + 512 * kc, 128, 128, kSwizzleNone));
-        for (int t = 0; t < T; ++t)
+      bool ok;
+      if (par == 0) {
+        ok = mbar_wait(bar(kBarQFull), 0, a.err, abort_flag) &&
+             mbar_wait(bar(kBarQbReady), 0, a.err, abort_flag);
+        if (ok) {
+          tc_fence_after();
           for (int kc = 0; kc < 2; ++kc)
-            tmem_cp_32x128b_x4(
-                tmem + kColSfQb + 8 * t + 4 * kc,
-                smem_desc(sbase + kOffQbs + 1024 * t + 512 * kc, 128, 128, kSwizzleNone));
+            tmem_cp_32x128b_x4(tmem + kColSfQ + 4 * kc,
+                               smem_desc(sbase + kOffQs + 512 * kc, 128, 128, kSwizzleNone));
+          for (int t = 0; t < T; ++t)
+            for (int kc = 0; kc < 2; ++kc)
+              tmem_cp_32x128b_x4(
+                  tmem + kColSfQb + 8 * t + 4 * kc,
+                  smem_desc(sbase + kOffQbs + 1024 * t + 512 * kc, 128, 128, kSwizzleNone));
+          tc_commit(bar(kBarQSf));
+        }
+      } else {
+        // the other issuer has copied the Q and rank-one scales into TMEM
+        // (its commit also says Q and the rank-one operand are in shared
+        // memory)
+        ok = mbar_wait(bar(kBarQSf), 0, a.err, abort_flag);
+        if (ok) tc_fence_after();
       }
       // shared-memory descriptors built once: the start address sits in the
       // low field in 16-byte units, so a K stage or a rank-one term (8 KB)
@@ -291,13 +278,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // QK_j (and the rank-one MMAs) into score bank j % 2
       auto issue_qk = [&](int j) -> bool {
         const int s = j % kKStages, bk = j & 1;
-        // K_j's scales are in slot j % 3 (the producer copied them after K_j
-        // landed, so K_j is in shared memory too); the slot cannot be a phase
-        // further on: the next copy into it needs S_j
-        if (!mbar_wait(bar(kBarSfReady0 + j % kSfSlots), (j / kSfSlots) & 1, a.err, abort_flag))
-          return false;
+        if (!mbar_wait(bar(kBarKFull0 + s), (j / kKStages) & 1, a.err, abort_flag)) return false;
         tc_fence_after();
+        // K_j's scales into this issuer's slot j % 2; its last reader,
+        // QK_{j-2}, completed before the softmax loaded S_{j-2} (waited for)
         const uint32_t sfk = tmem + col_sf_k(j % kSfSlots);
+        for (int kc = 0; kc < 2; ++kc)
+          tmem_cp_32x128b_x4(sfk + 4 * kc,
+                             smem_desc(sbase + kOffKs + 1024 * s + 512 * kc, 128, 128, kSwizzleNone));
         const uint32_t dS = tmem + kColS0 + 128 * bk;
         const uint64_t dk = dk0 + 512u * (uint32_t)s;
         mma_nvfp4_ss(dS, dq0, dk, id_qk, tmem + kColSfQ, sfk, 0u);
@@ -313,12 +301,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(bar(kBarSFull0 + bk));
         return true;
       };
-      if (ok) ok = issue_qk(0) && (nkv < 2 || issue_qk(1));
-      for (int j = 2; ok && j < nkv; ++j) {
-        // the softmax has loaded S_{j-2}: bank j % 2 is free.  SRead for
-        // stage (j-2) % 4 cannot be a phase further on: that needs S_{j+2}.
-        if (!mbar_wait(bar(kBarSRead0 + (j - 2) % kKStages), ((j - 2) / kKStages) & 1, a.err,
-                       abort_flag))
+      for (int j = par; ok && j < nkv; j += 2) {
+        // the softmax has loaded S_{j-2}: bank j % 2 and slot j % 2 are free.
+        // SRead for stage (j-2) % 4 cannot be a phase further on: that needs
+        // S_{j+2}.
+        if (j >= 2 && !mbar_wait(bar(kBarSRead0 + (j - 2) % kKStages), ((j - 2) / kKStages) & 1,
+                                 a.err, abort_flag))
           break;
         if (!issue_qk(j)) break;
       }
