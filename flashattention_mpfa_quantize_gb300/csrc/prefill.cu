@@ -11,33 +11,47 @@
 // denominator consumes exactly the codes the numerator consumes (the
 // explainer's Direct-P section states that rule) at no extra instruction.
 //
-// One CTA computes one 128-row query tile of one (batch, head):
-//   warp 8    TMA producer: Q tile once, then K / K-scale tiles through a
-//             ring of kKStages stages and V tiles through kVStages stages.
-//   warps 9, 11  QK issuers, one per score bank (warp 9 the even tiles,
-//             warp 11 the odd ones), each with its own TMEM slot for K's
-//             block scales: tcgen05.cp of the scales, QK^T and the rank-one
-//             MMAs into bank j % 2, QK_{j+2} as soon as the softmax has
-//             loaded S_j into registers.  Neither thread's tiles wait behind
-//             the other's.
-//   warp 10   PV issuer: once the softmax has published P_j, PV_j (with the
-//             row sum).  Each tcgen05 instruction costs its issuing thread on
-//             the order of a hundred cycles while the softmax warps load the
-//             scheduler it shares, hence three issuing threads on three
-//             schedulers.
+// Persistent: one CTA per SM walks a fixed list of work items (128-row query
+// tile of one (batch, head)), heaviest causal items first, dealt to the CTAs
+// in a snake order so every CTA gets a near-equal share of KV tiles.  All
+// roles see the CTA's KV tiles as one stream g = 0, 1, ... across items, and
+// every ring, bank and barrier phase is indexed by g, so the next item's Q,
+// K and scores are in flight while the previous item's last tiles and its
+// epilogue finish.
+//   warp 8    TMA producer (whole warp): per item the Q tile and scales into
+//             one of two Q buffers, the rank-one operand tile built by all 32
+//             lanes; K / K-scale tiles through kKStages stages and V tiles
+//             through kVStages stages.
+//   warps 9, 11  QK issuers, one per score bank (warp 9 the even tiles of
+//             the stream, warp 11 the odd ones), each with its own TMEM slot
+//             for K's block scales: tcgen05.cp of the scales, QK^T and the
+//             rank-one MMAs into bank g % 2, QK_{g+2} as soon as the softmax
+//             has loaded S_g into registers.  The issuer of an item's first
+//             tile also copies that item's Q scales into TMEM, once every
+//             score product of the previous item has completed.
+//   warp 10   PV issuer: once the softmax has published P_g, PV_g (with the
+//             row sum); an item's first PV (which overwrites O) waits until
+//             the previous item's O has been read out.  Each tcgen05
+//             instruction costs its issuing thread on the order of a hundred
+//             cycles while the softmax warps load the scheduler it shares,
+//             hence three issuing threads on three schedulers.
 //   warps 0-7 softmax + correction + epilogue.  Warp w owns TMEM lanes
-//             32(w%4)..32(w%4)+31 (query rows) for the KV tiles of parity
-//             w/4: thread = one query row, all 128 keys of its tiles.  The two
-//             warps on a scheduler thus alternate tiles, so one's
+//             32(w%4)..32(w%4)+31 (query rows) for the KV tiles of stream
+//             parity w/4: thread = one query row, all 128 keys of its tiles.
+//             The two warps on a scheduler thus alternate tiles, so one's
 //             exponentials overlap the other's loads, maxima and stores; the
 //             only exchange is the row's reference max, handed from the
-//             owner of tile j to the owner of tile j+1 through shared memory.
+//             owner of tile g to the owner of tile g+1 through shared memory
+//             (also across items, where the value is not used, to keep the
+//             hand-overs strictly alternating).  The owner of an item's last
+//             tile reads O and l out of TMEM, frees them for the next item,
+//             and writes O (bf16) and LSE while the other warps go on.
 // Tensor memory (512 columns): S0 [0,128) S1 [128,256) O [256,384) and the
 // row sum l at 384 (columns [384,400) all hold l), P0 [416,448) P1 [448,480),
 // block scales: Q [400,408), K slot 0 [408,416), rank-one terms
 // [480,480+8T), K slot 1 [496,504).  P has its own columns so the scores
-// of tile j+2 can be computed into bank j % 2 as soon as the softmax has read
-// tile j, while PV_j still reads P_j.
+// of tile g+2 can be computed into bank g % 2 as soon as the softmax has read
+// tile g, while PV_g still reads P_g.
 #include <cmath>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -49,15 +63,17 @@ namespace mpfa {
 
 bool make_map_2d_u8(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows,
                     uint32_t box_rows, CUtensorMapSwizzle sw);
+bool make_map_2d_u8_box(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t pitch,
+                        uint64_t rows, uint32_t box_inner, uint32_t box_rows,
+                        CUtensorMapSwizzle sw);
 
 namespace {
 
 constexpr int kKStages = 4;   // K tiles: released once the softmax has loaded S
 constexpr int kVStages = 3;   // V tiles: released once PV has read them
-constexpr int kSfSlots = 2;   // TMEM block-scale slots for K: slot j % 2, one per QK issuer
 constexpr int kThreads = 384;
-// QK issuers: warp 9 for the even tiles (score bank 0, scale slot 0), warp 11
-// for the odd ones (bank 1, slot 1)
+// QK issuers: warp 9 for the even tiles of the stream (score bank 0, scale
+// slot 0), warp 11 for the odd ones (bank 1, slot 1)
 constexpr int kWarpTma = 8, kWarpMma = 9, kWarpPv = 10, kWarpMma2 = 11;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kTileThreads = 128;   // softmax threads that own one KV tile
@@ -71,46 +87,76 @@ __device__ __forceinline__ uint32_t col_sf_k(int i) { return i == 0 ? 408u : 496
 
 // barrier indices
 enum : int {
-  kBarQFull = 0,
-  kBarQbReady = 1,
-  kBarSFull0 = 2,                      // +bank: scores of tile j in bank j % 2
-  kBarPReady0 = 4,                     // +bank: P_j published in P bank j % 2
-  kBarDrain = 6,
-  kBarSRead0 = 7,                      // +K stage: S_j (K stage j % 4) loaded by the softmax
+  kBarQFull0 = 0,                      // +Q buffer: Q tile, scales and rank-one operand in smem
+  kBarQEmpty0 = 2,                     // +Q buffer: both QK issuers done with that buffer's item
+  kBarQSf = 4,                         // the current item's Q block scales copied into TMEM
+  kBarOnes = 5,                        // E4M3 ones beside the V stages written
+  kBarOFree = 6,                       // the previous item's O and l read out of TMEM
+  kBarDrain = 7,
+  kBarSFull0 = 8,                      // +bank: scores of tile g in bank g % 2
+  kBarPReady0 = 10,                    // +bank: P_g published in P bank g % 2
+  kBarSRead0 = 12,                     // +K stage: S_g (K stage g % 4) loaded by the softmax
   kBarKFull0 = kBarSRead0 + kKStages,  // +K stage
   kBarVFull0 = kBarKFull0 + kKStages,  // +V stage
-  kBarODone0 = kBarVFull0 + kVStages,  // +V stage: PV_j (V stage j % 3) completed
+  kBarODone0 = kBarVFull0 + kVStages,  // +V stage: PV_g (V stage g % 3) completed
   kBarMax0 = kBarODone0 + kVStages,    // +2*quadrant+parity: reference max handed to that parity
-  kBarQSf = kBarMax0 + 8,              // Q and rank-one block scales copied into TMEM
-  kNumBars = kBarQSf + 1,
+  kNumBars = kBarMax0 + 8,
 };
 
 // shared memory layout (offsets from a 1024-byte aligned base)
-constexpr uint32_t kOffQ = 0;                           // 8 KB
-constexpr uint32_t kOffQb = kOffQ + 8192;               // 2 x 8 KB
-constexpr uint32_t kOffK = kOffQb + 2 * 8192;            // kKStages x 8 KB
-// V stage s: 16 KB of V at kOffV + 32 KB * s, then 16 KB of E4M3 ones (the
-// second 128-byte atom of the N = 144 operand, kVOnesLbo bytes further on)
-constexpr uint32_t kVStageBytes = 32768, kVOnesLbo = 16384;
-constexpr uint32_t kOffV = kOffK + kKStages * 8192;           // kVStages x 32 KB
-constexpr uint32_t kOffQs = kOffV + kVStages * kVStageBytes;  // 1 KB
-constexpr uint32_t kOffQbs = kOffQs + 1024;                   // 2 x 1 KB
-constexpr uint32_t kOffKs = kOffQbs + 2048;                   // kKStages x 1 KB
+constexpr uint32_t kOffQ = 0;                            // 2 Q buffers x 8 KB
+constexpr uint32_t kOffQb = kOffQ + 2 * 8192;            // 2 Q buffers x 2 terms x 8 KB
+constexpr uint32_t kOffK = kOffQb + 2 * 2 * 8192;        // kKStages x 8 KB
+constexpr uint32_t kVStageBytes = 16384;
+constexpr uint32_t kOffV = kOffK + kKStages * 8192;      // kVStages x 16 KB
+// 16 KB of E4M3 ones: the second 128-byte atom of every V stage's N = 144
+// operand (each stage's descriptor reaches it with its own leading offset)
+constexpr uint32_t kOffOnes = kOffV + kVStages * kVStageBytes;
+// O staging, one 32 KB tile per softmax parity: two 64-column halves of
+// 128 rows x 128 bytes in the 128-byte swizzle of the TMA store, each warp
+// storing its own 32 rows
+constexpr uint32_t kOffOst = kOffOnes + 16384;
+constexpr uint32_t kOffQs = kOffOst + 2 * 32768;         // 2 Q buffers x 1 KB
+constexpr uint32_t kOffQbs = kOffQs + 2 * 1024;               // 2 Q buffers x 2 terms x 1 KB
+constexpr uint32_t kOffKs = kOffQbs + 2 * 2048;               // kKStages x 1 KB
 constexpr uint32_t kOffMax = kOffKs + kKStages * 1024;        // 128 floats: reference max per row
 constexpr uint32_t kOffBar = kOffMax + 512;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemUsed = kOffMisc + 64;
 // More than half an SM's shared memory, so a single CTA owns the SM and its
 // 512 TMEM columns.
-constexpr uint32_t kSmemBytes = 168 * 1024;
+constexpr uint32_t kSmemBytes = 224 * 1024;
 static_assert(kSmemUsed + 1024 <= kSmemBytes, "shared memory layout overflow");
+// every address a tcgen05 descriptor holds fits its 14-bit field (16-byte
+// units) even after the 1 KB alignment of the dynamic shared base
+static_assert(kOffMax + 2048 <= (1u << 18), "descriptor address field overflow");
 
 struct Params {
   PrefillArgs a;
   float log2e_rsqrt_d;  // fp32(log2(e) / sqrt(128))
   int q_tiles;
-  int wave;             // CTAs resident at once (one per SM)
+  int items;            // q_tiles * B * Hq work items
 };
+
+// One work item: query tile qt of (batch, head) bh, nkv KV tiles.
+struct Item {
+  int qt, bh, nkv;
+};
+
+// Item k of this CTA, or false past the end.  Items are numbered heaviest
+// causal query tile first; round k deals items [kG, kG + G) to the G CTAs,
+// in reverse on odd rounds, so the per-CTA sums of KV tiles stay within one
+// round's spread.
+__device__ __forceinline__ bool item_of(const Params& p, int k, Item& it) {
+  const int G = (int)gridDim.x, c = (int)blockIdx.x;
+  const int i = k * G + ((k & 1) ? G - 1 - c : c);
+  if (i >= p.items) return false;
+  const int bh_count = p.a.B * p.a.Hq;
+  it.qt = p.q_tiles - 1 - i / bh_count;
+  it.bh = i % bh_count;
+  it.nkv = p.a.causal ? it.qt + 1 : p.q_tiles;
+  return true;
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -121,22 +167,15 @@ __device__ __forceinline__ float ex2(float x) {
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_k,
-                   const __grid_constant__ CUtensorMap map_v, const Params p) {
+                   const __grid_constant__ CUtensorMap map_v,
+                   const __grid_constant__ CUtensorMap map_o, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const PrefillArgs& a = p.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // work unit: heavy causal tiles first
-  const int bh_count = a.B * a.Hq;
-  const int qt = p.q_tiles - 1 - (int)(blockIdx.x / bh_count);
-  const int bh = (int)(blockIdx.x % bh_count);
-  const int h = bh % a.Hq, b = bh / a.Hq;
-  const int g = a.Hq / a.Hkv;
-  const int hk = h / g;
-  const int nkv = a.causal ? qt + 1 : a.N / 128;
+  const int g_kv = a.Hq / a.Hkv;
   const int T = a.compensate ? a.T : 0;
 
   auto bar = [&](int i) { return sbase + kOffBar + 8u * (uint32_t)i; };
@@ -145,14 +184,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    mbar_init(bar(kBarQFull), 1);
-    mbar_init(bar(kBarQbReady), kSoftmaxThreads);
     for (int b2 = 0; b2 < 2; ++b2) {
+      mbar_init(bar(kBarQFull0 + b2), 2);    // TMA arrive.expect_tx + rank-one operand built
+      mbar_init(bar(kBarQEmpty0 + b2), 2);   // one commit from each QK issuer
       mbar_init(bar(kBarSFull0 + b2), 1);
       mbar_init(bar(kBarPReady0 + b2), kTileThreads);
     }
-    mbar_init(bar(kBarDrain), 3);   // one commit from each issuing thread
     mbar_init(bar(kBarQSf), 1);
+    mbar_init(bar(kBarOnes), kSoftmaxThreads);
+    mbar_init(bar(kBarOFree), kTileThreads);
+    mbar_init(bar(kBarDrain), 3);   // one commit from each issuing thread
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(bar(kBarSRead0 + s), kTileThreads);
       mbar_init(bar(kBarKFull0 + s), 1);
@@ -171,144 +212,243 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == kWarpTma) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer (whole warp) ----------------
+    // every lane polls the same barriers (so the warp stays converged), lane
+    // 0 issues the copies, all lanes build the rank-one operand tile
+    auto wait_all = [&](int b2, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar(b2), parity, a.err, abort_flag));
+    };
     if (lane == 0) {
       prefetch_tensormap(&map_q);
       prefetch_tensormap(&map_k);
       prefetch_tensormap(&map_v);
-      // L2 prefetch of the query-side inputs of the CTA one wave later (one
-      // CTA per SM): its Q tile is otherwise a DRAM miss on its critical path
-      {
-        const unsigned nxt = blockIdx.x + (unsigned)p.wave;
-        if (nxt < gridDim.x) {
-          const int qt2 = p.q_tiles - 1 - (int)(nxt / bh_count);
-          const int bh2 = (int)(nxt % bh_count);
-          const size_t qrow2 = (size_t)bh2 * a.N + (size_t)qt2 * 128;
+      prefetch_tensormap(&map_o);
+    }
+    const int nblk = a.N / 128;
+    // Q tile, its scales and the rank-one operand of item k into buffer k % 2
+    auto load_q = [&](int k, const Item& it) -> bool {
+      const int buf = k & 1;
+      // the buffer held item k-2: both QK issuers are done with it
+      if (k >= 2 && !wait_all(kBarQEmpty0 + buf, ((k - 2) >> 1) & 1)) return false;
+      const size_t qrow = (size_t)it.bh * a.N + (size_t)it.qt * 128;
+      if (lane == 0) {
+        mbar_expect_tx(bar(kBarQFull0 + buf), 8192 + 1024);
+        tma_load_2d(sbase + kOffQ + 8192 * buf, &map_q, 0, (int)qrow, bar(kBarQFull0 + buf));
+        bulk_load(sbase + kOffQs + 1024 * buf, a.qs + qrow * 8, 1024, bar(kBarQFull0 + buf));
+        // L2 prefetch of the next item's query-side inputs: its Q tile is
+        // otherwise a DRAM miss when its turn comes
+        Item nx;
+        if (item_of(p, k + 1, nx)) {
+          const size_t qrow2 = (size_t)nx.bh * a.N + (size_t)nx.qt * 128;
           prefetch_l2_bulk(a.qc + qrow2 * 64, 8192);
           prefetch_l2_bulk(a.qs + qrow2 * 8, 1024);
           if (T > 0) {
-            const size_t qb2 = ((size_t)bh2 * (a.N / 128) + qt2) * a.T;
+            const size_t qb2 = ((size_t)nx.bh * nblk + nx.qt) * a.T;
             prefetch_l2_bulk(a.qbc + qb2 * 64, 64u * a.T);
             prefetch_l2_line(a.qbs + qb2 * 8);
           }
         }
       }
-      const int qrow = (b * a.Hq + h) * a.N + qt * 128;
-      mbar_expect_tx(bar(kBarQFull), 8192 + 1024);
-      tma_load_2d(sbase + kOffQ, &map_q, 0, qrow, bar(kBarQFull));
-      bulk_load(sbase + kOffQs, a.qs + (size_t)qrow * 8, 1024, bar(kBarQFull));
-      const int kvrow0 = (b * a.Hkv + hk) * a.N;
-      // loads in the order the MMA warp consumes them: K_0, K_1, then
-      // V_j and K_{j+2} for j = 0, 1, ...
-      int k_issued = 0, v_issued = 0;
-      auto load_k = [&](int j) -> bool {
-        const int s = j % kKStages;
-        // stage s held K_{j-4}: free once the softmax has loaded S_{j-4}
-        if (j >= kKStages &&
-            !mbar_wait(bar(kBarSRead0 + s), ((j / kKStages) - 1) & 1, a.err, abort_flag))
-          return false;
-        const int row = kvrow0 + j * 128;
+      // rank-one operand: every row holds the block's term t (same 64
+      // bytes), written with the 64-byte swizzle the TMA applies to Q and K;
+      // its block scales likewise, one 8-byte row per query row
+      for (int t = 0; t < T; ++t) {
+        const size_t qb = ((size_t)it.bh * nblk + it.qt) * a.T + t;
+        const uint4* src = reinterpret_cast<const uint4*>(a.qbc + qb * 64);
+        const uint4 v0 = src[0], v1 = src[1], v2 = src[2], v3 = src[3];
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(a.qbs + qb * 8);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(a.qbs + qb * 8 + 4);
+        uint8_t* qbt = smem + kOffQb + 16384 * buf + 8192 * t;
+        uint32_t* qbst = reinterpret_cast<uint32_t*>(smem + kOffQbs + 2048 * buf + 1024 * t);
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+          const int r = lane + 32 * rr, sw = (r >> 1) & 3;
+          uint4* dst = reinterpret_cast<uint4*>(qbt + 64 * r);
+          dst[0 ^ sw] = v0;
+          dst[1 ^ sw] = v1;
+          dst[2 ^ sw] = v2;
+          dst[3 ^ sw] = v3;
+          qbst[r] = w0;
+          qbst[128 + r] = w1;
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarQFull0 + buf));
+      return true;
+    };
+    // K and V cursors over this CTA's items: tile g of the stream is tile
+    // g - g0 of the cursor's item, whose K/V rows start at row0
+    struct Cur {
+      int k, g0, n, row0;
+    };
+    auto enter = [&](Cur& c, int k) -> bool {
+      Item it;
+      if (!item_of(p, k, it)) return false;
+      const int b = it.bh / a.Hq, hk = (it.bh % a.Hq) / g_kv;
+      c.k = k;
+      c.n = it.nkv;
+      c.row0 = (b * a.Hkv + hk) * a.N;
+      return true;
+    };
+    Cur ck{0, 0, 0, 0}, cv{0, 0, 0, 0};
+    int k_issued = 0, v_issued = 0, q_issued = 0;
+    bool lok = enter(ck, 0) && enter(cv, 0);
+    {
+      Item it0;
+      lok = lok && item_of(p, 0, it0) && load_q(0, it0);
+    }
+    if (lok) q_issued = 1;
+    auto load_k = [&](int g) -> bool {
+      while (g >= ck.g0 + ck.n) {   // the K cursor enters the next item: its Q first
+        const int g0n = ck.g0 + ck.n;
+        if (!enter(ck, ck.k + 1)) return false;
+        ck.g0 = g0n;
+        Item it;
+        item_of(p, ck.k, it);
+        if (!load_q(ck.k, it)) return false;
+        q_issued = ck.k + 1;
+      }
+      const int s = g % kKStages;
+      // stage s held K_{g-4}: free once the softmax has loaded S_{g-4}
+      if (g >= kKStages && !wait_all(kBarSRead0 + s, ((g / kKStages) - 1) & 1)) return false;
+      if (lane == 0) {
+        const int row = ck.row0 + (g - ck.g0) * 128;
         mbar_expect_tx(bar(kBarKFull0 + s), 8192 + 1024);
         tma_load_2d(sbase + kOffK + s * 8192, &map_k, 0, row, bar(kBarKFull0 + s));
         bulk_load(sbase + kOffKs + s * 1024, a.ks + (size_t)row * 8, 1024, bar(kBarKFull0 + s));
-        k_issued = j + 1;
-        return true;
-      };
-      auto load_v = [&](int j) -> bool {
-        const int s = j % kVStages;
-        // stage s held V_{j-3}: free once PV_{j-3} has completed
-        if (j >= kVStages &&
-            !mbar_wait(bar(kBarODone0 + s), ((j / kVStages) - 1) & 1, a.err, abort_flag))
-          return false;
-        mbar_expect_tx(bar(kBarVFull0 + s), 16384);
-        tma_load_2d(sbase + kOffV + s * kVStageBytes, &map_v, 0, kvrow0 + j * 128,
-                    bar(kBarVFull0 + s));
-        v_issued = j + 1;
-        return true;
-      };
-      bool lok = load_k(0) && (nkv < 2 || load_k(1));
-      for (int j = 0; lok && j < nkv; ++j) {
-        if (!load_v(j)) break;
-        if (j + 2 < nkv && !load_k(j + 2)) break;
       }
-      // drain: every stage's last load must have landed before the CTA exits
-      for (int j = k_issued - kKStages > 0 ? k_issued - kKStages : 0; j < k_issued; ++j)
-        mbar_wait(bar(kBarKFull0 + j % kKStages), (j / kKStages) & 1, a.err, nullptr);
-      for (int j = v_issued - kVStages > 0 ? v_issued - kVStages : 0; j < v_issued; ++j)
-        mbar_wait(bar(kBarVFull0 + j % kVStages), (j / kVStages) & 1, a.err, nullptr);
+      k_issued = g + 1;
+      return true;
+    };
+    auto load_v = [&](int g) -> bool {
+      while (g >= cv.g0 + cv.n) {
+        const int g0n = cv.g0 + cv.n;
+        if (!enter(cv, cv.k + 1)) return false;
+        cv.g0 = g0n;
+      }
+      const int s = g % kVStages;
+      // stage s held V_{g-3}: free once PV_{g-3} has completed
+      if (g >= kVStages && !wait_all(kBarODone0 + s, ((g / kVStages) - 1) & 1)) return false;
+      if (lane == 0) {
+        mbar_expect_tx(bar(kBarVFull0 + s), 16384);
+        tma_load_2d(sbase + kOffV + s * kVStageBytes, &map_v, 0, cv.row0 + (g - cv.g0) * 128,
+                    bar(kBarVFull0 + s));
+      }
+      v_issued = g + 1;
+      return true;
+    };
+    // total tiles of this CTA's stream
+    int gtot = 0;
+    {
+      Item it;
+      for (int k = 0; item_of(p, k, it); ++k) gtot += it.nkv;
+    }
+    // loads in the order the MMA warps consume them: K_0, K_1, then V_g and
+    // K_{g+2} for g = 0, 1, ...
+    if (lok) lok = load_k(0) && (gtot < 2 || load_k(1));
+    for (int g = 0; lok && g < gtot; ++g) {
+      if (!load_v(g)) break;
+      if (g + 2 < gtot && !load_k(g + 2)) break;
+    }
+    // drain: every buffer's last load must have landed before the CTA exits
+    if (lane == 0) {
+      for (int g = k_issued - kKStages > 0 ? k_issued - kKStages : 0; g < k_issued; ++g)
+        mbar_wait(bar(kBarKFull0 + g % kKStages), (g / kKStages) & 1, a.err, nullptr);
+      for (int g = v_issued - kVStages > 0 ? v_issued - kVStages : 0; g < v_issued; ++g)
+        mbar_wait(bar(kBarVFull0 + g % kVStages), (g / kVStages) & 1, a.err, nullptr);
+      for (int k = q_issued - 2 > 0 ? q_issued - 2 : 0; k < q_issued; ++k)
+        mbar_wait(bar(kBarQFull0 + (k & 1)), (k >> 1) & 1, a.err, nullptr);
     }
   } else if (warp == kWarpMma || warp == kWarpMma2) {
     // ---------------- QK issuers ----------------
-    // One thread per score bank, each issuing every other tile with its own
-    // K scale slot: each accumulator and slot has a single issuing thread,
-    // and neither thread's tiles wait behind the other's.
+    // One thread per score bank, each issuing every other tile of the stream
+    // with its own K scale slot: each accumulator and slot has a single
+    // issuing thread, and neither thread's tiles wait behind the other's.
     if (lane == 0) {
       const int par = warp == kWarpMma ? 0 : 1;
       const uint32_t id_qk = idesc_nvfp4(128, 128);
-      bool ok;
-      if (par == 0) {
-        ok = mbar_wait(bar(kBarQFull), 0, a.err, abort_flag) &&
-             mbar_wait(bar(kBarQbReady), 0, a.err, abort_flag);
-        if (ok) {
-          tc_fence_after();
-          for (int kc = 0; kc < 2; ++kc)
-            tmem_cp_32x128b_x4(tmem + kColSfQ + 4 * kc,
-                               smem_desc(sbase + kOffQs + 512 * kc, 128, 128, kSwizzleNone));
-          for (int t = 0; t < T; ++t)
-            for (int kc = 0; kc < 2; ++kc)
-              tmem_cp_32x128b_x4(
-                  tmem + kColSfQb + 8 * t + 4 * kc,
-                  smem_desc(sbase + kOffQbs + 1024 * t + 512 * kc, 128, 128, kSwizzleNone));
-          tc_commit(bar(kBarQSf));
-        }
-      } else {
-        // the other issuer has copied the Q and rank-one scales into TMEM
-        // (its commit also says Q and the rank-one operand are in shared
-        // memory)
-        ok = mbar_wait(bar(kBarQSf), 0, a.err, abort_flag);
-        if (ok) tc_fence_after();
-      }
       // shared-memory descriptors built once: the start address sits in the
-      // low field in 16-byte units, so a K stage or a rank-one term (8 KB)
-      // is +512 and the second 64-element K chunk (32 B) +2; every address
-      // stays below 2^18, inside that field
+      // low field in 16-byte units, so a K stage, a Q buffer or a rank-one
+      // term (8 KB) is +512 and the second 64-element K chunk (32 B) +2;
+      // every address stays below 2^18, inside that field
       const uint64_t dq0 = smem_desc(sbase + kOffQ, 16, 512, kSwizzle64B);
       const uint64_t dk0 = smem_desc(sbase + kOffK, 16, 512, kSwizzle64B);
       const uint64_t dqb0 = smem_desc(sbase + kOffQb, 16, 512, kSwizzle64B);
-      // QK_j (and the rank-one MMAs) into score bank j % 2
-      auto issue_qk = [&](int j) -> bool {
-        const int s = j % kKStages, bk = j & 1;
-        if (!mbar_wait(bar(kBarKFull0 + s), (j / kKStages) & 1, a.err, abort_flag)) return false;
+      // QK_g (and the rank-one MMAs) into score bank g % 2, Q from buffer buf
+      auto issue_qk = [&](int g, int buf) -> bool {
+        const int s = g % kKStages, bk = g & 1;
+        if (!mbar_wait(bar(kBarKFull0 + s), (g / kKStages) & 1, a.err, abort_flag)) return false;
         tc_fence_after();
-        // K_j's scales into this issuer's slot j % 2; its last reader,
-        // QK_{j-2}, completed before the softmax loaded S_{j-2} (waited for)
-        const uint32_t sfk = tmem + col_sf_k(j % kSfSlots);
+        // K_g's scales into this issuer's slot; its last reader, QK_{g-2},
+        // completed before the softmax loaded S_{g-2} (waited for)
+        const uint32_t sfk = tmem + col_sf_k(bk);
         for (int kc = 0; kc < 2; ++kc)
           tmem_cp_32x128b_x4(sfk + 4 * kc,
                              smem_desc(sbase + kOffKs + 1024 * s + 512 * kc, 128, 128, kSwizzleNone));
         const uint32_t dS = tmem + kColS0 + 128 * bk;
         const uint64_t dk = dk0 + 512u * (uint32_t)s;
-        mma_nvfp4_ss(dS, dq0, dk, id_qk, tmem + kColSfQ, sfk, 0u);
-        mma_nvfp4_ss(dS, dq0 + 2u, dk + 2u, id_qk, tmem + kColSfQ + 4, sfk + 4, 1u);
+        const uint64_t dq = dq0 + 512u * (uint32_t)buf, dqb = dqb0 + 1024u * (uint32_t)buf;
+        mma_nvfp4_ss(dS, dq, dk, id_qk, tmem + kColSfQ, sfk, 0u);
+        mma_nvfp4_ss(dS, dq + 2u, dk + 2u, id_qk, tmem + kColSfQ + 4, sfk + 4, 1u);
         if (T > 0) {
-          mma_nvfp4_ss(dS, dqb0, dk, id_qk, tmem + kColSfQb, sfk, 1u);
-          mma_nvfp4_ss(dS, dqb0 + 2u, dk + 2u, id_qk, tmem + kColSfQb + 4, sfk + 4, 1u);
+          mma_nvfp4_ss(dS, dqb, dk, id_qk, tmem + kColSfQb, sfk, 1u);
+          mma_nvfp4_ss(dS, dqb + 2u, dk + 2u, id_qk, tmem + kColSfQb + 4, sfk + 4, 1u);
         }
         if (T > 1) {
-          mma_nvfp4_ss(dS, dqb0 + 512u, dk, id_qk, tmem + kColSfQb + 8, sfk, 1u);
-          mma_nvfp4_ss(dS, dqb0 + 514u, dk + 2u, id_qk, tmem + kColSfQb + 12, sfk + 4, 1u);
+          mma_nvfp4_ss(dS, dqb + 512u, dk, id_qk, tmem + kColSfQb + 8, sfk, 1u);
+          mma_nvfp4_ss(dS, dqb + 514u, dk + 2u, id_qk, tmem + kColSfQb + 12, sfk + 4, 1u);
         }
         tc_commit(bar(kBarSFull0 + bk));
         return true;
       };
-      for (int j = par; ok && j < nkv; j += 2) {
-        // the softmax has loaded S_{j-2}: bank j % 2 and slot j % 2 are free.
-        // SRead for stage (j-2) % 4 cannot be a phase further on: that needs
-        // S_{j+2}.
-        if (j >= 2 && !mbar_wait(bar(kBarSRead0 + (j - 2) % kKStages), ((j - 2) / kKStages) & 1,
-                                 a.err, abort_flag))
-          break;
-        if (!issue_qk(j)) break;
+      // the softmax has loaded S_{g-2}: bank g % 2 and slot g % 2 are free.
+      // SRead for stage (g-2) % 4 cannot be a phase further on: that needs
+      // S_{g+2}.
+      auto wait_sread = [&](int g) -> bool {
+        return g < 2 || mbar_wait(bar(kBarSRead0 + (g - 2) % kKStages),
+                                  ((g - 2) / kKStages) & 1, a.err, abort_flag);
+      };
+      bool ok = true;
+      int g0 = 0;
+      Item it;
+      for (int k = 0; ok && item_of(p, k, it); ++k) {
+        const int buf = k & 1, n = it.nkv;
+        const bool copier = (g0 & 1) == par;   // this thread issues the item's first tile
+        if (copier) {
+          // the item's Q is in buffer buf, and every score product reading
+          // the TMEM Q scales of the previous item has completed: the other
+          // thread's QK_{g0-1} (its bank's next commit needs these scales)
+          // and this thread's QK_{g0-2} (waited for through S_{g0-2})
+          ok = mbar_wait(bar(kBarQFull0 + buf), (k >> 1) & 1, a.err, abort_flag) &&
+               (g0 < 1 || mbar_wait(bar(kBarSFull0 + ((g0 - 1) & 1)), ((g0 - 1) >> 1) & 1,
+                                    a.err, abort_flag)) &&
+               wait_sread(g0);
+          if (!ok) break;
+          tc_fence_after();
+          for (int kc = 0; kc < 2; ++kc)
+            tmem_cp_32x128b_x4(tmem + kColSfQ + 4 * kc,
+                               smem_desc(sbase + kOffQs + 1024 * buf + 512 * kc, 128, 128,
+                                         kSwizzleNone));
+          for (int t = 0; t < T; ++t)
+            for (int kc = 0; kc < 2; ++kc)
+              tmem_cp_32x128b_x4(tmem + kColSfQb + 8 * t + 4 * kc,
+                                 smem_desc(sbase + kOffQbs + 2048 * buf + 1024 * t + 512 * kc,
+                                           128, 128, kSwizzleNone));
+          // also says (to the other thread) that Q and the rank-one operand
+          // are in shared memory
+          tc_commit(bar(kBarQSf));
+          ok = issue_qk(g0, buf);
+        } else if (n > 1) {
+          ok = mbar_wait(bar(kBarQSf), k & 1, a.err, abort_flag);
+          if (ok) tc_fence_after();
+        }
+        for (int g = g0 + (copier ? 2 : 1); ok && g < g0 + n; g += 2) {
+          if (!wait_sread(g) || !issue_qk(g, buf)) ok = false;
+        }
+        // this thread's products of item k done with Q buffer buf
+        tc_commit(bar(kBarQEmpty0 + buf));
+        g0 += n;
       }
       // drain this thread's tensor-core work before the CTA releases TMEM
       tc_commit(bar(kBarDrain));
@@ -318,213 +458,253 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- PV issuer ----------------
     if (lane == 0) {
       const uint32_t id_pv = idesc_fp8(128, 144, 0, 1);   // 128 V columns + 16 ones
-      for (int j = 0; j < nkv; ++j) {
-        const int bp = j & 1, sp = j % kVStages;
-        // the softmax has published P_j in P bank j % 2
-        if (!mbar_wait(bar(kBarPReady0 + bp), (j >> 1) & 1, a.err, abort_flag)) break;
-        if (!mbar_wait(bar(kBarVFull0 + sp), (j / kVStages) & 1, a.err, abort_flag)) break;
-        tc_fence_after();
-        const uint32_t pcol = tmem + kColP0 + 32 * bp;
-        const uint32_t vaddr = sbase + kOffV + sp * kVStageBytes;
-        for (int kk = 0; kk < 4; ++kk)
-          mma_fp8_ts(tmem + kColO, pcol + 8 * kk,
-                     smem_desc(vaddr + 4096 * kk, kVOnesLbo, 1024, kSwizzle128B), id_pv,
-                     (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(bar(kBarODone0 + sp));
+      bool ok = mbar_wait(bar(kBarOnes), 0, a.err, abort_flag);
+      int g0 = 0;
+      Item it;
+      for (int k = 0; ok && item_of(p, k, it); ++k) {
+        // the item's first PV overwrites O and l: the previous item's
+        // epilogue must have read them out
+        if (k >= 1 && !mbar_wait(bar(kBarOFree), (k - 1) & 1, a.err, abort_flag)) break;
+        for (int j = 0; j < it.nkv; ++j) {
+          const int g = g0 + j, bp = g & 1, sp = g % kVStages;
+          // the softmax has published P_g in P bank g % 2
+          if (!mbar_wait(bar(kBarPReady0 + bp), (g >> 1) & 1, a.err, abort_flag) ||
+              !mbar_wait(bar(kBarVFull0 + sp), (g / kVStages) & 1, a.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t pcol = tmem + kColP0 + 32 * bp;
+          const uint32_t voff = kOffV + sp * kVStageBytes;
+          // the N = 144 operand: V's 128-byte atom, then the ones atom at a
+          // leading offset of kOffOnes - voff bytes (the same 32-key
+          // sub-tile offset in both)
+          for (int kk = 0; kk < 4; ++kk)
+            mma_fp8_ts(tmem + kColO, pcol + 8 * kk,
+                       smem_desc(sbase + voff + 4096 * kk, kOffOnes - voff, 1024, kSwizzle128B),
+                       id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(bar(kBarODone0 + sp));
+        }
+        g0 += it.nkv;
       }
       tc_commit(bar(kBarDrain));
       mbar_wait(bar(kBarDrain), 0, a.err, nullptr);
     }
   } else {
     // ---------------- softmax / correction / epilogue ----------------
-    const int half = warp >> 2;              // prologue split; afterwards the tile parity
-    const int row = threadIdx.x & 127;       // query row = TMEM lane
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    // Rank-one operand tiles: every row holds the block's term t (same 64
-    // bytes), written with the 64-byte swizzle the TMA applies to Q and K.
-    const int nblk = a.N / 128;
-    if (half == 0) {
-      for (int t = 0; t < T; ++t) {
-        const uint8_t* src = a.qbc + (((size_t)bh * nblk + qt) * a.T + t) * 64;
-        uint4* dst = reinterpret_cast<uint4*>(smem + kOffQb + 8192 * t + 64 * row);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          dst[c ^ ((row >> 1) & 3)] = reinterpret_cast<const uint4*>(src)[c];
-      }
-    } else {
-      for (int t = 0; t < T; ++t) {
-        const uint8_t* ssrc = a.qbs + (((size_t)bh * nblk + qt) * a.T + t) * 8;
-        uint32_t w0 = *reinterpret_cast<const uint32_t*>(ssrc);
-        uint32_t w1 = *reinterpret_cast<const uint32_t*>(ssrc + 4);
-        reinterpret_cast<uint32_t*>(smem + kOffQbs + 1024 * t)[row] = w0;
-        reinterpret_cast<uint32_t*>(smem + kOffQbs + 1024 * t + 512)[row] = w1;
-      }
-    }
-    // the ones atoms beside the V stages (E4M3 1.0 = 0x38; every byte equal,
-    // so the 128-byte swizzle leaves them unchanged)
-    for (int s = 0; s < kVStages; ++s) {
-      uint4* ones = reinterpret_cast<uint4*>(smem + kOffV + s * kVStageBytes + kVOnesLbo);
-      for (int i = threadIdx.x; i < (int)(kVOnesLbo / 16); i += kSoftmaxThreads)
+    const int par = warp >> 2, quad = warp & 3;   // tile parity, TMEM lane quadrant
+    const int row = threadIdx.x & 127;            // query row = TMEM lane
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    // the ones atom of the PV operand (E4M3 1.0 = 0x38; every byte equal,
+    // so the 128-byte swizzle leaves it unchanged), written once
+    {
+      uint4* ones = reinterpret_cast<uint4*>(smem + kOffOnes);
+      for (int i = threadIdx.x; i < 16384 / 16; i += kSoftmaxThreads)
         ones[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
     }
     fence_proxy_async_smem();
-    mbar_arrive(bar(kBarQbReady));
+    mbar_arrive(bar(kBarOnes));
 
-    // Tiles j = par, par + 2, ... of this warp; the owner of tile j hands
-    // the row's reference max m_j to the owner of tile j+1 (bar kBarMax0 +
+    int gtot = 0;
+    {
+      Item it;
+      for (int k = 0; item_of(p, k, it); ++k) gtot += it.nkv;
+    }
+    // Tiles g = par, par + 2, ... of the stream; the owner of tile g hands
+    // the row's reference max to the owner of tile g+1 (bar kBarMax0 +
     // 2*quadrant + receiving parity; one hand-over per phase, and a phase
-    // cannot run ahead because the next hand-over needs the reply).
-    const int par = half, quad = warp & 3;
+    // cannot run ahead because the next hand-over needs the reply).  At an
+    // item's first tile the value handed over is ignored.
     float* mrow = reinterpret_cast<float*>(smem + kOffMax);
     const uint32_t bar_in = bar(kBarMax0 + 2 * quad + par);
     const uint32_t bar_out = bar(kBarMax0 + 2 * quad + (par ^ 1));
     const float cs = __fmul_rn(__fmul_rn(*a.s_q, *a.s_k), p.log2e_rsqrt_d);
-    float m = -INFINITY;
     bool ok = true;
-    for (int j = par; j < nkv; j += 2) {
-      const int bk = par;   // == j & 1
-      const int it = j >> 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarSFull0 + bk), it & 1, a.err, abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t sS = tmem + lane_off + kColS0 + 128 * bk;
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(sS + 32 * c, sr[c]);
-      tmem_ld_wait();
-      // S_j is in registers: bank j % 2 and K stage j % 4 may be reused
-      tc_fence_before();
-      mbar_arrive(bar(kBarSRead0 + j % kKStages));
-      if (a.causal && j == qt) {  // diagonal tile: key > row is masked
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (32 * c + i > row) sr[c][i] = 0xFF800000u;  // -inf
-      }
-      // tile max over the row's 128 keys (3-input max tree)
-      float pm[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const int e = 8 * k;
-        pm[k] = fmax3(fmax3(__uint_as_float(sr[e >> 5][e & 31]),
-                            __uint_as_float(sr[e >> 5][(e + 1) & 31]),
-                            __uint_as_float(sr[e >> 5][(e + 2) & 31])),
-                      fmax3(__uint_as_float(sr[e >> 5][(e + 3) & 31]),
-                            __uint_as_float(sr[e >> 5][(e + 4) & 31]),
-                            __uint_as_float(sr[e >> 5][(e + 5) & 31])),
-                      fmaxf(__uint_as_float(sr[e >> 5][(e + 6) & 31]),
-                            __uint_as_float(sr[e >> 5][(e + 7) & 31])));
-      }
-      const float smax = fmax3(fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]),
-                                     fmax3(pm[6], pm[7], pm[8])),
-                               fmax3(pm[9], pm[10], pm[11]),
-                               fmax3(fmax3(pm[12], pm[13], pm[14]), pm[15], -INFINITY));
-      // reference max of the row after tile j-1, from that tile's owner
-      if (j > 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_in, ((j - 1) >> 1) & 1, a.err, abort_flag))) {
-          ok = false;
-          break;
-        }
-        m = mrow[row];
-      }
-      // cs > 0, so max_i(S_i * cs) == (max_i S_i) * cs exactly.  The reference
-      // max moves only when the tile max exceeds it by more than kRescaleTau,
-      // so O and L rarely need a rescale once the first tiles are done.
-      const float tmax = __fmul_rn(smax, cs);
-      const float mn = (m == -INFINITY || tmax > m + kRescaleTau) ? tmax : m;
-      if (j + 1 < nkv) {
-        mrow[row] = mn;
-        mbar_arrive(bar_out);
-      }
-      const float alpha = (m == -INFINITY) ? 0.0f : (mn == m ? 1.0f : ex2(m - mn));
-      const float bias = kPShift - mn;  // P8 = E4M3(2^(t - m) * 2^kPShift)
-      uint32_t pw[32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int w = 0; w < 8; ++w)
-          pw[8 * c + w] = e4m3x4(ex2(fmaf(__uint_as_float(sr[c][4 * w]), cs, bias)),
-                                 ex2(fmaf(__uint_as_float(sr[c][4 * w + 1]), cs, bias)),
-                                 ex2(fmaf(__uint_as_float(sr[c][4 * w + 2]), cs, bias)),
-                                 ex2(fmaf(__uint_as_float(sr[c][4 * w + 3]), cs, bias)));
-      // correction: O and L scale by alpha once PV_{j-1} has landed (PV_j is
-      // issued only after this tile's P is published)
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarODone0 + (j - 1) % kVStages),
-                                               ((j - 1) / kVStages) & 1, a.err, abort_flag))) {
+    int g0 = 0;
+    Item it;
+    for (int k = 0; ok && item_of(p, k, it); ++k) {
+      const int nkv = it.nkv, qt = it.qt;
+      float m = -INFINITY;
+      for (int j = (g0 & 1) == par ? 0 : 1; j < nkv; j += 2) {
+        const int g = g0 + j, bk = par;   // bk == g & 1
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(bar(kBarSFull0 + bk), (g >> 1) & 1, a.err, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t oO = tmem + lane_off + kColO;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(oO + 32 * c, o);
-          tmem_ld_wait();
+        const uint32_t sS = tmem + lane_off + kColS0 + 128 * bk;
+        uint32_t sr[4][32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(oO + 32 * c, o);
+        for (int c = 0; c < 4; ++c) tmem_ld32(sS + 32 * c, sr[c]);
+        tmem_ld_wait();
+        // S_g is in registers: bank g % 2 and K stage g % 4 may be reused
+        tc_fence_before();
+        mbar_arrive(bar(kBarSRead0 + g % kKStages));
+        if (a.causal && j == qt) {  // diagonal tile: key > row is masked
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (32 * c + i > row) sr[c][i] = 0xFF800000u;  // -inf
         }
-        uint32_t l4[4];
-        tmem_ld4(tmem + lane_off + kColL, l4);
-        tmem_ld_wait();
-        l4[0] = __float_as_uint(__uint_as_float(l4[0]) * alpha);
-        tmem_st4(tmem + lane_off + kColL, l4);
-      }
-      // P bank j % 2 was last read by PV_{j-2}: wait for it to complete
-      // (its ODone phase cannot be overtaken: PV_{j+1} needs this P first).
-      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar(kBarODone0 + (j - 2) % kVStages),
-                                                        ((j - 2) / kVStages) & 1, a.err,
-                                                        abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      tmem_st32(tmem + lane_off + kColP0 + 32 * bk, pw);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(kBarPReady0 + bk));
-      m = mn;
-    }
-    // epilogue: the owner of the last tile holds the final reference max
-    if (ok && nkv > 0 && par == ((nkv - 1) & 1) &&
-        __all_sync(0xffffffffu, mbar_wait(bar(kBarODone0 + (nkv - 1) % kVStages),
-                                          ((nkv - 1) / kVStages) & 1, a.err, abort_flag))) {
-      tc_fence_after();
-      uint32_t l4[4];
-      tmem_ld4(tmem + lane_off + kColL, l4);
-      tmem_ld_wait();
-      const float l = __uint_as_float(l4[0]);
-      const float sc = __fdiv_rn(*a.s_v, l);
-      const size_t grow = (size_t)qt * 128 + row;
-      uint4* out = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) +
-                                            (((size_t)b * a.N + grow) * a.Hq + h) * 128);
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tmem + lane_off + kColO + 32 * c, o);
-        tmem_ld_wait();
+        // tile max over the row's 128 keys (3-input max tree)
+        float pm[16];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(o[8 * q4 + 2 * e]) * sc,
-                                                     __uint_as_float(o[8 * q4 + 2 * e + 1]) * sc);
-            w[e] = *reinterpret_cast<uint32_t*>(&v);
+        for (int q = 0; q < 16; ++q) {
+          const int e = 8 * q;
+          pm[q] = fmax3(fmax3(__uint_as_float(sr[e >> 5][e & 31]),
+                              __uint_as_float(sr[e >> 5][(e + 1) & 31]),
+                              __uint_as_float(sr[e >> 5][(e + 2) & 31])),
+                        fmax3(__uint_as_float(sr[e >> 5][(e + 3) & 31]),
+                              __uint_as_float(sr[e >> 5][(e + 4) & 31]),
+                              __uint_as_float(sr[e >> 5][(e + 5) & 31])),
+                        fmaxf(__uint_as_float(sr[e >> 5][(e + 6) & 31]),
+                              __uint_as_float(sr[e >> 5][(e + 7) & 31])));
+        }
+        const float smax = fmax3(fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]),
+                                       fmax3(pm[6], pm[7], pm[8])),
+                                 fmax3(pm[9], pm[10], pm[11]),
+                                 fmax3(fmax3(pm[12], pm[13], pm[14]), pm[15], -INFINITY));
+        // reference max of the row after tile g-1, from that tile's owner
+        if (g > 0) {
+          if (!__all_sync(0xffffffffu, mbar_wait(bar_in, ((g - 1) >> 1) & 1, a.err, abort_flag))) {
+            ok = false;
+            break;
           }
-          out[4 * c + q4] = make_uint4(w[0], w[1], w[2], w[3]);
+          const float mi = mrow[row];
+          if (j > 0) m = mi;
         }
+        // cs > 0, so max_i(S_i * cs) == (max_i S_i) * cs exactly.  The
+        // reference max moves only when the tile max exceeds it by more than
+        // kRescaleTau, so O and L rarely need a rescale once the first tiles
+        // are done.
+        const float tmax = __fmul_rn(smax, cs);
+        const float mn = (m == -INFINITY || tmax > m + kRescaleTau) ? tmax : m;
+        if (g + 1 < gtot) {
+          mrow[row] = mn;
+          mbar_arrive(bar_out);
+        }
+        const float alpha = (m == -INFINITY) ? 0.0f : (mn == m ? 1.0f : ex2(m - mn));
+        const float bias = kPShift - mn;  // P8 = E4M3(2^(t - m) * 2^kPShift)
+        uint32_t pw[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int w = 0; w < 8; ++w)
+            pw[8 * c + w] = e4m3x4(ex2(fmaf(__uint_as_float(sr[c][4 * w]), cs, bias)),
+                                   ex2(fmaf(__uint_as_float(sr[c][4 * w + 1]), cs, bias)),
+                                   ex2(fmaf(__uint_as_float(sr[c][4 * w + 2]), cs, bias)),
+                                   ex2(fmaf(__uint_as_float(sr[c][4 * w + 3]), cs, bias)));
+        // correction: O and L scale by alpha once PV_{g-1} has landed (PV_g is
+        // issued only after this tile's P is published)
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarODone0 + (g - 1) % kVStages),
+                                                 ((g - 1) / kVStages) & 1, a.err, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t oO = tmem + lane_off + kColO;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(oO + 32 * c, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(oO + 32 * c, o);
+          }
+          uint32_t l4[4];
+          tmem_ld4(tmem + lane_off + kColL, l4);
+          tmem_ld_wait();
+          l4[0] = __float_as_uint(__uint_as_float(l4[0]) * alpha);
+          tmem_st4(tmem + lane_off + kColL, l4);
+        }
+        // P bank g % 2 was last read by PV_{g-2}: wait for it to complete
+        // (its ODone phase cannot be overtaken: PV_{g+1} needs this P first).
+        if (g >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar(kBarODone0 + (g - 2) % kVStages),
+                                                          ((g - 2) / kVStages) & 1, a.err,
+                                                          abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_st32(tmem + lane_off + kColP0 + 32 * bk, pw);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(kBarPReady0 + bk));
+        m = mn;
       }
-      if (a.lse)
-        a.lse[(size_t)bh * a.N + grow] = 0.69314718055994531f * (m + __log2f(l) - kPShift);
+      if (!ok) break;
+      if (((g0 + nkv - 1) & 1) == par) {
+        const int g = g0 + nkv - 1;
+        // epilogue of the item, by the owner of its last tile: once PV_g
+        // has completed, O and l into registers, TMEM freed for the next
+        // item's first PV, then the normalised O and the LSE out.  ODone
+        // for stage g % 3 cannot move on before this: PV_{g+3} needs the
+        // O freed here first.
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarODone0 + g % kVStages),
+                                               (g / kVStages) & 1, a.err, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t l4[4], o[4][32];
+        tmem_ld4(tmem + lane_off + kColL, l4);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_off + kColO + 32 * c, o[c]);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(bar(kBarOFree));
+        const float l = __uint_as_float(l4[0]);
+        const float sc = __fdiv_rn(*a.s_v, l);
+        const int h = it.bh % a.Hq, b = it.bh / a.Hq;
+        const size_t grow = (size_t)qt * 128 + row;
+        // O through this warp's 32 rows of its parity's staging tile and two
+        // TMA stores issued by the warp's lane 0, whose previous stores must
+        // have read those rows before they are rewritten
+        const uint32_t ost = kOffOst + 32768u * (uint32_t)par + 4096u * (uint32_t)quad;
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              __nv_bfloat162 v =
+                  __floats2bfloat162_rn(__uint_as_float(o[c][8 * q4 + 2 * e]) * sc,
+                                        __uint_as_float(o[c][8 * q4 + 2 * e + 1]) * sc);
+              w[e] = *reinterpret_cast<uint32_t*>(&v);
+            }
+            // columns 32c + 8q4 .. +7: half c / 2, 16-byte chunk 4(c % 2) + q4
+            // of the row, at chunk position chunk ^ (row % 8)
+            const int chunk = 4 * (c & 1) + q4;
+            *reinterpret_cast<uint4*>(smem + ost + 16384u * (uint32_t)(c >> 1) + 128u * lane +
+                                      16u * (uint32_t)(chunk ^ (lane & 7))) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          // O viewed as bytes [B*N rows][Hq*256]: head h at byte 256h
+          const int y = b * a.N + qt * 128 + 32 * quad;
+          tma_store_2d(&map_o, sbase + ost, 256 * h, y);
+          tma_store_2d(&map_o, sbase + ost + 16384u, 256 * h + 128, y);
+          bulk_commit_group();
+        }
+        if (a.lse)
+          a.lse[(size_t)it.bh * a.N + grow] =
+              0.69314718055994531f * (m + __log2f(l) - kPShift);
+      }
+      g0 += nkv;
     }
   }
 
+  // the O stores issued by this thread (lane 0 of a softmax warp) have completed
+  if (warp < 8 && lane == 0) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpMma) {
@@ -537,11 +717,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   const uint64_t qrows = (uint64_t)a.B * a.Hq * a.N, kvrows = (uint64_t)a.B * a.Hkv * a.N;
   if (!make_map_2d_u8(&mq, a.qc, 64, qrows, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map_2d_u8(&mk, a.kc, 64, kvrows, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_map_2d_u8(&mv, a.vc, 128, kvrows, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+      !make_map_2d_u8(&mv, a.vc, 128, kvrows, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d_u8_box(&mo, a.o, (uint64_t)a.Hq * 256, (uint64_t)a.Hq * 256,
+                          (uint64_t)a.B * a.N, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
@@ -554,19 +736,25 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.a = a;
   p.log2e_rsqrt_d = (float)(1.4426950408889634 / std::sqrt(128.0));
   p.q_tiles = a.N / 128;
+  p.items = p.q_tiles * a.B * a.Hq;
+  if (p.items == 0) return cudaSuccess;
+  int dev = 0, sms = 0;
   {
-    static int sms = 0;
-    if (!sms) {
-      int dev = 0;
-      cudaGetDevice(&dev);
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-      if (sms <= 0) sms = 148;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static int sms_of[64] = {};
+    if (dev >= 0 && dev < 64 && sms_of[dev] > 0) {
+      sms = sms_of[dev];
+    } else {
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) sms_of[dev] = sms;
     }
-    p.wave = sms;
   }
-  const unsigned grid = (unsigned)(p.q_tiles * a.B * a.Hq);
-  if (grid == 0) return cudaSuccess;
-  prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+  // persistent: one CTA per SM (shared memory and TMEM admit one), each
+  // walking its share of the work items
+  const unsigned grid = (unsigned)(p.items < sms ? p.items : sms);
+  prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mo, p);
   return cudaGetLastError();
 }
 

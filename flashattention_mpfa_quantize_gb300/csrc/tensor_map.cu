@@ -34,4 +34,21 @@ bool make_map_2d_u8(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint
   return r == CUDA_SUCCESS;
 }
 
+// 2-D byte matrix [rows][inner_bytes] with row pitch `pitch` bytes, moved in
+// boxes of box_inner bytes x box_rows rows with the given swizzle.
+bool make_map_2d_u8_box(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t pitch,
+                        uint64_t rows, uint32_t box_inner, uint32_t box_rows,
+                        CUtensorMapSwizzle sw) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner_bytes, rows};
+  cuuint64_t strides[1] = {pitch};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace mpfa
