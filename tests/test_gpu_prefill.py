@@ -69,6 +69,35 @@ def test_prefill_single_tile():
     _assert_close(got, want, lg, lw)
 
 
+@pytest.mark.parametrize("causal,compensate,T", [(True, True, 2), (True, False, 2),
+                                                  (False, True, 1)])
+def test_prefill_many_items_per_cta(causal, compensate, T):
+    """More work items (query tile of a (batch, head)) than SMs: each CTA of
+    the persistent grid walks three or four items as one KV-tile stream, of
+    1..8 tiles (odd and even counts) when causal, so the carries across items
+    (two Q buffers, the Q scale copy after the previous item's score
+    products, O freed for the next item's first PV, the max hand-over across
+    the boundary) all take part.  Full rows of sampled (batch, head) pairs
+    spread over the item list."""
+    cfg = mi.custom_prefill(2, 32, 4, 1024, causal, k_outliers=1, v_outlier_p=0.001,
+                            q_offset=True)
+    heads = [(0, 0), (0, 13), (1, 7), (1, 31)]
+    got, want, lg, lw, *_ = _prefill_case(cfg, compensate, T, seed=11, heads=heads)
+    _assert_close(got, want, lg, lw)
+
+
+def test_prefill_single_tile_items_back_to_back():
+    """256 one-tile items (N = 128) on a grid of at most one CTA per SM: every
+    tile of a CTA's stream starts an item, so each boundary step (Q scale
+    copy, O freed, epilogue beside the next item's first tile) runs at every
+    tile, alternating between the two softmax parities."""
+    cfg = mi.custom_prefill(2, 128, 8, 128, True, k_outliers=1, v_outlier_p=0.001,
+                            q_offset=True)
+    heads = [(0, 0), (0, 77), (1, 3), (1, 127)]
+    got, want, lg, lw, *_ = _prefill_case(cfg, True, 2, seed=12, heads=heads)
+    _assert_close(got, want, lg, lw)
+
+
 def test_prefill_error_vs_exact_reported():
     """Against exact fp64 attention the quantized pipeline stays a usable
     approximation (cosine > 0.8 on the tiny config with a Q offset) with and without the
