@@ -73,6 +73,9 @@ _lib.mpfa_decode.restype = _I
 _lib.mpfa_decode.argtypes = [_P, ctypes.POINTER(NVFP4), ctypes.POINTER(FP8), _P, _I, _I, _I, _I,
                              _I, _I, _I, _I, _P, _P, ctypes.POINTER(NVFP4),
                              ctypes.POINTER(Rank1), ctypes.POINTER(_I), _P, _SZ, _P]
+_lib.mpfa_append_kv.restype = _I
+_lib.mpfa_append_kv.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, ctypes.POINTER(NVFP4),
+                                ctypes.POINTER(FP8), _P]
 _lib.mpfa_get_error.restype = _I
 _lib.mpfa_get_error.argtypes = [_P]
 
@@ -234,6 +237,29 @@ def decode(q, cache, seqlens, *, compensate=True, T=2, kv_chunk=0, out=None, lse
     res["chunk"] = used.value
     res["_workspace"] = workspace
     return res
+
+
+def append_kv(k_new, v_new, cache, seqlens):
+    """Quantize-on-append: k_new / v_new bf16 [B, n_new, Hkv, 128] on the
+    device, quantized with the cache's own tensor scales and written into
+    the cache (from quantize_qkv(None, k, v)) at rows seqlens[b] ..
+    seqlens[b] + n_new - 1 (int32 [B] on the device, not advanced: pass
+    seqlens + n_new to the next decode).  A sequence that would run past the
+    cache is left as it is and get_error() then reports
+    MPFA_ERR_INVALID_ARG."""
+    B, n_new, Hkv, d = k_new.shape
+    dev = k_new.device
+    for t in (k_new, v_new):
+        assert t.dtype == torch.bfloat16 and t.is_contiguous() and t.shape == (B, n_new, Hkv, D)
+        assert t.device == dev
+    assert seqlens.dtype == torch.int32 and seqlens.device == dev and seqlens.numel() == B
+    assert cache["Hkv"] == Hkv and cache["B"] == B
+    ks = _nvfp4(cache["k"])
+    vs = FP8(cache["v"]["codes"].data_ptr(), cache["v"]["scale"].data_ptr())
+    st = _lib.mpfa_append_kv(_ptr(k_new), _ptr(v_new), _ptr(seqlens), B, n_new, Hkv, d,
+                             cache["Nk"], ctypes.byref(ks), ctypes.byref(vs), _stream(dev))
+    _check(st, "mpfa_append_kv")
+    return cache
 
 
 # --------------------------------------------------------------------------

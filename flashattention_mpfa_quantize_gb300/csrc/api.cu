@@ -255,6 +255,36 @@ mpfa_status mpfa_decode(const void* q_bf16, const mpfa_nvfp4* k_cache, const mpf
   return from_cuda(mpfa::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+mpfa_status mpfa_append_kv(const void* k_new_bf16, const void* v_new_bf16, const int32_t* seqlens,
+                           int B, int n_new, int Hkv, int d, int Lmax, mpfa_nvfp4* k_cache,
+                           mpfa_fp8* v_cache, mpfa_stream_t stream) {
+  if (d != 128) return MPFA_ERR_UNSUPPORTED;
+  if (!ok_ptr(k_new_bf16) || !ok_ptr(v_new_bf16) || !seqlens || !k_cache || !v_cache ||
+      B <= 0 || n_new <= 0 || Hkv <= 0 || Lmax <= 0 || Lmax % 128 || n_new > Lmax)
+    return MPFA_ERR_INVALID_ARG;
+  if (!ok_ptr(k_cache->codes) || !ok_ptr(k_cache->scales) || !k_cache->tensor_scale ||
+      !ok_ptr(v_cache->codes) || !v_cache->tensor_scale)
+    return MPFA_ERR_INVALID_ARG;
+  if ((uint64_t)B * Hkv * Lmax >= (1ull << 31) || (uint64_t)B * n_new * Hkv >= (1ull << 31))
+    return MPFA_ERR_INVALID_ARG;
+  mpfa::AppendArgs a = {};
+  a.k_new = k_new_bf16;
+  a.v_new = v_new_bf16;
+  a.seqlens = seqlens;
+  a.B = B;
+  a.n_new = n_new;
+  a.Hkv = Hkv;
+  a.Lmax = Lmax;
+  a.kc = k_cache->codes;
+  a.ks = k_cache->scales;
+  a.s_k = k_cache->tensor_scale;
+  a.vc = v_cache->codes;
+  a.s_v = v_cache->tensor_scale;
+  a.err = status_ptr();
+  if (!a.err) return MPFA_ERR_CUDA;
+  return from_cuda(mpfa::launch_append(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 mpfa_status mpfa_selftest_wait_timeout(unsigned long long limit_ns, mpfa_stream_t stream) {
   if (limit_ns == 0 || limit_ns > 2000000000ull) return MPFA_ERR_INVALID_ARG;
   int* err = status_ptr();

@@ -32,6 +32,22 @@ struct QuantArgs {
 size_t quant_workspace_bytes(int B, int Nq, int Hq, int compensate);
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream);
 
+// Quantize-on-append into a decode cache: new rows of K and V, quantized with
+// the cache's tensor scales, written at rows seqlens[b] + t.
+struct AppendArgs {
+  const void* k_new;  // bf16 [B][n_new][Hkv][128]
+  const void* v_new;  // bf16 [B][n_new][Hkv][128]
+  const int32_t* seqlens;
+  int B, n_new, Hkv, Lmax;
+  uint8_t *kc, *ks;
+  const float* s_k;
+  uint8_t* vc;
+  const float* s_v;
+  int* err;
+};
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
+
 struct PrefillArgs {
   const uint8_t *qc, *qs;
   const float* s_q;

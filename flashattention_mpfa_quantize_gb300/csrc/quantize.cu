@@ -573,6 +573,102 @@ __global__ void __launch_bounds__(kThreads, 6) quant_kernel(QuantArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// quantize-on-append into a decode cache
+// ---------------------------------------------------------------------------
+
+constexpr int kErrInvalidArg = 1;  // MPFA_ERR_INVALID_ARG in the device status word
+
+// New K and V rows, quantized with the cache's tensor scales exactly as the
+// quant pass codes them (the same block and element arithmetic), written at
+// cache rows seqlens[b] + t.  One thread per 16-element block, eight per row,
+// four rows per warp: the tiled scale store gathers a row's neighbouring
+// blocks by shuffles, so every lane takes part in every step and the
+// out-of-range and overrunning rows are masked, not skipped.
+__global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
+  const float sk = *a.s_k, sv = *a.s_v;
+  const bool vfast = sv >= kDivLo && sv <= kDivHi;
+  const float ysv = __frcp_rn(sv);
+  const __nv_bfloat16* kn = reinterpret_cast<const __nv_bfloat16*>(a.k_new);
+  const __nv_bfloat16* vn = reinterpret_cast<const __nv_bfloat16*>(a.v_new);
+  const size_t units = (size_t)a.B * a.n_new * a.Hkv * 8;
+  const size_t stride = (size_t)gridDim.x * kThreads;
+  const int lane = threadIdx.x & 31;
+  for (size_t base = (size_t)blockIdx.x * kThreads + (threadIdx.x & ~31u); base < units;
+       base += stride) {
+    const size_t u = base + lane;
+    const int j = (int)(u & 7);
+    const size_t rr = u >> 3;  // new row in the input's order (b, t, h)
+    const bool in = u < units;
+    int b = 0, t = 0, h = 0;
+    if (in) {
+      h = (int)(rr % a.Hkv);
+      const size_t bt = rr / a.Hkv;
+      t = (int)(bt % a.n_new);
+      b = (int)(bt / a.n_new);
+    }
+    const int pos0 = in ? a.seqlens[b] : 0;
+    const bool fits = pos0 >= 0 && pos0 <= a.Lmax - a.n_new;
+    if (in && !fits && t == 0 && h == 0 && j == 0) record_error(a.err, kErrInvalidArg);
+    const bool store = in && fits;
+    const size_t r = ((size_t)b * a.Hkv + h) * a.Lmax + (size_t)(store ? pos0 + t : 0);
+    float x[16];
+    {
+      uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
+      if (in) {
+        const uint4* src = reinterpret_cast<const uint4*>(kn + rr * 128 + 16 * j);
+        c0 = __ldg(src);
+        c1 = __ldg(src + 1);
+      }
+      const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        x[2 * i] = bf16_lo(w[i]);
+        x[2 * i + 1] = bf16_hi(w[i]);
+      }
+    }
+    uint2 codes;
+    uint32_t sb;
+    nvfp4_block(x, sk, codes, sb);
+    if (store) *reinterpret_cast<uint2*>(a.kc + r * 64 + 8 * j) = codes;
+    {
+      const uint32_t b1 = __shfl_down_sync(0xffffffffu, sb, 1);
+      const uint32_t b2 = __shfl_down_sync(0xffffffffu, sb, 2);
+      const uint32_t b3 = __shfl_down_sync(0xffffffffu, sb, 3);
+      if (store && (j & 3) == 0)
+        *reinterpret_cast<uint32_t*>(a.ks + sf_offset(r, j)) =
+            sb | (b1 << 8) | (b2 << 16) | (b3 << 24);
+    }
+    if (in) {
+      const uint4* src = reinterpret_cast<const uint4*>(vn + rr * 128 + 16 * j);
+      const uint4 c0 = __ldg(src), c1 = __ldg(src + 1);
+      const uint32_t w8[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        x[2 * i] = bf16_lo(w8[i]);
+        x[2 * i + 1] = bf16_hi(w8[i]);
+      }
+      float xm = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) xm = fmaxf(xm, fabsf(x[i]));
+      uint32_t w[4];
+      if (vfast && xm <= 3.40282347e38f) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          w[q] = e4m3x4(div_rn(x[4 * q], sv, ysv), div_rn(x[4 * q + 1], sv, ysv),
+                        div_rn(x[4 * q + 2], sv, ysv), div_rn(x[4 * q + 3], sv, ysv));
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          w[q] = e4m3x4(__fdiv_rn(x[4 * q], sv), __fdiv_rn(x[4 * q + 1], sv),
+                        __fdiv_rn(x[4 * q + 2], sv), __fdiv_rn(x[4 * q + 3], sv));
+      }
+      if (store)
+        *reinterpret_cast<uint4*>(a.vc + r * 128 + 16 * j) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
 int num_sms() {
   static int n = 0;
   if (!n) {
@@ -616,6 +712,15 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
   }
   dim3 grid(sms * 8, 4);
   quant_kernel<<<grid, kThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
+  const size_t units = (size_t)a.B * a.n_new * a.Hkv * 8;
+  if (units == 0) return cudaSuccess;
+  const size_t need = (units + kThreads - 1) / kThreads;
+  const size_t cap = (size_t)num_sms() * 8;
+  append_kernel<<<(unsigned)(need < cap ? need : cap), kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -193,6 +193,32 @@ mpfa_status mpfa_decode(const void *q_bf16, const mpfa_nvfp4 *k_cache, const mpf
                         mpfa_nvfp4 *q_quant_out, mpfa_rank1 *qbar_quant_out, int *used_chunk,
                         void *workspace, size_t ws_bytes, mpfa_stream_t stream);
 
+/*
+ * Quantize-on-append into a decode KV cache (the decode workload's producer:
+ * the MpFA abstract's KV operands quantized when they are written; NVFP4 K
+ * and FP8 V formats per the FP4 explainer section).  The n_new new tokens of
+ * every sequence are quantized with the cache's existing tensor scales
+ * (*k_cache->tensor_scale, *v_cache->tensor_scale, as mpfa_quantize_qkv set
+ * them when it built the cache; the scales do not change, so values beyond
+ * the cache's range saturate at the largest block scale and code) and
+ * written to cache rows seqlens[b] .. seqlens[b] + n_new - 1 of each
+ * (b, KV head), codes and tiled scales exactly as mpfa_quantize_qkv writes a
+ * row with those tensor scales.
+ *   k_new_bf16, v_new_bf16 [B][n_new][Hkv][d] bf16, device.
+ *   seqlens int32 [B], device: read, not advanced (pass seqlens + n_new to
+ *   the next mpfa_decode).  A sequence with seqlens[b] < 0 or
+ *   seqlens[b] + n_new > Lmax is left untouched and MPFA_ERR_INVALID_ARG is
+ *   recorded in the device status word (mpfa_get_error); the others are
+ *   appended.
+ *   k_cache / v_cache: as mpfa_quantize_qkv returned them for a [B][Lmax]
+ *   cache; Lmax multiple of 128, 1 <= n_new <= Lmax, B*Hkv*Lmax below 2^31
+ *   rows, d = 128 (else MPFA_ERR_UNSUPPORTED).  Host-checkable errors return
+ *   MPFA_ERR_INVALID_ARG with nothing enqueued.
+ */
+mpfa_status mpfa_append_kv(const void *k_new_bf16, const void *v_new_bf16, const int32_t *seqlens,
+                           int B, int n_new, int Hkv, int d, int Lmax, mpfa_nvfp4 *k_cache,
+                           mpfa_fp8 *v_cache, mpfa_stream_t stream);
+
 /* Failure-path self-test: enqueues a one-thread kernel that waits, with the
  * same bounded barrier wait every kernel uses, on an on-chip barrier that
  * nothing arrives on.  After limit_ns nanoseconds (1 .. 2e9) the wait gives up

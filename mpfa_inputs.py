@@ -158,6 +158,21 @@ def decode_inputs(cfg: DecodeConfig, device="cpu", seed: int = 0):
     return q.to(torch.bfloat16), K.to(torch.bfloat16), V.to(torch.bfloat16), seqlens
 
 
+def append_inputs(B: int, n_new: int, Hkv: int, device="cpu", seed: int = 0, d: int = 128,
+                  spike: float = 0.0):
+    """New decode tokens to append to a cache: K, V [B, n_new, Hkv, d] bf16,
+    N(0,1) draws; with spike > 0, one K channel and every 7th V element of
+    the first new token of each sequence are scaled by spike (values beyond
+    the cache's quantization range)."""
+    g = _gen(device, seed)
+    K = torch.randn(B, n_new, Hkv, d, generator=g, device=device)
+    V = torch.randn(B, n_new, Hkv, d, generator=g, device=device)
+    if spike > 0:
+        K[:, 0, :, 3] *= spike
+        V[:, 0, :, ::7] *= spike
+    return K.to(torch.bfloat16), V.to(torch.bfloat16)
+
+
 def custom_prefill(B, Hq, Hkv, N, causal, *, k_offset=True, k_outliers=1, v_outlier_p=0.001,
                    q_offset=False, name="custom") -> PrefillConfig:
     return PrefillConfig(name, B, Hq, Hkv, N, causal, k_offset, k_outliers, v_outlier_p,

@@ -27,7 +27,7 @@ def test_header_declares_entry_points():
     names = _declared()
     for n in ("mpfa_quantize_qkv", "mpfa_prefill", "mpfa_decode", "mpfa_get_error",
               "mpfa_status_string", "mpfa_quantize_workspace_size",
-              "mpfa_decode_workspace_size"):
+              "mpfa_decode_workspace_size", "mpfa_append_kv"):
         assert n in names
 
 
@@ -118,3 +118,37 @@ def test_host_validation_rejects_bad_shapes_and_pointers(lib):
               _fake(ok), ctypes.c_size_t(1 << 50), None) == 1
     assert qq(None, _fake(ok), _fake(ok), 1024, 0, 1 << 21, 4, 2, 128, 0, 2, None, None, R(k),
               R(v), _fake(ok), ctypes.c_size_t(1 << 50), None) == 1
+
+
+def test_append_kv_host_validation(lib):
+    """mpfa_append_kv rejects bad shapes and pointers before any CUDA call."""
+    class NV(ctypes.Structure):
+        _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                    ("tensor_scale", ctypes.c_void_p)]
+
+    class F8(ctypes.Structure):
+        _fields_ = [("codes", ctypes.c_void_p), ("tensor_scale", ctypes.c_void_p)]
+
+    ok = 0x10000
+    k, v, R = NV(ok, ok, ok), F8(ok, ok), ctypes.byref
+    a = lib.mpfa_append_kv
+    a.restype = ctypes.c_int
+    args = dict(kn=_fake(ok), vn=_fake(ok), sl=_fake(ok), B=2, n=1, H=2, d=128, L=256)
+
+    def call(**kw):
+        x = {**args, **kw}
+        return a(x["kn"], x["vn"], x["sl"], x["B"], x["n"], x["H"], x["d"], x["L"],
+                 kw.get("k", R(k)), kw.get("v", R(v)), None)
+
+    assert call(d=64) == 2                      # head dim other than 128
+    assert call(kn=None) == 1                   # null new K
+    assert call(vn=_fake(ok + 8)) == 1          # misaligned new V
+    assert call(sl=None) == 1                   # no lengths
+    assert call(L=200) == 1                     # Lmax not a multiple of 128
+    assert call(n=0) == 1                       # nothing to append
+    assert call(n=257) == 1                     # more new tokens than the cache holds
+    assert call(k=None) == 1                    # no cache
+    assert call(k=R(NV(ok, None, ok))) == 1     # cache without scales
+    assert call(v=R(F8(ok, None))) == 1         # cache without its tensor scale
+    assert call(B=4096, H=8, L=1 << 16) == 1    # 2^31 cache rows or more
+
