@@ -1,5 +1,6 @@
 // api.cu -- the C ABI declared in include/mpfa.h: argument validation, the
 // device status word, workspace carving and kernel launches.
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -9,23 +10,25 @@
 
 namespace {
 
-// Device status word: kernels record MPFA_ERR_TIMEOUT here when a bounded
-// on-chip wait expires.  One word per device (static storage, not an
-// allocation); its address is looked up once per device.
+// Device status word: kernels record MPFA_ERR_TIMEOUT (an expired bounded
+// on-chip wait) or MPFA_ERR_INVALID_ARG (a device-side argument check) here.
+// One word per device (static storage, not an allocation); its address is
+// looked up once per device and cached (atomically: concurrent first calls
+// from several host threads are safe).
 __device__ int g_status;
 
-constexpr int kMaxDevices = 64;
-int* g_status_ptr[kMaxDevices] = {nullptr};
+std::atomic<int*> g_status_ptr[mpfa::kMaxDevices];
 
 int* status_ptr() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!g_status_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
-    g_status_ptr[dev] = static_cast<int*>(p);
-  }
-  return g_status_ptr[dev];
+  const int dev = mpfa::current_device();
+  if (dev < 0) return nullptr;
+  int* p = g_status_ptr[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  void* v = nullptr;
+  if (cudaGetSymbolAddress(&v, g_status) != cudaSuccess || !v) return nullptr;
+  p = static_cast<int*>(v);
+  g_status_ptr[dev].store(p, std::memory_order_release);
+  return p;
 }
 
 // One thread waits on a shared-memory barrier that nothing arrives on; the
@@ -177,9 +180,8 @@ mpfa_status mpfa_prefill(const mpfa_nvfp4* q, const mpfa_rank1* qbar, const mpfa
 
 size_t mpfa_decode_workspace_size(int B, int Hq, int Hkv, int d, int Lmax, int kv_chunk) {
   if (d != 128 || B <= 0 || Hq <= 0 || Hkv <= 0 || Lmax <= 0) return 0;
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess)
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int sms = mpfa::sm_count(mpfa::current_device());
+  if (sms <= 0) sms = 148;
   int chunk = kv_chunk > 0 ? kv_chunk : mpfa::decode_default_chunk(B, Hkv, Lmax, sms);
   int nsplit = (Lmax + chunk - 1) / chunk;
   return mpfa::decode_workspace_bytes(B, Hq, Hkv, nsplit);
@@ -200,9 +202,8 @@ mpfa_status mpfa_decode(const void* q_bf16, const mpfa_nvfp4* k_cache, const mpf
     return MPFA_ERR_INVALID_ARG;
   if (Hq / Hkv > 16) return MPFA_ERR_UNSUPPORTED;
   if ((uint64_t)B * Hkv * Lmax >= (1ull << 31)) return MPFA_ERR_INVALID_ARG;
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess)
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int sms = mpfa::sm_count(mpfa::current_device());
+  if (sms <= 0) sms = 148;
   const int chunk = kv_chunk > 0 ? kv_chunk : mpfa::decode_default_chunk(B, Hkv, Lmax, sms);
   const int nsplit = (Lmax + chunk - 1) / chunk;
   const size_t need = mpfa::decode_workspace_bytes(B, Hq, Hkv, nsplit);

@@ -203,7 +203,12 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
   const int b = bk / a.Hkv;
   const int g = a.Hq / a.Hkv;
   const int T = a.compensate ? a.T : 0;
-  const int L = a.seqlens[b];
+  // 0 <= seqlens[b] <= Lmax is the caller's contract; a length outside it is
+  // clamped (so no split reads past its own cache rows) and recorded as
+  // MPFA_ERR_INVALID_ARG in the status word
+  const int L_in = a.seqlens[b];
+  const int L = L_in < 0 ? 0 : (L_in > a.Lmax ? a.Lmax : L_in);
+  if (L != L_in && threadIdx.x == 0 && split == 0) record_error(a.err, kErrInvalidArg);
   const int k0 = split * a.chunk;
   const int k1 = min(L, k0 + a.chunk);
   const int ntiles = k1 > k0 ? (k1 - k0 + 127) / 128 : 0;
@@ -590,24 +595,25 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
 // Resident split CTAs per SM, from the kernel's registers and shared memory
 // against the SM's register file and shared-memory capacity (1 KB of each
 // CTA's shared memory is reserved by the system).
-static int split_ctas_per_sm() {
-  static int occ = 0;
-  if (!occ) {
-    int dev = 0, smem_sm = 0, regs_sm = 0;
-    cudaFuncAttributes fa{};
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) ==
-            cudaSuccess &&
-        cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) ==
-            cudaSuccess &&
-        cudaFuncGetAttributes(&fa, split_kernel) == cudaSuccess && fa.numRegs > 0) {
-      const int by_smem = smem_sm / (int)(kSmemBytes + fa.sharedSizeBytes + 1024);
-      const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
-      const int by_regs = regs_sm / (regs_warp * (kThreads / 32));
-      occ = by_smem < by_regs ? by_smem : by_regs;
-    }
-    if (occ < 1) occ = 1;
+static int split_ctas_per_sm(int dev) {
+  static std::atomic<int> occ_of[kMaxDevices];
+  if (dev < 0 || dev >= kMaxDevices) return 1;
+  int occ = occ_of[dev].load(std::memory_order_acquire);
+  if (occ > 0) return occ;
+  int smem_sm = 0, regs_sm = 0;
+  cudaFuncAttributes fa{};
+  if (cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) ==
+          cudaSuccess &&
+      cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) ==
+          cudaSuccess &&
+      cudaFuncGetAttributes(&fa, split_kernel) == cudaSuccess && fa.numRegs > 0) {
+    const int by_smem = smem_sm / (int)(kSmemBytes + fa.sharedSizeBytes + 1024);
+    const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
+    const int by_regs = regs_sm / (regs_warp * (kThreads / 32));
+    occ = by_smem < by_regs ? by_smem : by_regs;
   }
+  if (occ < 1) occ = 1;
+  occ_of[dev].store(occ, std::memory_order_release);
   return occ;
 }
 
@@ -619,7 +625,7 @@ static int split_ctas_per_sm() {
 int decode_default_chunk(int B, int Hkv, int Lmax, int num_sms) {
   constexpr long long kCtaCostTiles = 4;
   const long long units = (long long)B * Hkv;
-  const long long slots = (long long)split_ctas_per_sm() * num_sms;
+  const long long slots = (long long)split_ctas_per_sm(current_device()) * num_sms;
   const long long tiles = (Lmax + 127) / 128;
   long long best_n = 1, best_cost = -1;
   for (long long n = 1; n <= tiles; ++n) {
@@ -649,12 +655,11 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (!make_map_2d_u8(&mk, a.kc, 64, rows, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map_2d_u8(&mv, a.vc, 128, rows, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
+  static std::atomic<bool> attr_set[kMaxDevices];
+  {
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(split_kernel), kSmemBytes,
+                                  current_device(), attr_set);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   cudaError_t e = cudaMemsetAsync(a.amax, 0, sizeof(unsigned), stream);
   if (e != cudaSuccess) return e;

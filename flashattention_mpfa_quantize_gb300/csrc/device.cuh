@@ -11,6 +11,7 @@
 namespace mpfa {
 
 // Status codes stored in the device status word (same values as mpfa_status).
+constexpr int kErrInvalidArg = 1;
 constexpr int kErrTimeout = 4;
 
 // Online softmax of the QK4PV8 forward: P is stored as E4M3(2^kPShift p) with

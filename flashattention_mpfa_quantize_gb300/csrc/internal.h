@@ -2,11 +2,27 @@
 // the kernel translation units.  Not part of the public ABI.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
 
 namespace mpfa {
+
+// ---------------------------------------------------------------------------
+// per-device host state (keyed by device ordinal; safe for concurrent first
+// calls from several host threads).  The cached values assume the device's
+// primary context is not reset while the library is loaded.
+// ---------------------------------------------------------------------------
+constexpr int kMaxDevices = 64;
+
+// Current device ordinal in [0, kMaxDevices), or -1.
+int current_device();
+// Multiprocessor count of `dev` (cached), or 0 on failure.
+int sm_count(int dev);
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) of `func` on `dev`, done
+// once per device (`done` is the kernel's own per-device flag array).
+cudaError_t set_smem_once(const void* func, int bytes, int dev, std::atomic<bool> (&done)[kMaxDevices]);
 
 // Everything the two quantization passes need.  Pointers are device pointers;
 // a tensor whose input pointer is null is skipped.

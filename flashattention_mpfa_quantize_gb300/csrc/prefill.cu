@@ -725,12 +725,13 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
       !make_map_2d_u8_box(&mo, a.o, (uint64_t)a.Hq * 256, (uint64_t)a.Hq * 256,
                           (uint64_t)a.B * a.N, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  static std::atomic<bool> attr_set[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  {
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(prefill_kernel), kSmemBytes, dev,
+                                  attr_set);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   Params p;
   p.a = a;
@@ -738,19 +739,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.q_tiles = a.N / 128;
   p.items = p.q_tiles * a.B * a.Hq;
   if (p.items == 0) return cudaSuccess;
-  int dev = 0, sms = 0;
-  {
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    static int sms_of[64] = {};
-    if (dev >= 0 && dev < 64 && sms_of[dev] > 0) {
-      sms = sms_of[dev];
-    } else {
-      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-      if (e != cudaSuccess) return e;
-      if (dev >= 0 && dev < 64) sms_of[dev] = sms;
-    }
-  }
+  const int sms = sm_count(dev);
+  if (sms <= 0) return cudaErrorInvalidDevice;
   // persistent: one CTA per SM (shared memory and TMEM admit one), each
   // walking its share of the work items
   const unsigned grid = (unsigned)(p.items < sms ? p.items : sms);

@@ -577,7 +577,6 @@ __global__ void __launch_bounds__(kThreads, 6) quant_kernel(QuantArgs a) {
 // quantize-on-append into a decode cache
 // ---------------------------------------------------------------------------
 
-constexpr int kErrInvalidArg = 1;  // MPFA_ERR_INVALID_ARG in the device status word
 
 // New K and V rows, quantized with the cache's tensor scales exactly as the
 // quant pass codes them (the same block and element arithmetic), written at
@@ -670,14 +669,8 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
 }
 
 int num_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
+  const int n = sm_count(current_device());
+  return n > 0 ? n : 148;
 }
 
 }  // namespace

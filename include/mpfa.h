@@ -25,6 +25,10 @@
  *    1 or 2).  A failed launch returns MPFA_ERR_CUDA.  A kernel whose bounded
  *    wait on an on-chip barrier expires records MPFA_ERR_TIMEOUT in a device
  *    status word and exits; mpfa_get_error reports it.
+ *  - Per-device state (the status word's address, kernel attributes, SM
+ *    counts) is looked up on a device's first call and cached; the cache
+ *    assumes the device's primary context is not reset while the library is
+ *    loaded.
  *
  * Quantized layouts
  * -----------------
@@ -175,8 +179,10 @@ size_t mpfa_decode_workspace_size(int B, int Hq, int Hkv, int d, int Lmax, int k
  * quantized KV cache.
  *   q_bf16 [B][Hq][d]; k_cache codes [B][Hkv][Lmax][64] + tiled scales,
  *   v_cache codes [B][Hkv][Lmax][128]; seqlens int32 [B] (device) with
- *   0 <= seqlens[b] <= Lmax.  Lmax multiple of 128; B*Hkv*Lmax below 2^31
- *   rows.
+ *   0 <= seqlens[b] <= Lmax.  A length outside that range is clamped to it
+ *   on the device (no read leaves the sequence's own cache rows) and
+ *   MPFA_ERR_INVALID_ARG is recorded in the device status word
+ *   (mpfa_get_error).  Lmax multiple of 128; B*Hkv*Lmax below 2^31 rows.
  *   The query is quantized inside the call (rank-one block = the Hq/Hkv
  *   heads of one KV head).  Keys [s*C, min(L, (s+1)*C)) form split s
  *   (C = kv_chunk, a multiple of 128; 0 = chosen by the library, returned in

@@ -462,3 +462,163 @@ def test_decode_emulate_matches_prefill_last_row():
     dec = orc.decode_emulate(dq, kz, vz, np.array([L]), chunk=0)[(0, 0)]
     np.testing.assert_array_equal(dec[0], pre[0][0])
     assert dec[1] == pre[1][0]
+
+
+# --------------------------------------------------------------------------
+# the score scale (t = S s_q s_k log2(e) / sqrt(d)) and the LSE it implies
+# --------------------------------------------------------------------------
+
+def _rn32(x):
+    """Nearest binary32 (ties to even) of an exact rational x (fractions.Fraction),
+    by integer arithmetic alone: no intermediate float rounding."""
+    from fractions import Fraction
+    x = Fraction(x)
+    if x == 0:
+        return np.float32(0.0)
+    sign = -1 if x < 0 else 1
+    a = abs(x)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    e = max(e, -126)                       # subnormals share the smallest exponent
+    scaled = a / Fraction(2) ** (e - 23)    # 24-bit significand + fraction
+    m = scaled.numerator // scaled.denominator
+    rem = scaled - m
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and m % 2 == 1):
+        m += 1
+    return np.float32(sign * float(Fraction(m) * Fraction(2) ** (e - 23)))
+
+
+def _log2e_rsqrt_d_exact(d=128, digits=60):
+    """log2(e) / sqrt(d) to `digits` decimal digits (mpmath), as a Fraction."""
+    from fractions import Fraction
+    import mpmath
+    with mpmath.workdps(digits):
+        v = 1 / (mpmath.log(2) * mpmath.sqrt(d))
+        return Fraction(mpmath.nstr(v, digits, strip_zeros=False))
+
+
+def test_score_scale_log2_bit_exact():
+    """The factor taking accumulated code products to log2-domain logits is
+    t = S * s_q * s_k * log2(e) / sqrt(d) (the explainer's attention section:
+    S = Q K^T / sqrt(d), evaluated with exp2), with the fp32 roundings the
+    kernels apply: c = RN32(log2(e)/sqrt(128)), then RN32(RN32(s_q s_k) c).
+    The constant is derived here from 60-digit log and sqrt with exact
+    rational rounding, independently of the oracle's fp64 expression."""
+    from fractions import Fraction
+    c = _rn32(_log2e_rsqrt_d_exact())
+    assert orc.score_scale_log2(1.0, 1.0) == float(c)
+    rng = np.random.default_rng(91)
+    # tensor scales as the quantizers produce them (amax / 2688 for amax over a
+    # wide range), plus powers of two and values whose product hits a tie
+    sq = [orc.tensor_scale(a, 2688.0) for a in rng.uniform(1e-3, 3e3, 300)]
+    sk = [orc.tensor_scale(a, 2688.0) for a in rng.uniform(1e-3, 3e3, 300)]
+    sq += [np.float32(1.0), np.float32(2.0 ** -7), np.float32(1 + 2 ** -12)]
+    sk += [np.float32(3.0), np.float32(2.0 ** 5), np.float32(1 + 2 ** -12)]
+    for a, b in zip(sq, sk):
+        ab = _rn32(Fraction(float(a)) * Fraction(float(b)))
+        want = _rn32(Fraction(float(ab)) * Fraction(float(c)))
+        assert orc.score_scale_log2(a, b) == float(want), (a, b)
+
+
+def test_lse_is_natural_log_of_scaled_logits():
+    """The emulated forward's LSE is ln sum_j exp(s_q s_k q_i.k_j / sqrt(d))
+    over the dequantized codes (tensor scales included), and O is the softmax
+    average of s_v-scaled V: checked against exact fp64 attention run on the
+    scaled dequantized operands.  Unrounded P: agreement to fp32 rounding of
+    the scale; rounded P (the method): within the E4M3 rounding of P."""
+    rng = np.random.default_rng(93)
+    n = 256
+    qc = rng.integers(0, 256, (1, 1, n, 64), dtype=np.uint8)
+    kc = rng.integers(0, 256, (1, 1, n, 64), dtype=np.uint8)
+    qs = rng.integers(0x28, 0x40, (1, 1, n, 8), dtype=np.uint8)
+    ks = rng.integers(0x28, 0x40, (1, 1, n, 8), dtype=np.uint8)
+    vc = rng.integers(0, 0x7F, (1, 1, n, 128), dtype=np.uint8)
+    vc[vc == 0x7F] = 0x7E
+    s_q, s_k, s_v = np.float32(0.0173), np.float32(0.00911), np.float32(0.0377)
+    qz = dict(qc=qc, qs=qs, qbc=None, qbs=None, s_q=s_q)
+    kz = dict(kc=kc, ks=ks, s_k=s_k)
+    vz = dict(vc=vc, s_v=s_v)
+    q = orc.nvfp4_dequant(qc[0, 0], qs[0, 0]) * float(s_q)
+    k = orc.nvfp4_dequant(kc[0, 0], ks[0, 0]) * float(s_k)
+    v = orc.fp8_dequant(vc[0, 0]) * float(s_v)
+    for causal in (False, True):
+        o_ex, l_ex = orc.attn_exact(q, k, v, causal=causal)
+        cs = orc.score_scale_log2(s_q, s_k)
+        o1, l1 = orc.attn_online(orc.nvfp4_dequant(qc[0, 0], qs[0, 0]), None,
+                                 orc.nvfp4_dequant(kc[0, 0], ks[0, 0]), orc.fp8_dequant(vc[0, 0]),
+                                 score_scale=cs, out_scale=float(s_v), causal=causal,
+                                 round_p=False)
+        np.testing.assert_allclose(l1, l_ex, rtol=0, atol=1e-5 * max(1.0, np.abs(l_ex).max()))
+        np.testing.assert_allclose(o1, o_ex, rtol=1e-4, atol=1e-5)
+        o2, l2 = orc.prefill_emulate(qz, kz, vz, causal=causal)[(0, 0)]
+        assert np.abs(l2 - l_ex).max() < math.log(1 + 2.0 ** -4)
+        assert np.linalg.norm(o2 - o_ex) / np.linalg.norm(o_ex) < 0.03
+
+
+# --------------------------------------------------------------------------
+# decode: the rank-one block is the g query heads of one KV head
+# --------------------------------------------------------------------------
+
+def test_decode_zero_mean_groups_make_compensation_vanish():
+    """Query heads of each KV head's group paired (x, -x): every group mean is
+    0, so the decode codes and O are the same with and without the smoothing.
+    Grouping heads by h % Hkv instead of h // g would mix x with another
+    group's rows and give non-zero means."""
+    rng = np.random.default_rng(95)
+    B, Hkv, g, L = 2, 3, 4, 384
+    x = _bf16(rng.standard_normal((B, Hkv, g // 2, 128)) * 1.3)
+    q = np.concatenate([x, -x], axis=2).reshape(B, Hkv * g, 128)     # heads (x0, x1, -x0, -x1)
+    K = _bf16(rng.standard_normal((B, L, Hkv, 128)))
+    V = _bf16(rng.standard_normal((B, L, Hkv, 128)))
+    on = orc.quantize_q_decode(q, Hkv, True, 2)
+    off = orc.quantize_q_decode(q, Hkv, False)
+    assert on["s_q"] == off["s_q"]
+    np.testing.assert_array_equal(on["qc"] & 0x77, off["qc"] & 0x77)
+    np.testing.assert_array_equal(on["qs"], off["qs"])
+    assert (on["qbs"] == 0).all() and (on["qbc"] & 0x77 == 0).all()
+    kz, vz = orc.quantize_k(K), orc.quantize_v(V)
+    lens = np.array([L, 200])
+    a = orc.decode_emulate(on, kz, vz, lens, chunk=128)
+    b = orc.decode_emulate(off, kz, vz, lens, chunk=128)
+    for key in a:
+        np.testing.assert_array_equal(a[key][0], b[key][0])
+        assert a[key][1] == b[key][1]
+
+
+def test_decode_compensation_exact_for_representable_group_means():
+    """All g query heads of KV head k equal to a vector mu_k that NVFP4
+    represents exactly (a different mu per group): with the smoothing, q' = 0
+    and the rank-one term alone carries mu_k, so decode O equals the
+    unsmoothed O bit for bit.  A rank-one block other than "the g heads of KV
+    head h // g" (e.g. h % Hkv) would average different mu and break it."""
+    rng = np.random.default_rng(97)
+    B, Hkv, g, L = 2, 2, 4, 256
+    s = 2.0 ** -6
+    e4 = np.array([orc.e4m3_value(c) for c in range(0x30, 0x7F)])
+    vals16 = np.array([orc.e2m1_value(int(c)) for c in range(16)])
+    mus = np.empty((B, Hkv, 128))
+    for b in range(B):
+        for hk in range(Hkv):
+            codes = rng.integers(0, 16, 128)
+            codes[::16] = 7 + 8 * rng.integers(0, 2, 8)
+            sb = rng.choice(e4, 8)
+            sb[0] = 448.0
+            mus[b, hk] = vals16[codes] * np.repeat(sb, 16) * s
+    q = np.repeat(mus, g, axis=1).astype(np.float32)        # head h = mu[h // g]
+    assert np.array_equal(_bf16(q), q)
+    K = _bf16(rng.standard_normal((B, L, Hkv, 128)))
+    V = _bf16(rng.standard_normal((B, L, Hkv, 128)))
+    on = orc.quantize_q_decode(q, Hkv, True, 2)
+    off = orc.quantize_q_decode(q, Hkv, False)
+    assert on["s_q"] == off["s_q"] == np.float32(s)
+    assert (on["qc"] & 0x77 == 0).all()                     # q' = 0 in every head
+    assert (on["qbs"][:, :, 1] == 0).all()                   # mu exact: no residual term
+    kz, vz = orc.quantize_k(K), orc.quantize_v(V)
+    lens = np.array([L, 129])
+    a = orc.decode_emulate(on, kz, vz, lens, chunk=128)
+    b = orc.decode_emulate(off, kz, vz, lens, chunk=128)
+    for key in a:
+        np.testing.assert_array_equal(a[key][0], b[key][0])
+        assert a[key][1] == b[key][1]
+    assert not np.array_equal(a[(0, 0)][0], a[(0, g)][0])
