@@ -1,18 +1,22 @@
 """Benchmark of the MpFA QK4PV8 attention forward on GB300.
 
-One step = the whole prefill hot path on the Llama-3.1-8B attention shape
-(B=1, 32 query / 8 KV heads, d=128, N=16384, causal): online NVFP4/FP8
-quantization of Q, K, V (mpfa_quantize_qkv) followed by the prefill kernel
-(mpfa_prefill), on synthetic inputs resident in HBM.  ``value`` is the
-algorithmic attention TFLOP/s of that step (512 FLOP per visible
-(query, key) pair: 256 for QK^T in FP4, 256 for PV in FP8).  L2 is flushed
-(a 512 MB write) before every timed step.
+One step = the whole prefill hot path on the largest single-GPU workload,
+the Qwen3-14B attention shape at 128K (B=1, 40 query / 8 KV heads, d=128,
+N=131072, causal): online NVFP4/FP8 quantization of Q, K, V
+(mpfa_quantize_qkv) followed by the prefill kernel (mpfa_prefill), on
+synthetic inputs resident in HBM.  ``value`` is the algorithmic attention
+TFLOP/s of that step (512 FLOP per visible (query, key) pair: 256 for QK^T in
+FP4, 256 for PV in FP8).  The inputs (1.9 GB of bf16) are larger than L2,
+and L2 is also flushed (a 512 MB write) before every timed step.
 
 The same JSON line carries:
   roofline      prefill kernel vs the FP4/FP8 tensor-pipe roofline
-  decode        split-KV decode on B=64 x 32K cached tokens: KV GB/s vs HBM
+  prefill_other the other prefill workloads (Llama-3.1-8B shape at 16K, the
+                B1/S4096/H24 and B1/S8192/H64 grid), each with its roofline
+  decode        split-KV decode on B=64 x 32K and on B=64 x U[4K, 64K]
+                cached tokens: KV GB/s vs HBM
   e2e           the step through the C ABI with host buffers (pinned H2D of
-                bf16 Q/K/V, D2H of O) inside the timed region
+                bf16 Q/K/V, D2H of O and LSE) inside the timed region
   cpu_baseline  the CPU oracle on a bounded sample of the same workload
   clocks        nvidia-smi samples taken during the timed region
 
@@ -21,8 +25,8 @@ The same JSON line carries:
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -38,15 +42,19 @@ import torch  # noqa: E402
 import mpfa_inputs as mi  # noqa: E402
 
 METRIC = "prefill attention TFLOP/s & decode KV GB/s on 1 GB300, % of FP4/FP8/HBM roofline"
-PREFILL_CFG = mi.PREFILL["llama8b_n16k_causal"]
-DECODE_CFG = mi.DECODE["decode_b64_l32k"]
+HEADLINE = "qwen14b_n128k_causal"
+OTHER_PREFILL = ("llama8b_n16k_causal", "b1_s4096_h24", "b1_s8192_h64")
+DECODES = ("decode_b64_l32k", "decode_b64_l4k_64k")
 FLOP_PER_PAIR = 512
 KV_BYTES_PER_TOKEN = 64 + 8 + 128   # K codes + K block scales + V codes, per KV head
-# prefill_kernel inputs and outputs per launch on the 16K workload: Q codes +
-# block scales, rank-one terms, K codes + scales, V codes, O (bf16) and LSE
-PREFILL_ALGO_BYTES = (PREFILL_CFG.B * PREFILL_CFG.N * (PREFILL_CFG.Hq * (64 + 8 + 128 * 2 + 4)
-                                                       + PREFILL_CFG.Hkv * (64 + 8 + 128))
-                      + PREFILL_CFG.B * PREFILL_CFG.Hq * (PREFILL_CFG.N // 128) * 2 * 72)
+T_TERMS = 2
+
+
+def prefill_algo_bytes(cfg, T=T_TERMS) -> int:
+    """prefill_kernel inputs and outputs per launch: Q codes + block scales,
+    rank-one terms, K codes + scales, V codes, O (bf16) and LSE."""
+    return (cfg.B * cfg.N * (cfg.Hq * (64 + 8 + 128 * 2 + 4) + cfg.Hkv * (64 + 8 + 128))
+            + cfg.B * cfg.Hq * (cfg.N // 128) * T * 72)
 
 
 def _peaks():
@@ -105,7 +113,7 @@ class Clocks:
             self.proc.kill()
             self.proc.wait()
         self.thread.join(timeout=5)
-        sm, mx, reasons = [], None, set()
+        sm, mx, power, reasons = [], None, [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.lines[self.skip:]:
             f = [x.strip() for x in line.split(",")]
@@ -114,6 +122,7 @@ class Clocks:
             try:
                 sm.append(float(f[1]))
                 mx = float(f[2])
+                power.append(float(f[3]))
             except ValueError:
                 continue
             for nm, v in zip(names, f[5:9]):
@@ -122,32 +131,32 @@ class Clocks:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "power_w_max": max(power) if power else None}
 
 
-def measured_traffic(kernel: str):
-    """DRAM bytes per launch (read + write) of `kernel` from the ncu table in
-    profiles/traffic.md, or None when the kernel's sources have changed since
-    the counters were taken (sha256 of the listed files)."""
-    import hashlib
-    path = os.path.join(ROOT, "profiles", "traffic.md")
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch (read + write) of `kernel` on `workload` from the
+    ncu figures in profiles/traffic.json, or None when the kernel's sources
+    have changed since the counters were taken (sha256 of the listed files)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     csrc = os.path.join(ROOT, "flashattention_mpfa_quantize_gb300", "csrc")
-    for line in open(path):
-        f = [x.strip() for x in line.strip().strip("|").split("|")]
-        if len(f) < 6 or f[0] != kernel:
+    with open(path) as f:
+        doc = json.load(f)
+    for row in doc.get("kernels", []):
+        if row.get("kernel") != kernel or row.get("workload") != workload:
             continue
         h = hashlib.sha256()
         try:
-            for src in f[1].split():
+            for src in row["sources"]:
                 with open(os.path.join(csrc, src), "rb") as fh:
                     h.update(fh.read())
         except OSError:
             return None
-        if h.hexdigest()[:16] != f[2]:
+        if h.hexdigest()[:16] != row["sha16"]:
             return None
-        return int(f[4]) + int(f[5])
+        return int(round((int(row["read"]) + int(row["write"])) * float(row.get("scale", 1.0))))
     return None
 
 
@@ -187,31 +196,30 @@ def _host_f32(x):
     return x if isinstance(x, np.ndarray) else x.float().cpu().numpy()
 
 
-def oracle_scales(Qn, Kn, Vn):
+def oracle_scales(cfg, Qn, Kn, Vn):
     """Whole-tensor statistics the codes depend on (tensor scales of Q' with
     the rank-one smoothing, K and V).  Returns ((s_q, s_k, s_v), seconds)."""
     import numpy as np
 
     import oracle as orc
-    cfg = PREFILL_CFG
     t0 = time.perf_counter()
     amax_q = np.float32(0)
-    for h in range(cfg.Hq):
-        qb, qp = orc.block_means(np.ascontiguousarray(Qn[0, :, h, :]), 128)
-        amax_q = max(amax_q, np.float32(np.abs(qp).max()), np.float32(np.abs(qb).max()))
+    for b in range(cfg.B):
+        for h in range(cfg.Hq):
+            qb, qp = orc.block_means(np.ascontiguousarray(Qn[b, :, h, :]), 128)
+            amax_q = max(amax_q, np.float32(np.abs(qp).max()), np.float32(np.abs(qb).max()))
     s = (orc.tensor_scale(amax_q, 2688.0), orc.tensor_scale(np.abs(Kn).max(), 2688.0),
          orc.tensor_scale(np.abs(Vn).max(), 448.0))
     return s, time.perf_counter() - t0
 
 
-def oracle_heads(Qn, Kn, Vn, scales, rows_per_head, heads):
+def oracle_heads(cfg, Qn, Kn, Vn, scales, rows_per_head, heads):
     """Codes of the sampled heads and the emulated forward of sampled query
     rows (spread over the sequence, full causal key range each).
     Returns (flops, seconds, rows)."""
     import numpy as np
 
     import oracle as orc
-    cfg = PREFILL_CFG
     g = cfg.Hq // cfg.Hkv
     s_q, s_k, s_v = scales
     t0 = time.perf_counter()
@@ -222,7 +230,7 @@ def oracle_heads(Qn, Kn, Vn, scales, rows_per_head, heads):
         hk = h // g
         qb, qp = orc.block_means(np.ascontiguousarray(Qn[b, :, h, :]), 128)
         qc, qs = orc.nvfp4_quantize(qp, s_q)
-        tc, ts = orc.rank_one_terms(qb, s_q, 2)
+        tc, ts = orc.rank_one_terms(qb, s_q, T_TERMS)
         kc, ks = orc.nvfp4_quantize(np.ascontiguousarray(Kn[b, :, hk, :]), s_k)
         vc = orc.fp8_quantize(np.ascontiguousarray(Vn[b, :, hk, :]), s_v)
         qz = dict(qc=qc[None, None], qs=qs[None, None], qbc=tc[None, None], qbs=ts[None, None],
@@ -234,18 +242,19 @@ def oracle_heads(Qn, Kn, Vn, scales, rows_per_head, heads):
     return flops, time.perf_counter() - t0, rows.size
 
 
-def oracle_sample(Q, K, V, rows_per_head=64, heads=((0, 0), (0, 9), (0, 22), (0, 31))):
+def oracle_sample(cfg, Q, K, V, rows_per_head, heads):
     """Time the CPU oracle on a bounded sample of the prefill workload: the
     whole-tensor statistics, the codes of the sampled heads and the emulated
     forward of the sampled rows.  Returns (tflops, seconds, description,
     threads)."""
     import oracle as orc
     Qn, Kn, Vn = _host_f32(Q), _host_f32(K), _host_f32(V)
-    scales, t_s = oracle_scales(Qn, Kn, Vn)
-    flops, t_h, nrows = oracle_heads(Qn, Kn, Vn, scales, rows_per_head, heads)
+    scales, t_s = oracle_scales(cfg, Qn, Kn, Vn)
+    flops, t_h, nrows = oracle_heads(cfg, Qn, Kn, Vn, scales, rows_per_head, heads)
     dt = t_s + t_h
-    desc = (f"{len(heads)} heads x {nrows} query rows of {PREFILL_CFG.name} (full causal key "
-            f"range each), incl. whole-tensor amax and per-head quantization")
+    desc = (f"{len(heads)} heads x {nrows} query rows of {cfg.name} (full causal key "
+            f"range each), incl. whole-tensor statistics ({t_s:.1f} s) and per-head "
+            f"quantization")
     return flops / dt / 1e12, dt, desc, orc.num_threads()
 
 
@@ -253,9 +262,9 @@ REFERENCE_BUDGET_S = 90.0   # oracle time of a whole --impl reference run
 
 
 def run_reference(args):
-    """The CPU oracle as it stands on the prefill workload.  The whole-tensor
+    """The CPU oracle as it stands on the headline workload.  The whole-tensor
     statistics are computed once per run (their time counts, spread over the
-    steps); each step then quantizes its sampled heads and emulates sampled
+    steps); each step then quantizes a sampled head and emulates sampled
     query rows, sized from two calibration samples so the timed work takes
     about REFERENCE_BUDGET_S in all, whatever --steps is."""
     ws, rank, _ = _dist()
@@ -263,37 +272,38 @@ def run_reference(args):
         return
     import oracle as orc
     orc.build()
-    Q, K, V = mi.prefill_inputs(PREFILL_CFG, "cpu", 0)
+    cfg = mi.PREFILL[args.workload]
+    Q, K, V = mi.prefill_inputs(cfg, "cpu", 0)
     Qn, Kn, Vn = Q.float().numpy(), K.float().numpy(), V.float().numpy()
+    del Q, K, V
     for _ in range(max(args.warmup, 1)):
-        oracle_heads(Qn, Kn, Vn, (1.0, 1.0, 1.0), 2, ((0, 0),))
-    scales, t_scales = oracle_scales(Qn, Kn, Vn)
+        oracle_heads(cfg, Qn, Kn, Vn, (1.0, 1.0, 1.0), 2, ((0, 0),))
+    scales, t_scales = oracle_scales(cfg, Qn, Kn, Vn)
     heads = ((0, 0),)
-    t_small = oracle_heads(Qn, Kn, Vn, scales, 2, heads)[1]
-    t_big = oracle_heads(Qn, Kn, Vn, scales, 34, heads)[1]
+    t_small = oracle_heads(cfg, Qn, Kn, Vn, scales, 2, heads)[1]
+    t_big = oracle_heads(cfg, Qn, Kn, Vn, scales, 34, heads)[1]
     per_row = max((t_big - t_small) / 32.0, 1e-6)
     target = max(REFERENCE_BUDGET_S - t_scales, 1.0) / max(args.steps, 1)
     rows = int(max(2, min(256, 2 + (target - t_small) / per_row)))
     flops_all, t_all = 0, t_scales
     times = []
+    nrows = 0
     for i in range(args.steps):
-        h = (0, (9 * i) % PREFILL_CFG.Hq)
-        f, dt, nrows = oracle_heads(Qn, Kn, Vn, scales, rows, (h,))
+        h = (0, (9 * i) % cfg.Hq)
+        f, dt, nrows = oracle_heads(cfg, Qn, Kn, Vn, scales, rows, (h,))
         flops_all += f
         t_all += dt
         times.append(dt + t_scales / max(args.steps, 1))
     value = flops_all / t_all / 1e12
     thr = orc.num_threads()
-    desc = (f"per step 1 head x {nrows} query rows of {PREFILL_CFG.name} (full causal key range "
+    desc = (f"per step 1 head x {nrows} query rows of {cfg.name} (full causal key range "
             f"each) incl. that head's quantization; whole-tensor statistics once per run "
             f"({t_scales:.2f} s, counted)")
-    vals = [value]
-    value = statistics.mean(vals)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64 (emulated nvfp4/fp8 codes)",
-            "data": "synthetic", "config": {"workload": PREFILL_CFG.name, "sample": desc},
+            "data": "synthetic", "config": {"workload": cfg.name, "sample": desc},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -305,6 +315,61 @@ def run_reference(args):
 # GPU arm
 # ----------------------------------------------------------------------------
 
+def prefill_roofline(cfg, pre_ms, peaks):
+    """prefill_kernel against the FP4 QK^T + FP8 PV tensor-pipe roofline: the
+    measured bf16 peak times the nominal dense ratios (FP4 = 6x, FP8 = 2x)."""
+    flops = FLOP_PER_PAIR * cfg.pairs
+    f4 = f8 = flops / 2
+    p4, p8 = 6 * peaks["bf16"], 2 * peaks["bf16"]
+    t_roof = f4 / (p4 * 1e12) + f8 / (p8 * 1e12)
+    peak_eff = flops / t_roof / 1e12
+    achieved = flops / (pre_ms * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": achieved, "peak": peak_eff, "unit": "TFLOP/s",
+            "frac": achieved / peak_eff, "traffic": measured_traffic("prefill_kernel", cfg.name),
+            "traffic_unit": "bytes per launch (ncu dram read + write)",
+            "algorithmic_bytes": prefill_algo_bytes(cfg), "kernel": "prefill_kernel",
+            "peak_source": peaks["source"] + " bf16 burst x nominal FP4 (6x) / FP8 (2x) "
+            "ratios, harmonic mix for equal FP4 and FP8 FLOPs"}
+
+
+def time_prefill(mp, cfg, Q, K, V, flush, stream, steps, warmup, compensate=True, T=T_TERMS,
+                 clocks=None):
+    """Quantize + prefill of `cfg` timed with CUDA events on the launching
+    stream, L2 flushed before every step.  Returns (step, quantize, prefill)
+    mean ms."""
+    z = mp.quantize_qkv(Q, K, V, compensate=compensate, T=T)
+    ws = z["_workspace"]
+    o, lse = mp.prefill(z, causal=cfg.causal)
+    for _ in range(max(warmup, 3)):
+        flush.zero_()
+        z = mp.quantize_qkv(Q, K, V, compensate=compensate, T=T, workspace=ws)
+        mp.prefill(z, causal=cfg.causal, out=o, lse=lse)
+    torch.cuda.synchronize()
+    if mp.get_error() != 0:
+        raise RuntimeError(f"device status word set during warm-up of {cfg.name}")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    if clocks is not None:
+        clocks.start()
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for ev in evs:
+        flush.zero_()
+        ev[0].record(stream)
+        z = mp.quantize_qkv(Q, K, V, compensate=compensate, T=T, workspace=ws)
+        ev[1].record(stream)
+        mp.prefill(z, causal=cfg.causal, out=o, lse=lse)
+        ev[2].record(stream)
+    torch.cuda.synchronize()
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+    if mp.get_error() != 0:
+        raise RuntimeError(f"device status word set while timing {cfg.name}")
+    return (statistics.mean(e[0].elapsed_time(e[2]) for e in evs),
+            statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
+            statistics.mean(e[1].elapsed_time(e[2]) for e in evs))
+
+
 def run_gpu(args):
     import flashattention_mpfa_quantize_gb300 as mp
     ws, rank, local = _dist()
@@ -314,98 +379,87 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     peaks = _peaks()
-    cfg = PREFILL_CFG
+    cfg = mi.PREFILL[args.workload]
     stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    launches = 0
+
+    if args.only == "decode":
+        dec = {name: run_decode(mp, dev, stream, peaks, flush, args, mi.DECODE[name])
+               for name in DECODES}
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": None, "unit": "GB/s", "n_gpus": ws,
+                              "steps": args.steps, "warmup": args.warmup, "decode": dec,
+                              "note": "profiling aid: decode only"}), flush=True)
+        return
 
     Q, K, V = mi.prefill_inputs(cfg, dev, seed=rank)
-    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    qz = mp.quantize_qkv(Q, K, V, compensate=True, T=2)
-    ws_q = qz["_workspace"]
-    o, lse = mp.prefill(qz, causal=cfg.causal)
-
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        z = mp.quantize_qkv(Q, K, V, compensate=True, T=2, workspace=ws_q)
-        if ev is not None:
-            ev[1].record(stream)
-        mp.prefill(z, causal=cfg.causal, out=o, lse=lse)
-        if ev is not None:
-            ev[2].record(stream)
-
-    for _ in range(max(args.warmup, 3)):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize()
-    if mp.get_error() != 0:
-        raise RuntimeError("device status word set during warm-up")
-
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     clocks = Clocks(dev.index)
-    if ws > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    t_wall = time.perf_counter()
-    for i in range(args.steps):
-        flush.zero_()
-        step(evs[i])
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall
-    if ws > 1:
-        torch.distributed.barrier()
+    step_ms, quant_ms, pre_ms = time_prefill(mp, cfg, Q, K, V, flush, stream, args.steps,
+                                             args.warmup, clocks=clocks)
     clk = clocks.stop()
-    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
-    quant_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    pre_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    launches += 3 * args.steps
     flops = FLOP_PER_PAIR * cfg.pairs
-    rate, ms = aggregate_rate(flops, statistics.mean(step_ms), ws, dev)
+    rate, ms = aggregate_rate(flops, step_ms, ws, dev)
     value = rate / 1e12
-
-    # prefill roofline: FP4 QK^T + FP8 PV against the measured bf16 peak times
-    # the nominal dense ratios (FP4 = 6x, FP8 = 2x bf16)
-    pre = statistics.mean(pre_ms)
-    f4 = f8 = flops / 2
-    p4, p8 = 6 * peaks["bf16"], 2 * peaks["bf16"]
-    t_roof = f4 / (p4 * 1e12) + f8 / (p8 * 1e12)
-    peak_eff = (f4 + f8) / t_roof / 1e12
-    achieved = flops / (pre * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_eff, "unit": "TFLOP/s",
-                "frac": achieved / peak_eff, "traffic": measured_traffic("prefill_kernel"),
-                "traffic_unit": "bytes per launch (ncu dram read + write)",
-                "algorithmic_bytes": PREFILL_ALGO_BYTES,
-                "kernel": "prefill_kernel", "peak_source": peaks["source"] + " bf16 burst x "
-                "nominal FP4 (6x) / FP8 (2x) ratios, harmonic mix for equal FP4 and FP8 FLOPs",
-                "quantize_ms": statistics.mean(quant_ms), "prefill_ms": pre}
-
-    # diagnostics outside the timed region: the exp-unit bound (one ex2 per
-    # pair at 32 per clock per SM on this part) and the cost of the rank-one
-    # compensation (the same step with compensation off)
+    roofline = prefill_roofline(cfg, pre_ms, peaks)
+    roofline.update({"workload": cfg.name, "quantize_ms": quant_ms, "prefill_ms": pre_ms})
+    # diagnostic: the exp-unit bound (one ex2 per pair at 32 per clock per SM)
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
     f_clk = (clk or {}).get("sm_mhz") or 2070.0
     t_exp = cfg.pairs / (n_sm * 32 * f_clk * 1e6) * 1e3
-    roofline["exp_unit"] = {"bound_ms": t_exp, "frac": t_exp / pre, "sm_mhz": f_clk,
+    roofline["exp_unit"] = {"bound_ms": t_exp, "frac": t_exp / pre_ms, "sm_mhz": f_clk,
                             "rate": "32 ex2 per clock per SM"}
-    roofline["compensation"] = compensation_cost(mp, Q, K, V, cfg, flush, stream,
-                                                 min(args.steps, 50),
-                                                 statistics.mean(quant_ms), pre)
 
-    bf16 = bf16_sdpa_baseline(Q, K, V, cfg, flush, stream, min(args.steps, 20), flops,
-                              statistics.mean(step_ms), pre)
-
-    dec = run_decode(mp, dev, stream, peaks, flush, args) if args.only != "prefill" else {}
-    e2e = run_e2e(mp, dev, stream, Q, K, V, args) if args.only is None else None
+    extra = {}
+    if args.only is None:
+        few = max(3, min(args.steps, 5))
+        roofline["compensation"] = compensation_cost(mp, cfg, Q, K, V, flush, stream, few,
+                                                     quant_ms, pre_ms)
+        extra["bf16_sdpa"] = bf16_sdpa_baseline(Q, K, V, cfg, flush, stream, few, flops,
+                                                step_ms, pre_ms)
+        e2e = run_e2e(mp, dev, stream, cfg, Q, K, V, max(3, min(args.steps, 20)))
+        launches += 3 * max(3, min(args.steps, 20)) + 6
+    else:
+        e2e = None
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and args.only is None:
         try:
-            Qc, Kc, Vc = Q.cpu(), K.cpu(), V.cpu()
-            v, dt, desc, thr = oracle_sample(Qc, Kc, Vc, rows_per_head=384,
-                                             heads=tuple((0, h) for h in range(cfg.Hq)))
+            heads = tuple((0, h) for h in range(0, cfg.Hq, max(1, cfg.Hq // 4)))[:4]
+            v, dt, desc, thr = oracle_sample(cfg, Q.cpu(), K.cpu(), V.cpu(), rows_per_head=128,
+                                             heads=heads)
             cpu = {"value": v, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
                    "sample": desc, "seconds": dt}
         except Exception as ex:  # pragma: no cover - reported, not fatal
             cpu = {"error": repr(ex)}
+    del Q, K, V
+    torch.cuda.empty_cache()
+
+    other = {}
+    if args.only is None and not args.no_secondary:
+        for name in OTHER_PREFILL:
+            if name == cfg.name:
+                continue
+            c2 = mi.PREFILL[name]
+            q2, k2, v2 = mi.prefill_inputs(c2, dev, seed=rank)
+            n2 = max(3, min(args.steps, 20))
+            s2, qm2, pm2 = time_prefill(mp, c2, q2, k2, v2, flush, stream, n2, 3)
+            launches += 3 * n2
+            r2 = prefill_roofline(c2, pm2, peaks)
+            r2.pop("peak_source")
+            other[name] = {"value": FLOP_PER_PAIR * c2.pairs / (s2 * 1e-3) / 1e12,
+                           "unit": "TFLOP/s", "ms_per_step": s2, "quantize_ms": qm2,
+                           "prefill_ms": pm2, "roofline": r2}
+            del q2, k2, v2
+            torch.cuda.empty_cache()
+
+    dec = {}
+    if args.only is None:
+        for name in DECODES:
+            d = run_decode(mp, dev, stream, peaks, flush, args, mi.DECODE[name])
+            launches += d.pop("gpu_launches")
+            dec[name] = d
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
@@ -414,13 +468,12 @@ def run_gpu(args):
                 "dtype": "nvfp4 e2m1 (QK) + fp8 e4m3 (PV), fp32 accumulate", "data": "synthetic",
                 "config": {"workload": cfg.name, "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv,
                            "N": cfg.N, "d": 128, "causal": cfg.causal, "compensate": True,
-                           "T": 2, "step": "mpfa_quantize_qkv + mpfa_prefill",
-                           "l2": "flushed (512 MB write) before every step",
+                           "T": T_TERMS, "step": "mpfa_quantize_qkv + mpfa_prefill",
+                           "l2": "inputs larger than L2, and L2 flushed (512 MB write) before "
+                                 "every step",
                            "parallelism": "replicas" if ws > 1 else "single"},
-                "roofline": roofline, "bf16_sdpa": bf16, "decode": dec, "e2e": e2e,
-                "cpu_baseline": cpu,
-                "gpu_launches": args.steps * 3 + dec.get("gpu_launches", 0),
-                "clocks": clk, "wall_s": t_wall}
+                "roofline": roofline, "prefill_other": other, "decode": dec, "e2e": e2e,
+                "cpu_baseline": cpu, "gpu_launches": launches, "clocks": clk, **extra}
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
@@ -428,20 +481,20 @@ def run_gpu(args):
 
 def bf16_sdpa_baseline(Q, K, V, cfg, flush, stream, steps, flops, step_ms, pre_ms):
     """Context, not part of the product: torch's fused bf16 attention backends
-    (flash, cuDNN, memory-efficient) on the same unquantized inputs, each
-    timed the same way; the ratios are against the fastest one."""
+    (cuDNN, flash) on the same unquantized inputs, each timed the same way;
+    the ratios are against the fastest one."""
     from torch.nn.attention import SDPBackend, sdpa_kernel
     import torch.nn.functional as F
     q, k, v = (t.transpose(1, 2).contiguous() for t in (Q, K, V))   # [B, H, N, d]
     out = {}
-    for name, be in (("flash", SDPBackend.FLASH_ATTENTION), ("cudnn", SDPBackend.CUDNN_ATTENTION),
-                     ("efficient", SDPBackend.EFFICIENT_ATTENTION)):
+    for name, be in (("cudnn", SDPBackend.CUDNN_ATTENTION),
+                     ("flash", SDPBackend.FLASH_ATTENTION)):
         try:
             with sdpa_kernel([be]):
                 def run():
                     return F.scaled_dot_product_attention(q, k, v, is_causal=cfg.causal,
                                                           enable_gqa=cfg.Hq != cfg.Hkv)
-                for _ in range(3):
+                for _ in range(2):
                     run()
                 evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                        for _ in range(max(steps, 1))]
@@ -465,32 +518,12 @@ def bf16_sdpa_baseline(Q, K, V, cfg, flush, stream, steps, flops, step_ms, pre_m
             "speedup_of_step": ms / step_ms, "speedup_of_prefill_kernel": ms / pre_ms}
 
 
-def compensation_cost(mp, Q, K, V, cfg, flush, stream, steps, quant_on_ms, pre_on_ms):
+def compensation_cost(mp, cfg, Q, K, V, flush, stream, steps, quant_on_ms, pre_on_ms):
     """Quantize and prefill times with the rank-one compensation off and with
-    one term, against the timed step's (compensation on, T=2)."""
-    def timed(compensate, T):
-        z = mp.quantize_qkv(Q, K, V, compensate=compensate, T=T)
-        ws = z["_workspace"]
-        o, lse = mp.prefill(z, causal=cfg.causal)
-        for _ in range(3):
-            flush.zero_()
-            z = mp.quantize_qkv(Q, K, V, compensate=compensate, T=T, workspace=ws)
-            mp.prefill(z, causal=cfg.causal, out=o, lse=lse)
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
-               for _ in range(max(steps, 1))]
-        for ev in evs:
-            flush.zero_()
-            ev[0].record(stream)
-            z = mp.quantize_qkv(Q, K, V, compensate=compensate, T=T, workspace=ws)
-            ev[1].record(stream)
-            mp.prefill(z, causal=cfg.causal, out=o, lse=lse)
-            ev[2].record(stream)
-        torch.cuda.synchronize()
-        return (statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
-                statistics.mean(e[1].elapsed_time(e[2]) for e in evs))
-    q_off, p_off = timed(False, 2)
-    q_1, p_1 = timed(True, 1)
-    return {"quantize_ms_off": q_off, "prefill_ms_off": p_off,
+    one term, against the timed step's (compensation on, two terms)."""
+    _, q_off, p_off = time_prefill(mp, cfg, Q, K, V, flush, stream, steps, 2, compensate=False)
+    _, q_1, p_1 = time_prefill(mp, cfg, Q, K, V, flush, stream, steps, 2, compensate=True, T=1)
+    return {"steps": steps, "quantize_ms_off": q_off, "prefill_ms_off": p_off,
             "quantize_ms_T1": q_1, "prefill_ms_T1": p_1,
             "quantize_ms_T2": quant_on_ms, "prefill_ms_T2": pre_on_ms,
             "prefill_overhead_pct_T1": 100.0 * (p_1 / p_off - 1.0),
@@ -499,14 +532,14 @@ def compensation_cost(mp, Q, K, V, cfg, flush, stream, steps, quant_on_ms, pre_o
             "step_overhead_pct_T2": 100.0 * ((quant_on_ms + pre_on_ms) / (q_off + p_off) - 1.0)}
 
 
-def run_decode(mp, dev, stream, peaks, flush, args):
-    cfg = DECODE_CFG
+def run_decode(mp, dev, stream, peaks, flush, args, cfg):
     if args.decode_batch:
         cfg = mi.custom_decode(args.decode_batch, cfg.Hq, cfg.Hkv, cfg.Lmax, cfg.len_lo,
                                cfg.len_hi, name=f"{cfg.name}_b{args.decode_batch}")
     q, K, V, seqlens = mi.decode_inputs(cfg, dev, seed=1)
     cache = mp.quantize_qkv(None, K, V)
     del K, V
+    torch.cuda.empty_cache()
     res = mp.decode(q, cache, seqlens)
     ws_d = res["_workspace"]
     out, lse = res["o"], res["lse"]
@@ -525,46 +558,54 @@ def run_decode(mp, dev, stream, peaks, flush, args):
         evs[i][1].record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
+    if mp.get_error() != 0:
+        raise RuntimeError(f"device status word set while timing {cfg.name}")
     ms_local = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     tokens = int(seqlens.long().sum().item())
     nbytes = tokens * cfg.Hkv * KV_BYTES_PER_TOKEN
     gbs = nbytes / (ms_local * 1e-3) / 1e9          # this replica's kernel rate (roofline)
     job, ms = aggregate_rate(nbytes, ms_local, _dist()[0], dev)
     del cache
-    return {"workload": cfg.name, "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "L": cfg.Lmax,
+    torch.cuda.empty_cache()
+    return {"workload": cfg.name, "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "Lmax": cfg.Lmax,
+            "lengths": [cfg.len_lo, cfg.len_hi], "cached_tokens": tokens,
             "value": job / 1e9, "unit": "GB/s", "ms": ms, "chunk": res["chunk"],
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm"],
-                         "traffic": measured_traffic("split_kernel") if not args.decode_batch else None,
+                         "traffic": (measured_traffic("split_kernel", cfg.name)
+                                     if not args.decode_batch else None),
                          "traffic_unit": "bytes per launch (ncu dram read + write)",
                          "algorithmic_bytes": nbytes, "kernel": "split_kernel"},
             "gpu_launches": 4 * n, "clocks": clk}
 
 
-def run_e2e(mp, dev, stream, Q, K, V, args):
+def run_e2e(mp, dev, stream, cfg, Q, K, V, n):
     """Same step through the public API with pinned host buffers: every step
     copies its bf16 Q/K/V from the host, quantizes, runs the prefill and
-    copies its O back to the host, all inside the timed region.  The copies
-    run on two copy streams with two device buffer sets, so the upload of
-    step i+1 and the download of step i-1 overlap the compute of step i."""
-    cfg = PREFILL_CFG
+    copies its O and LSE back to the host, all inside the timed region.  The
+    copies run on two copy streams with two device buffer sets, so the upload
+    of step i+1 and the download of step i-1 overlap the compute of step i."""
     hq = torch.empty(Q.shape, dtype=Q.dtype, pin_memory=True)
     hk = torch.empty(K.shape, dtype=K.dtype, pin_memory=True)
     hv = torch.empty(V.shape, dtype=V.dtype, pin_memory=True)
     hq.copy_(Q)
     hk.copy_(K)
     hv.copy_(V)
+    B, N, Hq = cfg.B, cfg.N, cfg.Hq
     ho = [torch.empty(Q.shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
+    hl = [torch.empty(B, Hq, N, dtype=torch.float32, pin_memory=True) for _ in range(2)]
     dq = [torch.empty_like(Q) for _ in range(2)]
     dk = [torch.empty_like(K) for _ in range(2)]
     dv = [torch.empty_like(V) for _ in range(2)]
     o = [torch.empty_like(Q) for _ in range(2)]
+    lse = [torch.empty(B, Hq, N, dtype=torch.float32, device=dev) for _ in range(2)]
     up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = lambda: torch.cuda.Event()  # noqa: E731
     in_ready = [ev(), ev()]      # inputs of buffer b uploaded
     in_free = [None, None]       # quantize of buffer b done (inputs consumed)
     out_ready = [ev(), ev()]     # O of buffer b computed
     out_free = [None, None]      # O of buffer b downloaded
+    ws_q = [None, None]
 
     def step(i):
         b = i & 1
@@ -578,15 +619,17 @@ def run_e2e(mp, dev, stream, Q, K, V, args):
         stream.wait_event(in_ready[b])
         if out_free[b] is not None:
             stream.wait_event(out_free[b])
-        z = mp.quantize_qkv(dq[b], dk[b], dv[b], compensate=True, T=2)
+        z = mp.quantize_qkv(dq[b], dk[b], dv[b], compensate=True, T=T_TERMS, workspace=ws_q[b])
+        ws_q[b] = z["_workspace"]
         e = ev()
         e.record(stream)
         in_free[b] = e
-        mp.prefill(z, causal=cfg.causal, out=o[b], want_lse=False)
+        mp.prefill(z, causal=cfg.causal, out=o[b], lse=lse[b])
         out_ready[b].record(stream)
         with torch.cuda.stream(down):
             down.wait_event(out_ready[b])
             ho[b].copy_(o[b], non_blocking=True)
+            hl[b].copy_(lse[b], non_blocking=True)
             f = ev()
             f.record(down)
             out_free[b] = f
@@ -594,7 +637,6 @@ def run_e2e(mp, dev, stream, Q, K, V, args):
     for i in range(2):
         step(i)
     torch.cuda.synchronize()
-    n = max(args.steps, 3)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -605,22 +647,27 @@ def run_e2e(mp, dev, stream, Q, K, V, args):
     stream.wait_event(out_free[n & 1])
     t1.record(stream)
     torch.cuda.synchronize()
-    ws = _dist()[0]
+    wsz = _dist()[0]
     flops = FLOP_PER_PAIR * cfg.pairs
-    rate, ms = aggregate_rate(flops, t0.elapsed_time(t1) / n, ws, dev)
+    rate, ms = aggregate_rate(flops, t0.elapsed_time(t1) / n, wsz, dev)
     h2d = (Q.numel() + K.numel() + V.numel()) * 2
-    return {"value": rate / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": Q.numel() * 2,
+    d2h = Q.numel() * 2 + B * Hq * N * 4
+    return {"value": rate / 1e12, "unit": "TFLOP/s", "ms_per_step": ms, "steps": n,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "pipelining": "two buffer sets; H2D of step i+1 and D2H of step i-1 overlap step i"}
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(mi.PREFILL),
+                    help="prefill workload of the timed step (default: the 128K headline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the other prefill workloads")
     ap.add_argument("--only", choices=["prefill", "decode"], default=None,
                     help="profiling aid: time only this part (no e2e / cpu baseline)")
     ap.add_argument("--decode-batch", type=int, default=None,

@@ -35,7 +35,10 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
 class MpfaError(RuntimeError):
     def __init__(self, status: int, where: str):
         name = _lib.mpfa_status_string(status).decode()
-        super().__init__(f"{where}: {name} ({status})")
+        extra = ""
+        if status == ERR_CUDA:
+            extra = f" [{_lib.mpfa_last_cuda_error().decode()}]"
+        super().__init__(f"{where}: {name} ({status}){extra}")
         self.status = status
 
 
@@ -57,6 +60,8 @@ _I = ctypes.c_int
 _SZ = ctypes.c_size_t
 _lib.mpfa_status_string.restype = ctypes.c_char_p
 _lib.mpfa_status_string.argtypes = [_I]
+_lib.mpfa_last_cuda_error.restype = ctypes.c_char_p
+_lib.mpfa_last_cuda_error.argtypes = []
 _lib.mpfa_quantize_workspace_size.restype = _SZ
 _lib.mpfa_quantize_workspace_size.argtypes = [_I, _I, _I, _I]
 _lib.mpfa_quantize_qkv.restype = _I

@@ -44,11 +44,21 @@ __global__ void selftest_wait_kernel(int* err, unsigned long long limit_ns) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
 
-mpfa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MPFA_OK : MPFA_ERR_CUDA; }
+// The last CUDA runtime error this library met on the calling host thread
+// (reported by mpfa_last_cuda_error).
+thread_local cudaError_t g_last_cuda = cudaSuccess;
+
+mpfa_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return MPFA_OK;
+  g_last_cuda = e;
+  return MPFA_ERR_CUDA;
+}
 
 }  // namespace
 
 extern "C" {
+
+const char* mpfa_last_cuda_error(void) { return cudaGetErrorName(g_last_cuda); }
 
 const char* mpfa_status_string(mpfa_status s) {
   switch (s) {
@@ -296,7 +306,7 @@ mpfa_status mpfa_selftest_wait_timeout(unsigned long long limit_ns, mpfa_stream_
 
 mpfa_status mpfa_get_error(mpfa_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return MPFA_ERR_CUDA;
+  if (e != cudaSuccess) return from_cuda(e);
   int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return MPFA_ERR_CUDA;
   if (v != 0) {

@@ -53,10 +53,14 @@ __device__ __forceinline__ uint32_t e4m3_pos(float t) {
 // at +-448, the sign kept (the signed hardware conversion matched |y| plus
 // the copied sign bit on every binary32 input except NaN).
 __device__ __forceinline__ uint32_t e4m3x4(float a0, float a1, float a2, float a3) {
-  uint16_t lo, hi;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(a1), "f"(a0));
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(a3), "f"(a2));
-  return (uint32_t)lo | ((uint32_t)hi << 16);
+  uint32_t r;
+  asm("{\n.reg .b16 lo, hi;\n"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n"
+      "mov.b32 %0, {lo, hi};\n}"
+      : "=r"(r)
+      : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+  return r;
 }
 
 // Value of an E4M3 code (exact).
@@ -160,9 +164,13 @@ __device__ __forceinline__ bool mbar_wait_loop(uint32_t bar, uint32_t parity, in
   }
 }
 
+// The phase is first tested without blocking: a potentially suspending
+// try_wait costs its thread some hundreds of cycles even when the phase has
+// already completed (measured in the prefill kernel), the test a few.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err,
                                           volatile int* abort,
                                           unsigned long long limit_ns = kWaitLimitNs) {
+  if (mbar_test_wait(bar, parity)) return true;
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_loop(bar, parity, err, abort, limit_ns);
 }
@@ -174,6 +182,28 @@ __device__ __forceinline__ bool mbar_wait_tf(uint32_t bar, uint32_t parity, int*
                                              unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_test_wait(bar, parity)) return true;
   return mbar_wait_loop(bar, parity, err, abort, limit_ns);
+}
+
+// Bounded wait that never suspends the thread: polls the phase with the
+// non-blocking test (a suspended thread is resumed only some hundreds of
+// cycles after the phase completes).  For waits on a latency-critical
+// hand-over; the bounds are those of mbar_wait.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, int* err,
+                                               volatile int* abort,
+                                               unsigned long long limit_ns = kWaitLimitNs) {
+  if (mbar_test_wait(bar, parity)) return true;
+  unsigned long long t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_test_wait(bar, parity)) return true;
+    if (abort && *abort) return false;
+    if (globaltimer() - t0 > limit_ns) {
+      record_error(err, kErrTimeout);
+      if (abort) *abort = 1;
+      return false;
+    }
+  }
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -323,6 +353,47 @@ __device__ __forceinline__ void mma_fp8_ss(uint32_t d, uint64_t a, uint64_t b, u
       : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// the same single-thread tcgen05 operations for a warp that runs its issue
+// loop converged: every lane computes the (warp-uniform) operands, one lane
+// elected inside the instruction block issues the operation
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void mma_nvfp4_ss_w(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                               uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p, e;\nelect.sync _|e, 0xffffffff;\nsetp.ne.b32 p, %4, 0;\n"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_fp8_ts_w(uint32_t d, uint32_t a_tmem, uint64_t b,
+                                             uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p, e;\nelect.sync _|e, 0xffffffff;\nsetp.ne.b32 p, %4, 0;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_cp_32x128b_x4_w(uint32_t taddr, uint64_t sdesc) {
+  asm volatile(
+      "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n}" ::"r"(taddr),
+      "l"(sdesc)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_w(uint32_t bar) {
+  asm volatile(
+      "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(
+          bar)
+      : "memory");
+}
+
 // Copy 32 rows x 16 bytes from shared memory into 4 TMEM columns of every
 // 32-lane quarter (the block-scale operand layout of the tensor core).
 __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
@@ -385,6 +456,14 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
       "r"(r[15])
       : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
+                   taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+               "r"(r[7])
+               : "memory");
 }
 
 __device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&r)[4]) {

@@ -361,11 +361,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(bar(kBarQFull0 + (k & 1)), (k >> 1) & 1, a.err, nullptr);
     }
   } else if (warp == kWarpMma || warp == kWarpMma2) {
-    // ---------------- QK issuers ----------------
-    // One thread per score bank, each issuing every other tile of the stream
+    // ---------------- QK issuers (whole warps, converged) ----------------
+    // One warp per score bank, each issuing every other tile of the stream
     // with its own K scale slot: each accumulator and slot has a single
-    // issuing thread, and neither thread's tiles wait behind the other's.
-    if (lane == 0) {
+    // issuing warp, and neither warp's tiles wait behind the other's.  Every
+    // lane computes the warp-uniform operands; one lane, elected inside each
+    // tcgen05 instruction block, issues it.
+    {
+      const uint32_t tmem_w = __shfl_sync(0xffffffffu, tmem, 0);
+      auto mbar_wait_w = [&](uint32_t b, uint32_t parity, volatile int* ab) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(b, parity, a.err, ab));
+      };
       const int par = warp == kWarpMma ? 0 : 1;
       const uint32_t id_qk = idesc_nvfp4(128, 128);
       // shared-memory descriptors built once: the start address sits in the
@@ -378,36 +384,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       // QK_g (and the rank-one MMAs) into score bank g % 2, Q from buffer buf
       auto issue_qk = [&](int g, int buf) -> bool {
         const int s = g % kKStages, bk = g & 1;
-        if (!mbar_wait(bar(kBarKFull0 + s), (g / kKStages) & 1, a.err, abort_flag)) return false;
+        if (!mbar_wait_w(bar(kBarKFull0 + s), (g / kKStages) & 1, abort_flag)) return false;
         tc_fence_after();
         // K_g's scales into this issuer's slot; its last reader, QK_{g-2},
         // completed before the softmax loaded S_{g-2} (waited for)
-        const uint32_t sfk = tmem + col_sf_k(bk);
+        const uint32_t sfk = tmem_w + col_sf_k(bk);
         for (int kc = 0; kc < 2; ++kc)
-          tmem_cp_32x128b_x4(sfk + 4 * kc,
+          tmem_cp_32x128b_x4_w(sfk + 4 * kc,
                              smem_desc(sbase + kOffKs + 1024 * s + 512 * kc, 128, 128, kSwizzleNone));
-        const uint32_t dS = tmem + kColS0 + 128 * bk;
+        const uint32_t dS = tmem_w + kColS0 + 128 * bk;
         const uint64_t dk = dk0 + 512u * (uint32_t)s;
         const uint64_t dq = dq0 + 512u * (uint32_t)buf, dqb = dqb0 + 1024u * (uint32_t)buf;
-        mma_nvfp4_ss(dS, dq, dk, id_qk, tmem + kColSfQ, sfk, 0u);
-        mma_nvfp4_ss(dS, dq + 2u, dk + 2u, id_qk, tmem + kColSfQ + 4, sfk + 4, 1u);
+        mma_nvfp4_ss_w(dS, dq, dk, id_qk, tmem_w + kColSfQ, sfk, 0u);
+        mma_nvfp4_ss_w(dS, dq + 2u, dk + 2u, id_qk, tmem_w + kColSfQ + 4, sfk + 4, 1u);
         if (T > 0) {
-          mma_nvfp4_ss(dS, dqb, dk, id_qk, tmem + kColSfQb, sfk, 1u);
-          mma_nvfp4_ss(dS, dqb + 2u, dk + 2u, id_qk, tmem + kColSfQb + 4, sfk + 4, 1u);
+          mma_nvfp4_ss_w(dS, dqb, dk, id_qk, tmem_w + kColSfQb, sfk, 1u);
+          mma_nvfp4_ss_w(dS, dqb + 2u, dk + 2u, id_qk, tmem_w + kColSfQb + 4, sfk + 4, 1u);
         }
         if (T > 1) {
-          mma_nvfp4_ss(dS, dqb + 512u, dk, id_qk, tmem + kColSfQb + 8, sfk, 1u);
-          mma_nvfp4_ss(dS, dqb + 514u, dk + 2u, id_qk, tmem + kColSfQb + 12, sfk + 4, 1u);
+          mma_nvfp4_ss_w(dS, dqb + 512u, dk, id_qk, tmem_w + kColSfQb + 8, sfk, 1u);
+          mma_nvfp4_ss_w(dS, dqb + 514u, dk + 2u, id_qk, tmem_w + kColSfQb + 12, sfk + 4, 1u);
         }
-        tc_commit(bar(kBarSFull0 + bk));
+        tc_commit_w(bar(kBarSFull0 + bk));
         return true;
       };
       // the softmax has loaded S_{g-2}: bank g % 2 and slot g % 2 are free.
       // SRead for stage (g-2) % 4 cannot be a phase further on: that needs
       // S_{g+2}.
       auto wait_sread = [&](int g) -> bool {
-        return g < 2 || mbar_wait(bar(kBarSRead0 + (g - 2) % kKStages),
-                                  ((g - 2) / kKStages) & 1, a.err, abort_flag);
+        return g < 2 || mbar_wait_w(bar(kBarSRead0 + (g - 2) % kKStages),
+                                  ((g - 2) / kKStages) & 1, abort_flag);
       };
       bool ok = true;
       int g0 = 0;
@@ -420,75 +426,79 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the TMEM Q scales of the previous item has completed: the other
           // thread's QK_{g0-1} (its bank's next commit needs these scales)
           // and this thread's QK_{g0-2} (waited for through S_{g0-2})
-          ok = mbar_wait(bar(kBarQFull0 + buf), (k >> 1) & 1, a.err, abort_flag) &&
-               (g0 < 1 || mbar_wait(bar(kBarSFull0 + ((g0 - 1) & 1)), ((g0 - 1) >> 1) & 1,
-                                    a.err, abort_flag)) &&
+          ok = mbar_wait_w(bar(kBarQFull0 + buf), (k >> 1) & 1, abort_flag) &&
+               (g0 < 1 || mbar_wait_w(bar(kBarSFull0 + ((g0 - 1) & 1)), ((g0 - 1) >> 1) & 1,
+                                      abort_flag)) &&
                wait_sread(g0);
           if (!ok) break;
           tc_fence_after();
           for (int kc = 0; kc < 2; ++kc)
-            tmem_cp_32x128b_x4(tmem + kColSfQ + 4 * kc,
+            tmem_cp_32x128b_x4_w(tmem_w + kColSfQ + 4 * kc,
                                smem_desc(sbase + kOffQs + 1024 * buf + 512 * kc, 128, 128,
                                          kSwizzleNone));
           for (int t = 0; t < T; ++t)
             for (int kc = 0; kc < 2; ++kc)
-              tmem_cp_32x128b_x4(tmem + kColSfQb + 8 * t + 4 * kc,
+              tmem_cp_32x128b_x4_w(tmem_w + kColSfQb + 8 * t + 4 * kc,
                                  smem_desc(sbase + kOffQbs + 2048 * buf + 1024 * t + 512 * kc,
                                            128, 128, kSwizzleNone));
           // also says (to the other thread) that Q and the rank-one operand
           // are in shared memory
-          tc_commit(bar(kBarQSf));
+          tc_commit_w(bar(kBarQSf));
           ok = issue_qk(g0, buf);
         } else if (n > 1) {
-          ok = mbar_wait(bar(kBarQSf), k & 1, a.err, abort_flag);
+          ok = mbar_wait_w(bar(kBarQSf), k & 1, abort_flag);
           if (ok) tc_fence_after();
         }
         for (int g = g0 + (copier ? 2 : 1); ok && g < g0 + n; g += 2) {
           if (!wait_sread(g) || !issue_qk(g, buf)) ok = false;
         }
         // this thread's products of item k done with Q buffer buf
-        tc_commit(bar(kBarQEmpty0 + buf));
+        tc_commit_w(bar(kBarQEmpty0 + buf));
         g0 += n;
       }
       // drain this thread's tensor-core work before the CTA releases TMEM
-      tc_commit(bar(kBarDrain));
-      mbar_wait(bar(kBarDrain), 0, a.err, nullptr);
+      tc_commit_w(bar(kBarDrain));
+      mbar_wait_w(bar(kBarDrain), 0, nullptr);
     }
   } else if (warp == kWarpPv) {
-    // ---------------- PV issuer ----------------
-    if (lane == 0) {
+    // ---------------- PV issuer (whole warp, converged) ----------------
+    {
+      const uint32_t tmem_w = __shfl_sync(0xffffffffu, tmem, 0);
+      auto mbar_wait_w = [&](uint32_t b, uint32_t parity, volatile int* ab) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(b, parity, a.err, ab));
+      };
       const uint32_t id_pv = idesc_fp8(128, 144, 0, 1);   // 128 V columns + 16 ones
-      bool ok = mbar_wait(bar(kBarOnes), 0, a.err, abort_flag);
+      bool ok = mbar_wait_w(bar(kBarOnes), 0, abort_flag);
       int g0 = 0;
       Item it;
       for (int k = 0; ok && item_of(p, k, it); ++k) {
         // the item's first PV overwrites O and l: the previous item's
         // epilogue must have read them out
-        if (k >= 1 && !mbar_wait(bar(kBarOFree), (k - 1) & 1, a.err, abort_flag)) break;
+        if (k >= 1 && !mbar_wait_w(bar(kBarOFree), (k - 1) & 1, abort_flag)) break;
         for (int j = 0; j < it.nkv; ++j) {
           const int g = g0 + j, bp = g & 1, sp = g % kVStages;
           // the softmax has published P_g in P bank g % 2
-          if (!mbar_wait(bar(kBarPReady0 + bp), (g >> 1) & 1, a.err, abort_flag) ||
-              !mbar_wait(bar(kBarVFull0 + sp), (g / kVStages) & 1, a.err, abort_flag)) {
+          if (!mbar_wait_w(bar(kBarPReady0 + bp), (g >> 1) & 1, abort_flag) ||
+              !mbar_wait_w(bar(kBarVFull0 + sp), (g / kVStages) & 1, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t pcol = tmem + kColP0 + 32 * bp;
+          const uint32_t pcol = tmem_w + kColP0 + 32 * bp;
           const uint32_t voff = kOffV + sp * kVStageBytes;
           // the N = 144 operand: V's 128-byte atom, then the ones atom at a
           // leading offset of kOffOnes - voff bytes (the same 32-key
           // sub-tile offset in both)
           for (int kk = 0; kk < 4; ++kk)
-            mma_fp8_ts(tmem + kColO, pcol + 8 * kk,
+            mma_fp8_ts_w(tmem_w + kColO, pcol + 8 * kk,
                        smem_desc(sbase + voff + 4096 * kk, kOffOnes - voff, 1024, kSwizzle128B),
                        id_pv, (j > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(bar(kBarODone0 + sp));
+          tc_commit_w(bar(kBarODone0 + sp));
         }
         g0 += it.nkv;
       }
-      tc_commit(bar(kBarDrain));
-      mbar_wait(bar(kBarDrain), 0, a.err, nullptr);
+      tc_commit_w(bar(kBarDrain));
+      mbar_wait_w(bar(kBarDrain), 0, nullptr);
     }
   } else {
     // ---------------- softmax / correction / epilogue ----------------
@@ -587,15 +597,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float alpha = (m == -INFINITY) ? 0.0f : (mn == m ? 1.0f : ex2(m - mn));
         const float bias = kPShift - mn;  // P8 = E4M3(2^(t - m) * 2^kPShift)
+        const float2 cs2 = make_float2(cs, cs), bias2 = make_float2(bias, bias);
         uint32_t pw[32];
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int w = 0; w < 8; ++w)
-            pw[8 * c + w] = e4m3x4(ex2(fmaf(__uint_as_float(sr[c][4 * w]), cs, bias)),
-                                   ex2(fmaf(__uint_as_float(sr[c][4 * w + 1]), cs, bias)),
-                                   ex2(fmaf(__uint_as_float(sr[c][4 * w + 2]), cs, bias)),
-                                   ex2(fmaf(__uint_as_float(sr[c][4 * w + 3]), cs, bias)));
+          for (int w = 0; w < 8; ++w) {
+            // two scores per packed fp32 FMA
+            const float2 t0 = __ffma2_rn(
+                make_float2(__uint_as_float(sr[c][4 * w]), __uint_as_float(sr[c][4 * w + 1])),
+                cs2, bias2);
+            const float2 t1 = __ffma2_rn(
+                make_float2(__uint_as_float(sr[c][4 * w + 2]), __uint_as_float(sr[c][4 * w + 3])),
+                cs2, bias2);
+            pw[8 * c + w] = e4m3x4(ex2(t0.x), ex2(t0.y), ex2(t1.x), ex2(t1.y));
+          }
         // correction: O and L scale by alpha once PV_{g-1} has landed (PV_g is
         // issued only after this tile's P is published)
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {

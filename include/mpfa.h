@@ -102,6 +102,12 @@ typedef struct {
 /* Human-readable name of a status. */
 const char *mpfa_status_string(mpfa_status s);
 
+/* Name of the last CUDA runtime error (cudaGetErrorName) behind an
+ * MPFA_ERR_CUDA returned to the calling host thread; "cudaSuccess" if there
+ * was none.  Diagnostic only: the library's own state, not the caller's CUDA
+ * error state. */
+const char *mpfa_last_cuda_error(void);
+
 /* Bytes of device workspace mpfa_quantize_qkv needs (amax words and the
  * fp32 block means of Q when compensate != 0). */
 size_t mpfa_quantize_workspace_size(int B, int Nq, int Hq, int compensate);

@@ -42,6 +42,13 @@ def test_status_strings(lib):
     assert lib.mpfa_status_string(4) == b"MPFA_ERR_TIMEOUT"
 
 
+def test_last_cuda_error_starts_clear(lib):
+    """The CUDA error behind an MPFA_ERR_CUDA is reported by name; before any
+    CUDA failure on this thread it is cudaSuccess."""
+    lib.mpfa_last_cuda_error.restype = ctypes.c_char_p
+    assert lib.mpfa_last_cuda_error() == b"cudaSuccess"
+
+
 def test_host_side_validation_without_gpu(lib):
     """Bad arguments are rejected on the host before anything is enqueued."""
     f = lib.mpfa_prefill

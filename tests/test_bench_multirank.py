@@ -57,3 +57,28 @@ def test_reference_arm_other_ranks_do_no_work(monkeypatch, capsys):
         steps, warmup, gpus = 1, 3, 2
     assert bench.run_reference(Args()) is None
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_prints_its_line_on_a_small_workload(monkeypatch, capsys):
+    """Rank 0 of the reference arm times the oracle on the selected workload
+    and prints one JSON line with the contract's keys."""
+    import json
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+
+    class Args:
+        steps, warmup, gpus, workload = 2, 1, 1, "tiny_n256"
+    bench.run_reference(Args())
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["config"]["workload"] == "tiny_n256"
+    assert line["value"] > 0 and line["unit"] == "TFLOP/s" and line["higher_is_better"]
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+
+
+def test_bench_traffic_table_is_keyed_by_kernel_and_workload():
+    """profiles/traffic.json rows are found by (kernel, workload); a workload
+    without a row gives None."""
+    assert bench.measured_traffic("prefill_kernel", "no_such_workload") is None
+    assert bench.prefill_algo_bytes(bench.mi.PREFILL["llama8b_n16k_causal"]) == 200867840
