@@ -55,6 +55,10 @@ class Rank1(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
 
 
+class KSmooth(ctypes.Structure):
+    _fields_ = [("kbar", ctypes.c_void_p), ("lse_shift", ctypes.c_void_p)]
+
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _SZ = ctypes.c_size_t
@@ -63,24 +67,25 @@ _lib.mpfa_status_string.argtypes = [_I]
 _lib.mpfa_last_cuda_error.restype = ctypes.c_char_p
 _lib.mpfa_last_cuda_error.argtypes = []
 _lib.mpfa_quantize_workspace_size.restype = _SZ
-_lib.mpfa_quantize_workspace_size.argtypes = [_I, _I, _I, _I]
+_lib.mpfa_quantize_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I, _I]
 _lib.mpfa_quantize_qkv.restype = _I
 _lib.mpfa_quantize_qkv.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                    ctypes.POINTER(NVFP4), ctypes.POINTER(Rank1),
-                                   ctypes.POINTER(NVFP4), ctypes.POINTER(FP8), _P, _SZ, _P]
+                                   ctypes.POINTER(NVFP4), ctypes.POINTER(FP8),
+                                   ctypes.POINTER(KSmooth), _P, _SZ, _P]
 _lib.mpfa_prefill.restype = _I
 _lib.mpfa_prefill.argtypes = [ctypes.POINTER(NVFP4), ctypes.POINTER(Rank1),
                               ctypes.POINTER(NVFP4), ctypes.POINTER(FP8), _I, _I, _I, _I, _I,
-                              _I, _I, _I, _P, _P, _P]
+                              _I, _I, _I, _P, _P, _P, _P]
 _lib.mpfa_decode_workspace_size.restype = _SZ
 _lib.mpfa_decode_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I]
 _lib.mpfa_decode.restype = _I
-_lib.mpfa_decode.argtypes = [_P, ctypes.POINTER(NVFP4), ctypes.POINTER(FP8), _P, _I, _I, _I, _I,
-                             _I, _I, _I, _I, _P, _P, ctypes.POINTER(NVFP4),
+_lib.mpfa_decode.argtypes = [_P, ctypes.POINTER(NVFP4), ctypes.POINTER(FP8), _P, _P, _I, _I, _I,
+                             _I, _I, _I, _I, _I, _P, _P, ctypes.POINTER(NVFP4),
                              ctypes.POINTER(Rank1), ctypes.POINTER(_I), _P, _SZ, _P]
 _lib.mpfa_append_kv.restype = _I
 _lib.mpfa_append_kv.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, ctypes.POINTER(NVFP4),
-                                ctypes.POINTER(FP8), _P]
+                                ctypes.POINTER(FP8), _P, _P]
 _lib.mpfa_get_error.restype = _I
 _lib.mpfa_get_error.argtypes = [_P]
 
@@ -119,13 +124,16 @@ def alloc_nvfp4(rows_shape, device):
                 scale=torch.empty(1, dtype=torch.float32, device=device))
 
 
-def quantize_qkv(q=None, k=None, v=None, *, compensate=True, T=2, workspace=None):
+def quantize_qkv(q=None, k=None, v=None, *, compensate=True, T=2, k_smooth=False,
+                 workspace=None):
     """Quantize bf16 q [B,Nq,Hq,128], k / v [B,Nk,Hkv,128] (any may be None).
 
     Returns a dict with ``q`` (codes [B,Hq,Nq,64], scales, scale), ``qbar``
     (codes [B,Hq,Nq/128,T,64], scales [B,Hq,Nq/128,T,8]) when compensating,
     ``k`` (codes [B,Hkv,Nk,64], scales, scale), ``v`` (codes [B,Hkv,Nk,128],
-    scale), plus the shape fields."""
+    scale), plus the shape fields.  k_smooth (needs k): key-side smoothing,
+    adding ``kbar`` (f32 [B,Hkv,128]) and, with q, ``lse_shift`` (f32
+    [B,Hq,Nq]); prefill and decode pick them up from the dict."""
     ref = next(t for t in (q, k, v) if t is not None)
     dev = ref.device
     B = ref.shape[0]
@@ -156,13 +164,23 @@ def quantize_qkv(q=None, k=None, v=None, *, compensate=True, T=2, workspace=None
         out["v"] = dict(codes=torch.empty(B, Hkv, Nk, 128, dtype=torch.uint8, device=dev),
                         scale=torch.empty(1, dtype=torch.float32, device=dev))
         vs = FP8(out["v"]["codes"].data_ptr(), out["v"]["scale"].data_ptr())
-    ws_bytes = _lib.mpfa_quantize_workspace_size(B, Nq, Hq, int(comp))
+    ksm = None
+    if k_smooth:
+        assert k is not None, "key-side smoothing needs k"
+        out["kbar"] = torch.empty(B, Hkv, D, dtype=torch.float32, device=dev)
+        if q is not None:
+            out["lse_shift"] = torch.empty(B, Hq, Nq, dtype=torch.float32, device=dev)
+        ksm = KSmooth(out["kbar"].data_ptr(),
+                      out["lse_shift"].data_ptr() if q is not None else None)
+    ws_bytes = _lib.mpfa_quantize_workspace_size(B, Nq, Nk if k is not None else 0, Hq, Hkv,
+                                                 int(comp), int(bool(k_smooth)))
     if workspace is None or workspace.numel() < ws_bytes:
         workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     st = _lib.mpfa_quantize_qkv(
         _ptr(q), _ptr(k), _ptr(v), B, Nq, Nk, Hq, Hkv, D, int(comp), int(T),
         ctypes.byref(qs) if qs is not None else None, ctypes.byref(rb) if rb is not None else None,
         ctypes.byref(ks) if ks is not None else None, ctypes.byref(vs) if vs is not None else None,
+        ctypes.byref(ksm) if ksm is not None else None,
         _ptr(workspace), workspace.numel(), _stream(dev))
     _check(st, "mpfa_quantize_qkv")
     out["_workspace"] = workspace
@@ -193,7 +211,8 @@ def prefill(qz, *, causal, out=None, lse=None, want_lse=True):
     rb = Rank1(qz["qbar"]["codes"].data_ptr(), qz["qbar"]["scales"].data_ptr()) if comp else None
     st = _lib.mpfa_prefill(ctypes.byref(qs), ctypes.byref(rb) if rb is not None else None,
                            ctypes.byref(ks), ctypes.byref(vs), B, N, Hq, Hkv, D, int(bool(causal)),
-                           int(comp), int(qz["T"]), _ptr(out), _ptr(lse), _stream(dev))
+                           int(comp), int(qz["T"]), _ptr(out), _ptr(lse),
+                           _ptr(qz.get("lse_shift")), _stream(dev))
     _check(st, "mpfa_prefill")
     return out, lse
 
@@ -205,7 +224,8 @@ def decode_workspace_bytes(B, Hq, Hkv, Lmax, kv_chunk=0) -> int:
 def decode(q, cache, seqlens, *, compensate=True, T=2, kv_chunk=0, out=None, lse=None,
            want_lse=True, return_query_codes=False, workspace=None):
     """One decode step: q bf16 [B,Hq,128] against a cache from quantize_qkv
-    (k and v given, q None), seqlens int32 [B] on the device.
+    (k and v given, q None), seqlens int32 [B] on the device.  A cache built
+    with k_smooth carries its ``kbar``, which adds the smoothing's LSE term.
     Returns dict(o, lse, chunk[, q, qbar])."""
     B, Hq, _ = q.shape
     Hkv, Lmax = cache["Hkv"], cache["Nk"]
@@ -233,7 +253,8 @@ def decode(q, cache, seqlens, *, compensate=True, T=2, kv_chunk=0, out=None, lse
                                scales=torch.empty(B, Hkv, T, 8, dtype=torch.uint8, device=dev))
             rb = Rank1(res["qbar"]["codes"].data_ptr(), res["qbar"]["scales"].data_ptr())
     used = ctypes.c_int(0)
-    st = _lib.mpfa_decode(_ptr(q), ctypes.byref(ks), ctypes.byref(vs), _ptr(seqlens), B, Hq, Hkv,
+    st = _lib.mpfa_decode(_ptr(q), ctypes.byref(ks), ctypes.byref(vs), _ptr(cache.get("kbar")),
+                          _ptr(seqlens), B, Hq, Hkv,
                           D, Lmax, int(bool(compensate)), int(T), int(kv_chunk), _ptr(out),
                           _ptr(lse), ctypes.byref(qq) if qq is not None else None,
                           ctypes.byref(rb) if rb is not None else None, ctypes.byref(used),
@@ -249,7 +270,8 @@ def append_kv(k_new, v_new, cache, seqlens):
     device, quantized with the cache's own tensor scales and written into
     the cache (from quantize_qkv(None, k, v)) at rows seqlens[b] ..
     seqlens[b] + n_new - 1 (int32 [B] on the device, not advanced: pass
-    seqlens + n_new to the next decode).  A sequence that would run past the
+    seqlens + n_new to the next decode); a cache built with k_smooth has
+    its ``kbar`` subtracted from the new keys first.  A sequence that would run past the
     cache is left as it is and get_error() then reports
     MPFA_ERR_INVALID_ARG."""
     B, n_new, Hkv, d = k_new.shape
@@ -262,7 +284,8 @@ def append_kv(k_new, v_new, cache, seqlens):
     ks = _nvfp4(cache["k"])
     vs = FP8(cache["v"]["codes"].data_ptr(), cache["v"]["scale"].data_ptr())
     st = _lib.mpfa_append_kv(_ptr(k_new), _ptr(v_new), _ptr(seqlens), B, n_new, Hkv, d,
-                             cache["Nk"], ctypes.byref(ks), ctypes.byref(vs), _stream(dev))
+                             cache["Nk"], ctypes.byref(ks), ctypes.byref(vs),
+                             _ptr(cache.get("kbar")), _stream(dev))
     _check(st, "mpfa_append_kv")
     return cache
 

@@ -71,16 +71,17 @@ const char* mpfa_status_string(mpfa_status s) {
   return "MPFA_ERR_UNKNOWN";
 }
 
-size_t mpfa_quantize_workspace_size(int B, int Nq, int Hq, int compensate) {
-  if (B < 0 || Nq < 0 || Hq < 0) return 0;
-  return mpfa::quant_workspace_bytes(B, Nq, Hq, compensate);
+size_t mpfa_quantize_workspace_size(int B, int Nq, int Nk, int Hq, int Hkv, int compensate,
+                                    int ksmooth) {
+  if (B < 0 || Nq < 0 || Nk < 0 || Hq < 0 || Hkv < 0) return 0;
+  return mpfa::quant_workspace_bytes(B, Nq, Nk, Hq, Hkv, compensate, ksmooth);
 }
 
 mpfa_status mpfa_quantize_qkv(const void* q_bf16, const void* k_bf16, const void* v_bf16, int B,
                               int Nq, int Nk, int Hq, int Hkv, int d, int compensate, int T,
                               mpfa_nvfp4* q_out, mpfa_rank1* qbar_out, mpfa_nvfp4* k_out,
-                              mpfa_fp8* v_out, void* workspace, size_t ws_bytes,
-                              mpfa_stream_t stream) {
+                              mpfa_fp8* v_out, const mpfa_ksmooth* ksmooth, void* workspace,
+                              size_t ws_bytes, mpfa_stream_t stream) {
   if (d != 128) return MPFA_ERR_UNSUPPORTED;
   if (B <= 0) return MPFA_ERR_INVALID_ARG;
   if (!q_bf16 && !k_bf16 && !v_bf16) return MPFA_ERR_INVALID_ARG;
@@ -136,12 +137,26 @@ mpfa_status mpfa_quantize_qkv(const void* q_bf16, const void* k_bf16, const void
   if ((q_bf16 && (uint64_t)B * Hq * Nq >= (1ull << 31)) ||
       ((k_bf16 || v_bf16) && (uint64_t)B * Hkv * Nk >= (1ull << 31)))
     return MPFA_ERR_INVALID_ARG;
-  if (!ok_ptr(workspace) ||
-      ws_bytes < mpfa::quant_workspace_bytes(B, q_bf16 ? Nq : 0, Hq, a.compensate))
-    return MPFA_ERR_INVALID_ARG;
-  a.amax = static_cast<unsigned*>(workspace);
-  a.qbar = a.compensate ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 256)
-                        : nullptr;
+  if (ksmooth) {
+    // key-side smoothing needs the keys, and the LSE term needs the queries
+    if (!k_bf16 || !ok_ptr(ksmooth->kbar) || (ksmooth->lse_shift && !q_bf16) ||
+        (q_bf16 && Hq % Hkv))
+      return MPFA_ERR_INVALID_ARG;
+    a.ksmooth = 1;
+    a.kbar = ksmooth->kbar;
+    a.lse_shift = q_bf16 ? ksmooth->lse_shift : nullptr;
+  }
+  const size_t need = mpfa::quant_workspace_bytes(B, q_bf16 ? Nq : 0, k_bf16 ? Nk : 0, Hq, Hkv,
+                                                  a.compensate, a.ksmooth);
+  if (!ok_ptr(workspace) || ws_bytes < need) return MPFA_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.amax = reinterpret_cast<unsigned*>(ws);
+  size_t off = 256;
+  if (a.compensate) {
+    a.qbar = reinterpret_cast<float*>(ws + off);
+    off += (size_t)B * Hq * (Nq / 128) * 128 * sizeof(float);
+  }
+  if (a.ksmooth) a.kstat = reinterpret_cast<float*>(ws + off);
   a.err = status_ptr();
   if (!a.err) return MPFA_ERR_CUDA;
   return from_cuda(mpfa::launch_quantize(a, reinterpret_cast<cudaStream_t>(stream)));
@@ -150,7 +165,7 @@ mpfa_status mpfa_quantize_qkv(const void* q_bf16, const void* k_bf16, const void
 mpfa_status mpfa_prefill(const mpfa_nvfp4* q, const mpfa_rank1* qbar, const mpfa_nvfp4* k,
                          const mpfa_fp8* v, int B, int N, int Hq, int Hkv, int d, int causal,
                          int compensate, int T, void* o_bf16, float* lse,
-                         mpfa_stream_t stream) {
+                         const float* lse_shift, mpfa_stream_t stream) {
   if (d != 128) return MPFA_ERR_UNSUPPORTED;
   if (compensate && T != 1 && T != 2) return MPFA_ERR_UNSUPPORTED;
   if (!q || !k || !v || B <= 0 || N <= 0 || N % 128 || Hq <= 0 || Hkv <= 0 || Hq % Hkv)
@@ -183,6 +198,7 @@ mpfa_status mpfa_prefill(const mpfa_nvfp4* q, const mpfa_rank1* qbar, const mpfa
   a.T = compensate ? T : 0;
   a.o = o_bf16;
   a.lse = lse;
+  a.lse_shift = lse_shift;
   a.err = status_ptr();
   if (!a.err) return MPFA_ERR_CUDA;
   return from_cuda(mpfa::launch_prefill(a, reinterpret_cast<cudaStream_t>(stream)));
@@ -198,7 +214,7 @@ size_t mpfa_decode_workspace_size(int B, int Hq, int Hkv, int d, int Lmax, int k
 }
 
 mpfa_status mpfa_decode(const void* q_bf16, const mpfa_nvfp4* k_cache, const mpfa_fp8* v_cache,
-                        const int32_t* seqlens, int B, int Hq, int Hkv, int d, int Lmax,
+                        const float* kbar, const int32_t* seqlens, int B, int Hq, int Hkv, int d, int Lmax,
                         int compensate, int T, int kv_chunk, void* o_bf16, float* lse,
                         mpfa_nvfp4* q_quant_out, mpfa_rank1* qbar_quant_out, int* used_chunk,
                         void* workspace, size_t ws_bytes, mpfa_stream_t stream) {
@@ -226,6 +242,7 @@ mpfa_status mpfa_decode(const void* q_bf16, const mpfa_nvfp4* k_cache, const mpf
   a.vc = v_cache->codes;
   a.s_v = v_cache->tensor_scale;
   a.seqlens = seqlens;
+  a.kbar = kbar;
   a.B = B;
   a.Hq = Hq;
   a.Hkv = Hkv;
@@ -252,6 +269,7 @@ mpfa_status mpfa_decode(const void* q_bf16, const mpfa_nvfp4* k_cache, const mpf
   a.qbar = reinterpret_cast<float*>(take((size_t)B * Hkv * 128 * sizeof(float)));
   a.part_o = reinterpret_cast<float*>(take((size_t)B * Hq * nsplit * 128 * sizeof(float)));
   a.part_lse = reinterpret_cast<float*>(take((size_t)B * Hq * nsplit * sizeof(float)));
+  a.q_kbar = reinterpret_cast<float*>(take((size_t)B * (Hq + Hkv) * sizeof(float)));
   const bool qout = q_quant_out && q_quant_out->codes && q_quant_out->scales &&
                     q_quant_out->tensor_scale;
   a.qc = qout ? q_quant_out->codes : qc_ws;
@@ -268,7 +286,7 @@ mpfa_status mpfa_decode(const void* q_bf16, const mpfa_nvfp4* k_cache, const mpf
 
 mpfa_status mpfa_append_kv(const void* k_new_bf16, const void* v_new_bf16, const int32_t* seqlens,
                            int B, int n_new, int Hkv, int d, int Lmax, mpfa_nvfp4* k_cache,
-                           mpfa_fp8* v_cache, mpfa_stream_t stream) {
+                           mpfa_fp8* v_cache, const float* kbar, mpfa_stream_t stream) {
   if (d != 128) return MPFA_ERR_UNSUPPORTED;
   if (!ok_ptr(k_new_bf16) || !ok_ptr(v_new_bf16) || !seqlens || !k_cache || !v_cache ||
       B <= 0 || n_new <= 0 || Hkv <= 0 || Lmax <= 0 || Lmax % 128 || n_new > Lmax)
@@ -291,6 +309,7 @@ mpfa_status mpfa_append_kv(const void* k_new_bf16, const void* v_new_bf16, const
   a.s_k = k_cache->tensor_scale;
   a.vc = v_cache->codes;
   a.s_v = v_cache->tensor_scale;
+  a.kbar = kbar;
   a.err = status_ptr();
   if (!a.err) return MPFA_ERR_CUDA;
   return from_cuda(mpfa::launch_append(a, reinterpret_cast<cudaStream_t>(stream)));

@@ -140,7 +140,21 @@ __global__ void __launch_bounds__(128) dq_stats_kernel(DecodeArgs a) {
   }
 }
 
+// sum_i e2m1(code_i) * w_i over the 16 codes of one NVFP4 block (fp32)
+__device__ __forceinline__ float codes_dot(const uint2& codes, const float* w) {
+  const uint32_t cw[2] = {codes.x, codes.y};
+  float acc = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    acc = __fmaf_rn(e2m1_value((cw[i >> 3] >> (4 * (i & 7))) & 15u), w[i], acc);
+  return acc;
+}
+
 // 8 threads per row: rows [0, B*Hq) are query rows, then B*Hkv mean rows.
+// With a smoothed cache (kbar) each row also gets its code-unit dot product
+// with kbar: sum over its blocks of block scale * sum e2m1(code) * kbar
+// (a mean row: over its T terms), which combine_kernel turns into the LSE
+// term q_eff . kbar / sqrt(d).
 __global__ void __launch_bounds__(128) dq_quant_kernel(DecodeArgs a) {
   const int g = a.Hq / a.Hkv;
   const float s = tensor_scale(a.amax[0], 2688.0f);
@@ -149,6 +163,7 @@ __global__ void __launch_bounds__(128) dq_quant_kernel(DecodeArgs a) {
   const int row = gt >> 3, j = gt & 7;
   const int nq = a.B * a.Hq;
   const int nb = a.compensate ? a.B * a.Hkv : 0;
+  float part = 0.0f;
   if (row < nq) {
     const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(a.q) + (size_t)row * 128 + 16 * j;
     float x[16];
@@ -164,6 +179,7 @@ __global__ void __launch_bounds__(128) dq_quant_kernel(DecodeArgs a) {
     nvfp4_block(x, s, codes, sb);
     *reinterpret_cast<uint2*>(a.qc + (size_t)row * 64 + 8 * j) = codes;
     a.qs[(size_t)row * 8 + j] = (uint8_t)sb;
+    if (a.kbar) part = e4m3_value(sb) * codes_dot(codes, a.kbar + (size_t)(row / g) * 128 + 16 * j);
   } else if (row < nq + nb) {
     const int r = row - nq;
     float x[16];
@@ -176,6 +192,7 @@ __global__ void __launch_bounds__(128) dq_quant_kernel(DecodeArgs a) {
       *reinterpret_cast<uint2*>(a.qbc + ((size_t)r * a.T + t) * 64 + 8 * j) = codes;
       a.qbs[((size_t)r * a.T + t) * 8 + j] = (uint8_t)sb;
       const float sbv = e4m3_value(sb);
+      if (a.kbar) part = __fmaf_rn(sbv, codes_dot(codes, a.kbar + (size_t)r * 128 + 16 * j), part);
       uint32_t w[2] = {codes.x, codes.y};
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -183,6 +200,13 @@ __global__ void __launch_bounds__(128) dq_quant_kernel(DecodeArgs a) {
         x[i] = __fsub_rn(x[i], __fmul_rn(__fmul_rn(e2m1_value(cc), sbv), s));
       }
     }
+  }
+  if (a.kbar) {
+    // the 8 threads of a row are 8 consecutive lanes
+    part += __shfl_xor_sync(0xffffffffu, part, 1);
+    part += __shfl_xor_sync(0xffffffffu, part, 2);
+    part += __shfl_xor_sync(0xffffffffu, part, 4);
+    if (j == 0 && row < nq + nb) a.q_kbar[row] = part;
   }
 }
 
@@ -198,8 +222,13 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int split = blockIdx.x % a.nsplit;
-  const int bk = blockIdx.x / a.nsplit;  // b * Hkv + kv head
+  // split-major order: every unit's first split is dispatched before any
+  // second split, and so on, so the shorter tail splits of variable-length
+  // sequences (and the empty splits past a sequence's end) come last and
+  // fill in behind the full ones instead of extending the kernel's tail
+  const int units = a.B * a.Hkv;
+  const int split = blockIdx.x / units;
+  const int bk = blockIdx.x % units;  // b * Hkv + kv head
   const int b = bk / a.Hkv;
   const int g = a.Hq / a.Hkv;
   const int T = a.compensate ? a.T : 0;
@@ -587,7 +616,18 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
   }
   const float o = wsum > 0.0f ? acc / wsum : 0.0f;
   reinterpret_cast<__nv_bfloat16*>(a.o)[row * 128 + c] = __float2bfloat16_rn(o);
-  if (a.lse && c == 0) a.lse[row] = wsum > 0.0f ? lmax + __logf(wsum) : -INFINITY;
+  if (a.lse && c == 0) {
+    float lse = wsum > 0.0f ? lmax + __logf(wsum) : -INFINITY;
+    if (a.kbar && wsum > 0.0f) {
+      // key-side smoothing: the dropped logit part s_q * (q codes + the
+      // group's rank-one terms) . kbar / sqrt(d)
+      const int g = a.Hq / a.Hkv;
+      float dq = a.q_kbar[row];
+      if (a.compensate) dq += a.q_kbar[(size_t)a.B * a.Hq + row / g];
+      lse += __fmul_rn(__fmul_rn(dq, *a.s_q), 0.08838834764831845f);
+    }
+    a.lse[row] = lse;
+  }
 }
 
 }  // namespace
@@ -646,7 +686,7 @@ size_t decode_workspace_bytes(int B, int Hq, int Hkv, int nsplit) {
   return r(256) + r(256) + r((size_t)B * Hq * 64) + r((size_t)B * Hq * 8) +
          r((size_t)B * Hkv * 2 * 64) + r((size_t)B * Hkv * 2 * 8) +
          r((size_t)B * Hkv * 128 * 4) + r((size_t)B * Hq * nsplit * 128 * 4) +
-         r((size_t)B * Hq * nsplit * 4);
+         r((size_t)B * Hq * nsplit * 4) + r((size_t)B * (Hq + Hkv) * 4);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {

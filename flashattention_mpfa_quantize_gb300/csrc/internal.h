@@ -39,13 +39,19 @@ struct QuantArgs {
   float* s_k;
   uint8_t* vc;
   float* s_v;
+  // K-side smoothing (ksmooth != 0): the keys' channel means and the LSE
+  // term of every query row
+  int ksmooth;
+  float* kbar;       // [B][Hkv][128] (output)
+  float* lse_shift;  // [B][Hq][Nq] (output; null when q is null)
   // workspace
-  unsigned* amax;  // [3] fp32 bit patterns of amax(Q or Q'/qbar), amax(K), amax(V)
+  unsigned* amax;  // [3] fp32 bit patterns of amax(Q or Q'/qbar), amax(K or K'), amax(V)
   float* qbar;     // [B][Hq][Nq/128][128] fp32 block means (compensate only)
+  float* kstat;    // [B][Hkv][Nk/128][3][128]: block mean, max, min of K (ksmooth only)
   int* err;
 };
 
-size_t quant_workspace_bytes(int B, int Nq, int Hq, int compensate);
+size_t quant_workspace_bytes(int B, int Nq, int Nk, int Hq, int Hkv, int compensate, int ksmooth);
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream);
 
 // Quantize-on-append into a decode cache: new rows of K and V, quantized with
@@ -59,6 +65,7 @@ struct AppendArgs {
   const float* s_k;
   uint8_t* vc;
   const float* s_v;
+  const float* kbar;  // [B][Hkv][128] channel means of a smoothed cache, or null
   int* err;
 };
 
@@ -75,6 +82,7 @@ struct PrefillArgs {
   int B, N, Hq, Hkv, causal, compensate, T;
   void* o;     // bf16 [B][N][Hq][128]
   float* lse;  // [B][Hq][N] or null
+  const float* lse_shift;  // [B][Hq][N] added to the LSE (K-side smoothing), or null
   int* err;
 };
 
@@ -87,6 +95,7 @@ struct DecodeArgs {
   const uint8_t* vc;
   const float* s_v;
   const int32_t* seqlens;
+  const float* kbar;  // [B][Hkv][128] channel means of a smoothed cache, or null
   int B, Hq, Hkv, Lmax, compensate, T, chunk, nsplit;
   void* o;     // bf16 [B][Hq][128]
   float* lse;  // [B][Hq] or null
@@ -98,6 +107,7 @@ struct DecodeArgs {
   float* qbar;         // [B][Hkv][128]
   float* part_o;       // [B][Hq][nsplit][128]
   float* part_lse;     // [B][Hq][nsplit]
+  float* q_kbar;       // [B][Hq + Hkv]: code-unit dot products with kbar (kbar only)
   int* err;
 };
 

@@ -21,7 +21,8 @@
 //   warp 8    TMA producer (whole warp): per item the Q tile and scales into
 //             one of two Q buffers, the rank-one operand tile built by all 32
 //             lanes; K / K-scale tiles through kKStages stages and V tiles
-//             through kVStages stages.
+//             through kVStages stages, each ring refilled as soon as its own
+//             stage frees up (polled, so a late V stage never holds back K).
 //   warps 9, 11  QK issuers, one per score bank (warp 9 the even tiles of
 //             the stream, warp 11 the odd ones), each with its own TMEM slot
 //             for K's block scales: tcgen05.cp of the scales, QK^T and the
@@ -188,21 +189,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarQFull0 + b2), 2);    // TMA arrive.expect_tx + rank-one operand built
       mbar_init(bar(kBarQEmpty0 + b2), 2);   // one commit from each QK issuer
       mbar_init(bar(kBarSFull0 + b2), 1);
-      mbar_init(bar(kBarPReady0 + b2), kTileThreads);
+      // softmax-side barriers count warps: each warp arrives once, from one
+      // lane, after a __syncwarp that orders its lanes' stores before it
+      mbar_init(bar(kBarPReady0 + b2), kTileThreads / 32);
     }
     mbar_init(bar(kBarQSf), 1);
     mbar_init(bar(kBarOnes), kSoftmaxThreads);
-    mbar_init(bar(kBarOFree), kTileThreads);
+    mbar_init(bar(kBarOFree), kTileThreads / 32);
     mbar_init(bar(kBarDrain), 3);   // one commit from each issuing thread
     for (int s = 0; s < kKStages; ++s) {
-      mbar_init(bar(kBarSRead0 + s), kTileThreads);
+      mbar_init(bar(kBarSRead0 + s), kTileThreads / 32);
       mbar_init(bar(kBarKFull0 + s), 1);
     }
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(bar(kBarVFull0 + s), 1);
       mbar_init(bar(kBarODone0 + s), 1);
     }
-    for (int i = 0; i < 8; ++i) mbar_init(bar(kBarMax0 + i), 32);
+    for (int i = 0; i < 8; ++i) mbar_init(bar(kBarMax0 + i), 1);
     fence_barrier_init();
   }
   if (warp == kWarpMma) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -299,19 +302,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       lok = lok && item_of(p, 0, it0) && load_q(0, it0);
     }
     if (lok) q_issued = 1;
-    auto load_k = [&](int g) -> bool {
-      while (g >= ck.g0 + ck.n) {   // the K cursor enters the next item: its Q first
-        const int g0n = ck.g0 + ck.n;
-        if (!enter(ck, ck.k + 1)) return false;
-        ck.g0 = g0n;
-        Item it;
-        item_of(p, ck.k, it);
-        if (!load_q(ck.k, it)) return false;
-        q_issued = ck.k + 1;
-      }
+    // lane 0's test of a phase, the same answer in every lane
+    auto test_all = [&](int b2, uint32_t parity) -> bool {
+      return __shfl_sync(0xffffffffu, mbar_test_wait(bar(b2), parity) ? 1 : 0, 0) != 0;
+    };
+    auto issue_k = [&](int g) {
       const int s = g % kKStages;
-      // stage s held K_{g-4}: free once the softmax has loaded S_{g-4}
-      if (g >= kKStages && !wait_all(kBarSRead0 + s, ((g / kKStages) - 1) & 1)) return false;
       if (lane == 0) {
         const int row = ck.row0 + (g - ck.g0) * 128;
         mbar_expect_tx(bar(kBarKFull0 + s), 8192 + 1024);
@@ -319,24 +315,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_load(sbase + kOffKs + s * 1024, a.ks + (size_t)row * 8, 1024, bar(kBarKFull0 + s));
       }
       k_issued = g + 1;
-      return true;
     };
-    auto load_v = [&](int g) -> bool {
-      while (g >= cv.g0 + cv.n) {
-        const int g0n = cv.g0 + cv.n;
-        if (!enter(cv, cv.k + 1)) return false;
-        cv.g0 = g0n;
-      }
+    auto issue_v = [&](int g) {
       const int s = g % kVStages;
-      // stage s held V_{g-3}: free once PV_{g-3} has completed
-      if (g >= kVStages && !wait_all(kBarODone0 + s, ((g / kVStages) - 1) & 1)) return false;
       if (lane == 0) {
         mbar_expect_tx(bar(kBarVFull0 + s), 16384);
         tma_load_2d(sbase + kOffV + s * kVStageBytes, &map_v, 0, cv.row0 + (g - cv.g0) * 128,
                     bar(kBarVFull0 + s));
       }
       v_issued = g + 1;
-      return true;
     };
     // total tiles of this CTA's stream
     int gtot = 0;
@@ -344,12 +331,75 @@ __global__ void __launch_bounds__(kThreads, 1)
       Item it;
       for (int k = 0; item_of(p, k, it); ++k) gtot += it.nkv;
     }
-    // loads in the order the MMA warps consume them: K_0, K_1, then V_g and
-    // K_{g+2} for g = 0, 1, ...
-    if (lok) lok = load_k(0) && (gtot < 2 || load_k(1));
-    for (int g = 0; lok && g < gtot; ++g) {
-      if (!load_v(g)) break;
-      if (g + 2 < gtot && !load_k(g + 2)) break;
+    // K and V tiles are loaded as soon as their own stages free up, polled
+    // without blocking, so neither ring waits behind the other: K stage
+    // g % 4 held K_{g-4} (free once the softmax has loaded S_{g-4}), V stage
+    // g % 3 held V_{g-3} (free once PV_{g-3} has completed); an item's Q
+    // goes into its buffer before the item's first K tile, once both QK
+    // issuers are done with the item two back.  Idle polls sleep briefly;
+    // the polling gives up (timeout) when nothing has moved for the wait
+    // limit.
+    int gk = 0, gv = 0;
+    unsigned long long idle_since = 0;
+    unsigned spins = 0;
+    while (lok && (gk < gtot || gv < gtot)) {
+      bool did = false;
+      if (gk < gtot) {
+        if (gk >= ck.g0 + ck.n) {
+          // the K cursor enters the next item: its Q first
+          const int kn = ck.k + 1;
+          if (kn < 2 || test_all(kBarQEmpty0 + (kn & 1), ((kn - 2) >> 1) & 1)) {
+            const int g0n = ck.g0 + ck.n;
+            Item it;
+            if (!enter(ck, kn) || !item_of(p, kn, it)) {
+              lok = false;
+              break;
+            }
+            ck.g0 = g0n;
+            if (!load_q(kn, it)) {
+              lok = false;
+              break;
+            }
+            q_issued = kn + 1;
+            did = true;
+          }
+        } else if (gk < kKStages ||
+                   test_all(kBarSRead0 + gk % kKStages, ((gk / kKStages) - 1) & 1)) {
+          issue_k(gk);
+          ++gk;
+          did = true;
+        }
+      }
+      if (gv < gtot) {
+        if (gv >= cv.g0 + cv.n) {
+          const int g0n = cv.g0 + cv.n;
+          if (!enter(cv, cv.k + 1)) {
+            lok = false;
+            break;
+          }
+          cv.g0 = g0n;
+        }
+        if (gv < kVStages || test_all(kBarODone0 + gv % kVStages, ((gv / kVStages) - 1) & 1)) {
+          issue_v(gv);
+          ++gv;
+          did = true;
+        }
+      }
+      if (did) {
+        idle_since = 0;
+        continue;
+      }
+      if (*abort_flag) break;
+      if (idle_since == 0) {
+        idle_since = globaltimer();
+      } else if ((++spins & 63u) == 0 && globaltimer() - idle_since > kWaitLimitNs) {
+        if (lane == 0) {
+          record_error(a.err, kErrTimeout);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      __nanosleep(40);
     }
     // drain: every buffer's last load must have landed before the CTA exits
     if (lane == 0) {
@@ -550,7 +600,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         // S_g is in registers: bank g % 2 and K stage g % 4 may be reused
         tc_fence_before();
-        mbar_arrive(bar(kBarSRead0 + g % kKStages));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarSRead0 + g % kKStages));
         if (a.causal && j == qt) {  // diagonal tile: key > row is masked
 #pragma unroll
           for (int c = 0; c < 4; ++c)
@@ -593,7 +644,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mn = (m == -INFINITY || tmax > m + kRescaleTau) ? tmax : m;
         if (g + 1 < gtot) {
           mrow[row] = mn;
-          mbar_arrive(bar_out);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_out);
         }
         const float alpha = (m == -INFINITY) ? 0.0f : (mn == m ? 1.0f : ex2(m - mn));
         const float bias = kPShift - mn;  // P8 = E4M3(2^(t - m) * 2^kPShift)
@@ -649,7 +701,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st32(tmem + lane_off + kColP0 + 32 * bk, pw);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar(kBarPReady0 + bk));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarPReady0 + bk));
         m = mn;
       }
       if (!ok) break;
@@ -672,7 +725,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_off + kColO + 32 * c, o[c]);
         tmem_ld_wait();
         tc_fence_before();
-        mbar_arrive(bar(kBarOFree));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarOFree));
         const float l = __uint_as_float(l4[0]);
         const float sc = __fdiv_rn(*a.s_v, l);
         const int h = it.bh % a.Hq, b = it.bh / a.Hq;
@@ -711,9 +765,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_store_2d(&map_o, sbase + ost + 16384u, 256 * h + 128, y);
           bulk_commit_group();
         }
-        if (a.lse)
-          a.lse[(size_t)it.bh * a.N + grow] =
-              0.69314718055994531f * (m + __log2f(l) - kPShift);
+        if (a.lse) {
+          // natural-log LSE of the scaled logits; with key-side smoothing
+          // plus the row's dropped logit part q_eff . kbar / sqrt(d)
+          const size_t li = (size_t)it.bh * a.N + grow;
+          const float lse = 0.69314718055994531f * (m + __log2f(l) - kPShift);
+          a.lse[li] = a.lse_shift ? lse + a.lse_shift[li] : lse;
+        }
       }
       g0 += nkv;
     }

@@ -159,6 +159,173 @@ __device__ void amax_bf16(const uint4* p, size_t n8, int b0, int nblk, unsigned*
 // pass 1
 // ---------------------------------------------------------------------------
 
+// Exact fp32 means of the 128-row blocks of one (b, h) of a bf16 tensor
+// x [B][N][H][128], persistent over the B*H*N/128 blocks (this CTA: blocks
+// bid, bid + nblocks, ...), the next block's rows loaded while the current
+// one is reduced.  Queries (kKeys false): the block means into out
+// [B][H][N/128][128] and max(|qbar|, |x - qbar|) into *amax_out.  Keys
+// (kKeys true): per block its means, column maxima and column minima into
+// out [block][3][128] (the key-side smoothing's statistics).
+template <bool kKeys>
+__device__ __forceinline__ void block_stats(const __nv_bfloat16* x, int B, int N, int H, int bid,
+                                            int nblocks, float* out, unsigned* amax_out,
+                                            unsigned* red, float (*xpose)[32][33]) {
+  // Warp w owns columns
+  // 16w..16w+15 of the unit for all 128 rows (lane: 16-byte column group
+  // 2w + (lane & 1), rows lane/2 + 16k), so every column reduction stays
+  // inside the warp.
+  //
+  // Each column sum is exact, in two fp32 sums.  With E the largest
+  // biased exponent of the column (at least 1) and u = 2^(E - 143) (the
+  // bf16 spacing 9 binades below the largest value), every x splits
+  // exactly into hi = x rounded to a multiple of u (adding and subtracting
+  // C = 1.5 * 2^23 * u) and lo = x - hi, |lo| <= u / 2.  Any partial sum
+  // of the his is a multiple of u below 2^24 u, and, when no nonzero value
+  // lies more than 26 binades below E, any partial sum of the los is a
+  // multiple of 2^(E - 160) below 2^24 times that: both are exact in fp32
+  // in any order, and one fp32 addition rounds hi + lo correctly.  The
+  // mean is that sum times 2^-7 (computed in fp64 if it is subnormal).  A
+  // column with a wider spread, or with E > 247, takes an fp64 path with a
+  // compensation term instead.  max |x - qbar| over a column is reached at
+  // its largest or smallest x, since fp32(x - qbar) is monotonic in x.
+  const int nblk = N / 128;
+  const int units = B * H * nblk;
+  const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cg = 2 * wid + (lane & 1);      // 16-byte column group (8 columns)
+  const int rr = lane >> 1;                 // row within each group of 16
+  auto load_unit = [&](int unit, uint4 (&w)[8]) {
+    const int blk = unit % nblk, bh = unit / nblk;
+    const int h = bh % H, b = bh / H;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const size_t n = (size_t)blk * 128 + rr + 16 * k;
+      w[k] = __ldg(reinterpret_cast<const uint4*>(
+          x + (((size_t)b * N + n) * H + h) * 128 + 8 * cg));
+    }
+  };
+  auto word = [](const uint4& v, int j) -> uint32_t {
+    return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+  };
+  float (*xp)[33] = xpose[wid];
+  unsigned m = 0;
+  uint4 wn[8];
+  if (bid < units) load_unit(bid, wn);
+  for (int unit = bid; unit < units; unit += nblocks) {
+    uint4 w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w[k] = wn[k];
+    if (unit + nblocks < units) load_unit(unit + nblocks, wn);
+    const int blk = unit % nblk, bh = unit / nblk;
+    const int h = bh % H, b = bh / H;
+    // column max |x| and min (|x| - 1) (zero -> 0xFFFF) on bf16 bit
+    // patterns, two columns per 32-bit word, over the 16 lanes of the
+    // column group
+    float C[8];
+    bool bad[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t mx = 0, mn = 0xFFFFFFFFu;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t mag = word(w[k], j) & 0x7FFF7FFFu;
+        mx = __vmaxu2(mx, mag);
+        mn = __vminu2(mn, __vsub2(mag, 0x00010001u));
+      }
+#pragma unroll
+      for (int o = 2; o < 32; o <<= 1) {
+        mx = __vmaxu2(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        mn = __vminu2(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const uint32_t cmx = e ? mx >> 16 : mx & 0xFFFFu, cmn = e ? mn >> 16 : mn & 0xFFFFu;
+        const int E = max((int)(cmx >> 7), 1);
+        const int Emin = max((int)((cmn + 1) >> 7), 1);
+        bad[2 * j + e] = E > 247 || (cmn != 0xFFFFu && Emin < E - 26);
+        C[2 * j + e] = bad[2 * j + e] ? 0.0f : __uint_as_float(((uint32_t)(E + 7) << 23) | 0x400000u);
+      }
+    }
+    // per column: the two sums and the extremes over the lane's 8 rows,
+    // stored as lane-major partials [lane][quantity * 8 + column]
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      float s0 = 0.0f, s1 = 0.0f, xmx = -INFINITY, xmn = INFINITY;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t wv = word(w[k], t >> 1);
+        const float x = __uint_as_float((t & 1) ? (wv & 0xFFFF0000u) : (wv << 16));
+        const float hi = __fsub_rn(__fadd_rn(x, C[t]), C[t]);
+        s0 = __fadd_rn(s0, hi);
+        s1 = __fadd_rn(s1, __fsub_rn(x, hi));
+        xmx = fmaxf(xmx, x);
+        xmn = fminf(xmn, x);
+      }
+      xp[lane][t] = s0;
+      xp[lane][8 + t] = s1;
+      xp[lane][16 + t] = xmx;
+      xp[lane][24 + t] = xmn;
+    }
+    __syncwarp();
+    // lane L < 16 finishes column group 2w + (L & 1), column t = L >> 1:
+    // sums and extremes over the 16 lanes of that group
+    float s0 = 0.0f, s1 = 0.0f, xmx = -INFINITY, xmn = INFINITY;
+    const int gsel = lane & 1, tc = (lane >> 1) & 7;
+    if (lane < 16) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float* row = xp[2 * i + gsel];
+        s0 = __fadd_rn(s0, row[tc]);
+        s1 = __fadd_rn(s1, row[8 + tc]);
+        xmx = fmaxf(xmx, row[16 + tc]);
+        xmn = fminf(xmn, row[24 + tc]);
+      }
+    }
+    __syncwarp();   // xpose is rewritten by the next unit
+    // the column's flag (lane L belongs to column group 2w + (L & 1) itself)
+    bool cbad = false;
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+      if (t == tc) cbad = bad[t];
+    if (lane < 16) {
+      const int c = 8 * (2 * wid + gsel) + tc;
+      float mean;
+      if (!cbad) {
+        mean = __fmul_rn(__fadd_rn(s0, s1), 0.0078125f);
+        if (mean != 0.0f && fabsf(mean) < 1.17549435e-38f)
+          mean = __double2float_rn(((double)s0 + (double)s1) * 0.0078125);
+      } else {
+        // fp64 sum with a compensation term (same rounding as a correctly
+        // rounded sum whenever the correction captures the error)
+        double sd = 0.0, comp = 0.0;
+        for (int r = 0; r < 128; ++r) {
+          const double v = (double)__bfloat162float(
+              x[(((size_t)b * N + (size_t)blk * 128 + r) * H + h) * 128 + c]);
+          const double t2 = sd + v;
+          comp += (fabs(sd) >= fabs(v)) ? ((sd - t2) + v) : ((v - t2) + sd);
+          sd = t2;
+        }
+        mean = (float)((sd + comp) * (1.0 / 128.0));
+      }
+      if (kKeys) {
+        float* st = out + (size_t)unit * 384;
+        st[c] = mean;
+        st[128 + c] = xmx;
+        st[256 + c] = xmn;
+      } else {
+        out[((size_t)bh * nblk + blk) * 128 + c] = mean;
+        m = max(m, __float_as_uint(fabsf(mean)));
+        m = max(m, __float_as_uint(fabsf(__fsub_rn(xmx, mean))));
+        m = max(m, __float_as_uint(fabsf(__fsub_rn(xmn, mean))));
+      }
+    }
+  }
+  if (!kKeys) {
+    m = block_max_u32(m, red);
+    if (threadIdx.x == 0 && m) atomicMax(amax_out, m);
+  }
+}
+
+
 __global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm)
     stats_kernel(QuantArgs a, int nq_blocks, int nk_blocks, int nv_blocks) {
   __shared__ unsigned red[kStatsThreads / 32];
@@ -171,156 +338,19 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm)
       amax_bf16(reinterpret_cast<const uint4*>(a.q), n8, 0, nq_blocks, &a.amax[0], red);
       return;
     }
-    // Persistent over the (b, h, 128-row block) units, the next unit's rows
-    // loaded while the current one is reduced.  Warp w owns columns
-    // 16w..16w+15 of the unit for all 128 rows (lane: 16-byte column group
-    // 2w + (lane & 1), rows lane/2 + 16k), so every column reduction stays
-    // inside the warp.
-    //
-    // Each column sum is exact, in two fp32 sums.  With E the largest
-    // biased exponent of the column (at least 1) and u = 2^(E - 143) (the
-    // bf16 spacing 9 binades below the largest value), every x splits
-    // exactly into hi = x rounded to a multiple of u (adding and subtracting
-    // C = 1.5 * 2^23 * u) and lo = x - hi, |lo| <= u / 2.  Any partial sum
-    // of the his is a multiple of u below 2^24 u, and, when no nonzero value
-    // lies more than 26 binades below E, any partial sum of the los is a
-    // multiple of 2^(E - 160) below 2^24 times that: both are exact in fp32
-    // in any order, and one fp32 addition rounds hi + lo correctly.  The
-    // mean is that sum times 2^-7 (computed in fp64 if it is subnormal).  A
-    // column with a wider spread, or with E > 247, takes an fp64 path with a
-    // compensation term instead.  max |x - qbar| over a column is reached at
-    // its largest or smallest x, since fp32(x - qbar) is monotonic in x.
-    const int nblk = a.Nq / 128;
-    const int units = a.B * a.Hq * nblk;
-    const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int cg = 2 * wid + (lane & 1);      // 16-byte column group (8 columns)
-    const int rr = lane >> 1;                 // row within each group of 16
-    const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(a.q);
-    auto load_unit = [&](int unit, uint4 (&w)[8]) {
-      const int blk = unit % nblk, bh = unit / nblk;
-      const int h = bh % a.Hq, b = bh / a.Hq;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const size_t n = (size_t)blk * 128 + rr + 16 * k;
-        w[k] = __ldg(reinterpret_cast<const uint4*>(
-            q + (((size_t)b * a.Nq + n) * a.Hq + h) * 128 + 8 * cg));
-      }
-    };
-    auto word = [](const uint4& v, int j) -> uint32_t {
-      return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
-    };
-    float (*xp)[33] = xpose[wid];
-    unsigned m = 0;
-    uint4 wn[8];
-    if (bid < units) load_unit(bid, wn);
-    for (int unit = bid; unit < units; unit += nq_blocks) {
-      uint4 w[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) w[k] = wn[k];
-      if (unit + nq_blocks < units) load_unit(unit + nq_blocks, wn);
-      const int blk = unit % nblk, bh = unit / nblk;
-      const int h = bh % a.Hq, b = bh / a.Hq;
-      // column max |x| and min (|x| - 1) (zero -> 0xFFFF) on bf16 bit
-      // patterns, two columns per 32-bit word, over the 16 lanes of the
-      // column group
-      float C[8];
-      bool bad[8];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t mx = 0, mn = 0xFFFFFFFFu;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t mag = word(w[k], j) & 0x7FFF7FFFu;
-          mx = __vmaxu2(mx, mag);
-          mn = __vminu2(mn, __vsub2(mag, 0x00010001u));
-        }
-#pragma unroll
-        for (int o = 2; o < 32; o <<= 1) {
-          mx = __vmaxu2(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-          mn = __vminu2(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-        }
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const uint32_t cmx = e ? mx >> 16 : mx & 0xFFFFu, cmn = e ? mn >> 16 : mn & 0xFFFFu;
-          const int E = max((int)(cmx >> 7), 1);
-          const int Emin = max((int)((cmn + 1) >> 7), 1);
-          bad[2 * j + e] = E > 247 || (cmn != 0xFFFFu && Emin < E - 26);
-          C[2 * j + e] = bad[2 * j + e] ? 0.0f : __uint_as_float(((uint32_t)(E + 7) << 23) | 0x400000u);
-        }
-      }
-      // per column: the two sums and the extremes over the lane's 8 rows,
-      // stored as lane-major partials [lane][quantity * 8 + column]
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        float s0 = 0.0f, s1 = 0.0f, xmx = -INFINITY, xmn = INFINITY;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t wv = word(w[k], t >> 1);
-          const float x = __uint_as_float((t & 1) ? (wv & 0xFFFF0000u) : (wv << 16));
-          const float hi = __fsub_rn(__fadd_rn(x, C[t]), C[t]);
-          s0 = __fadd_rn(s0, hi);
-          s1 = __fadd_rn(s1, __fsub_rn(x, hi));
-          xmx = fmaxf(xmx, x);
-          xmn = fminf(xmn, x);
-        }
-        xp[lane][t] = s0;
-        xp[lane][8 + t] = s1;
-        xp[lane][16 + t] = xmx;
-        xp[lane][24 + t] = xmn;
-      }
-      __syncwarp();
-      // lane L < 16 finishes column group 2w + (L & 1), column t = L >> 1:
-      // sums and extremes over the 16 lanes of that group
-      float s0 = 0.0f, s1 = 0.0f, xmx = -INFINITY, xmn = INFINITY;
-      const int gsel = lane & 1, tc = (lane >> 1) & 7;
-      if (lane < 16) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float* row = xp[2 * i + gsel];
-          s0 = __fadd_rn(s0, row[tc]);
-          s1 = __fadd_rn(s1, row[8 + tc]);
-          xmx = fmaxf(xmx, row[16 + tc]);
-          xmn = fminf(xmn, row[24 + tc]);
-        }
-      }
-      __syncwarp();   // xpose is rewritten by the next unit
-      // the column's flag (lane L belongs to column group 2w + (L & 1) itself)
-      bool cbad = false;
-#pragma unroll
-      for (int t = 0; t < 8; ++t)
-        if (t == tc) cbad = bad[t];
-      if (lane < 16) {
-        const int c = 8 * (2 * wid + gsel) + tc;
-        float mean;
-        if (!cbad) {
-          mean = __fmul_rn(__fadd_rn(s0, s1), 0.0078125f);
-          if (mean != 0.0f && fabsf(mean) < 1.17549435e-38f)
-            mean = __double2float_rn(((double)s0 + (double)s1) * 0.0078125);
-        } else {
-          // fp64 sum with a compensation term (same rounding as a correctly
-          // rounded sum whenever the correction captures the error)
-          double sd = 0.0, comp = 0.0;
-          for (int r = 0; r < 128; ++r) {
-            const double v = (double)__bfloat162float(
-                q[(((size_t)b * a.Nq + (size_t)blk * 128 + r) * a.Hq + h) * 128 + c]);
-            const double t2 = sd + v;
-            comp += (fabs(sd) >= fabs(v)) ? ((sd - t2) + v) : ((v - t2) + sd);
-            sd = t2;
-          }
-          mean = (float)((sd + comp) * (1.0 / 128.0));
-        }
-        a.qbar[((size_t)bh * nblk + blk) * 128 + c] = mean;
-        m = max(m, __float_as_uint(fabsf(mean)));
-        m = max(m, __float_as_uint(fabsf(__fsub_rn(xmx, mean))));
-        m = max(m, __float_as_uint(fabsf(__fsub_rn(xmn, mean))));
-      }
-    }
-    m = block_max_u32(m, red);
-    if (threadIdx.x == 0 && m) atomicMax(&a.amax[0], m);
+    block_stats<false>(reinterpret_cast<const __nv_bfloat16*>(a.q), a.B, a.Nq, a.Hq, bid,
+                       nq_blocks, a.qbar, &a.amax[0], red, xpose);
     return;
   }
   bid -= nq_blocks;
   if (bid < nk_blocks) {
+    if (a.ksmooth) {
+      // key-side smoothing: block statistics now, the channel means and
+      // amax(K - kbar) in kbar_kernel
+      block_stats<true>(reinterpret_cast<const __nv_bfloat16*>(a.k), a.B, a.Nk, a.Hkv, bid,
+                        nk_blocks, a.kstat, nullptr, red, xpose);
+      return;
+    }
     size_t n8 = (size_t)a.B * a.Nk * a.Hkv * 16;
     amax_bf16(reinterpret_cast<const uint4*>(a.k), n8, nq_blocks, nk_blocks, &a.amax[1], red);
     return;
@@ -330,12 +360,51 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm)
             &a.amax[2], red);
 }
 
+// Key-side smoothing: per (b, KV head) and channel, kbar = fp32(fp64 sum of
+// the block means in block order / number of blocks), and amax(K - kbar)
+// from the blocks' column extremes (fp32(x - kbar) is monotonic in x, so a
+// column's largest |x - kbar| is at its largest or smallest x).
+__global__ void __launch_bounds__(128) kbar_kernel(QuantArgs a) {
+  __shared__ unsigned red[4];
+  const int bh = blockIdx.x, c = threadIdx.x;
+  const int nblk = a.Nk / 128;
+  const float* st = a.kstat + (size_t)bh * nblk * 384;
+  double acc = 0.0;
+  float mx = -INFINITY, mn = INFINITY;
+  for (int blk = 0; blk < nblk; ++blk) {
+    acc = __dadd_rn(acc, (double)st[(size_t)blk * 384 + c]);
+    mx = fmaxf(mx, st[(size_t)blk * 384 + 128 + c]);
+    mn = fminf(mn, st[(size_t)blk * 384 + 256 + c]);
+  }
+  const float kb = __double2float_rn(__ddiv_rn(acc, (double)nblk));
+  a.kbar[(size_t)bh * 128 + c] = kb;
+  unsigned m = max(__float_as_uint(fabsf(__fsub_rn(mx, kb))),
+                   __float_as_uint(fabsf(__fsub_rn(mn, kb))));
+  m = block_max_u32(m, red);
+  if (threadIdx.x == 0 && m) atomicMax(&a.amax[1], m);
+}
+
 // ---------------------------------------------------------------------------
 // pass 2
 // ---------------------------------------------------------------------------
 
+constexpr float kInvSqrtD = 0.08838834764831845f;  // fp32(1 / sqrt(128))
+
+// sum_i e2m1(code_i) * w_i over the 16 codes of one NVFP4 block (fp32)
+__device__ __forceinline__ float codes_dot(const uint2& codes, const float (&w)[16]) {
+  const uint32_t cw[2] = {codes.x, codes.y};
+  float acc = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    acc = __fmaf_rn(e2m1_value((cw[i >> 3] >> (4 * (i & 7))) & 15u), w[i], acc);
+  return acc;
+}
+
 // blockIdx.y: 0 = Q rows, 1 = qbar terms, 2 = K rows, 3 = V elements.
-__global__ void __launch_bounds__(kThreads, 6) quant_kernel(QuantArgs a) {
+// kSmooth: the key-side smoothing variant (K' codes, the LSE term of every
+// query row), with a register budget of its own.
+template <bool kSmooth>
+__global__ void __launch_bounds__(kThreads, kSmooth ? 5 : 6) quant_kernel(QuantArgs a) {
   const int lane = threadIdx.x & 31;
   const int warps_total = gridDim.x * (kThreads / 32);
   const int gwarp = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
@@ -368,6 +437,40 @@ __global__ void __launch_bounds__(kThreads, 6) quant_kernel(QuantArgs a) {
           m[4 * t + 1] = v.y;
           m[4 * t + 2] = v.z;
           m[4 * t + 3] = v.w;
+        }
+      }
+      // key-side smoothing: the lane's 16 channels of kbar and, with the
+      // rank-one terms, their part of every row's q_eff . kbar (the terms
+      // are re-derived here as the rank-one pass codes them)
+      float kb[16];
+      float rq = 0.0f;
+      if (kSmooth && a.lse_shift) {
+        const float4* kp = reinterpret_cast<const float4*>(
+            a.kbar + (b * a.Hkv + h / (a.Hq / a.Hkv)) * 128 + 16 * j);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float4 v = kp[t];
+          kb[4 * t] = v.x;
+          kb[4 * t + 1] = v.y;
+          kb[4 * t + 2] = v.z;
+          kb[4 * t + 3] = v.w;
+        }
+        if (a.compensate) {
+          float y[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) y[i] = m[i];
+          for (int term = 0; term < a.T; ++term) {
+            uint2 codes;
+            uint32_t sb;
+            nvfp4_block(y, s, codes, sb);
+            const float sbv = e4m3_value(sb);
+            rq = __fmaf_rn(sbv, codes_dot(codes, kb), rq);
+            const uint32_t cw[2] = {codes.x, codes.y};
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              y[i] = __fsub_rn(y[i], __fmul_rn(__fmul_rn(e2m1_value((cw[i >> 3] >> (4 * (i & 7))) & 15u),
+                                                         sbv), s));
+          }
         }
       }
       // rows 8 step + ri and 8 step + 4 + ri of the block (lane group ri)
@@ -414,6 +517,14 @@ __global__ void __launch_bounds__(kThreads, 6) quant_kernel(QuantArgs a) {
           nvfp4_block(x, s, codes, sb);
           *reinterpret_cast<uint2*>(a.qc + r * 64 + 8 * j) = codes;
           store_scales_tiled(a.qs, r, j, sb);
+          if (kSmooth && a.lse_shift) {
+            // s_q * (code * block scale + rank-one terms) . kbar / sqrt(d)
+            float part = __fmaf_rn(e4m3_value(sb), codes_dot(codes, kb), rq);
+            part += __shfl_xor_sync(0xffffffffu, part, 1);
+            part += __shfl_xor_sync(0xffffffffu, part, 2);
+            part += __shfl_xor_sync(0xffffffffu, part, 4);
+            if (j == 0) a.lse_shift[r] = __fmul_rn(__fmul_rn(part, s), kInvSqrtD);
+          }
         }
       }
     }
@@ -498,6 +609,17 @@ __global__ void __launch_bounds__(kThreads, 6) quant_kernel(QuantArgs a) {
           x[2 * i + 1] = bf16_hi(w[i]);
         }
         const size_t r = 8 * u + 4 * h2 + ri;
+        if (kSmooth) {  // K' = fp32(K - kbar)
+          const float4* kp = reinterpret_cast<const float4*>(a.kbar + (r / a.Nk) * 128 + 16 * j);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const float4 v = kp[t];
+            x[4 * t] = __fsub_rn(x[4 * t], v.x);
+            x[4 * t + 1] = __fsub_rn(x[4 * t + 1], v.y);
+            x[4 * t + 2] = __fsub_rn(x[4 * t + 2], v.z);
+            x[4 * t + 3] = __fsub_rn(x[4 * t + 3], v.w);
+          }
+        }
         uint2 codes;
         uint32_t sb;
         nvfp4_block(x, s, codes, sb);
@@ -626,6 +748,11 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
         x[2 * i + 1] = bf16_hi(w[i]);
       }
     }
+    if (a.kbar) {  // a smoothed cache holds K' = fp32(K - kbar)
+      const float* kb = a.kbar + ((size_t)b * a.Hkv + h) * 128 + 16 * j;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) x[i] = __fsub_rn(x[i], kb[i]);
+    }
     uint2 codes;
     uint32_t sb;
     nvfp4_block(x, sk, codes, sb);
@@ -675,9 +802,11 @@ int num_sms() {
 
 }  // namespace
 
-size_t quant_workspace_bytes(int B, int Nq, int Hq, int compensate) {
+size_t quant_workspace_bytes(int B, int Nq, int Nk, int Hq, int Hkv, int compensate,
+                             int ksmooth) {
   size_t bytes = 256;  // amax words
   if (compensate) bytes += (size_t)B * Hq * (Nq / 128) * 128 * sizeof(float);
+  if (ksmooth) bytes += (size_t)B * Hkv * (Nk / 128) * 384 * sizeof(float);
   return bytes;
 }
 
@@ -696,15 +825,27 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
     nq = a.compensate ? (units < kStatsCtasPerSm * sms ? units : kStatsCtasPerSm * sms)  // persistent
                       : amax_blocks((size_t)a.B * a.Nq * a.Hq * 128);
   }
-  if (a.k) nk = amax_blocks((size_t)a.B * a.Nk * a.Hkv * 128);
+  if (a.k) {
+    const int units = a.B * a.Hkv * (a.Nk / 128);
+    nk = a.ksmooth ? (units < kStatsCtasPerSm * sms ? units : kStatsCtasPerSm * sms)  // persistent
+                   : amax_blocks((size_t)a.B * a.Nk * a.Hkv * 128);
+  }
   if (a.v) nv = amax_blocks((size_t)a.B * a.Nk * a.Hkv * 128);
   if (nq + nk + nv > 0) {
     stats_kernel<<<nq + nk + nv, kStatsThreads, 0, stream>>>(a, nq, nk, nv);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  if (a.k && a.ksmooth) {
+    kbar_kernel<<<a.B * a.Hkv, 128, 0, stream>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   dim3 grid(sms * 8, 4);
-  quant_kernel<<<grid, kThreads, 0, stream>>>(a);
+  if (a.ksmooth)
+    quant_kernel<true><<<grid, kThreads, 0, stream>>>(a);
+  else
+    quant_kernel<false><<<grid, kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

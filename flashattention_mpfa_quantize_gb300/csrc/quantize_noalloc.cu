@@ -52,10 +52,10 @@ extern "C" mpfa_status mpfa_quantize_qkv_noalloc(
     int Hkv, int d, int compensate, int T, mpfa_nvfp4* q_out, mpfa_rank1* qbar_out,
     mpfa_nvfp4* k_out, mpfa_fp8* v_out, mpfa_stream_t stream) {
   const int comp = (q_bf16 && compensate) ? 1 : 0;
-  const size_t need = mpfa_quantize_workspace_size(B, q_bf16 ? Nq : 0, Hq, comp);
+  const size_t need = mpfa_quantize_workspace_size(B, q_bf16 ? Nq : 0, 0, Hq, 0, comp, 0);
   if (need == 0 || need > kScratchBytes) return MPFA_ERR_INVALID_ARG;
   void* ws = scratch_address();
   if (!ws) return MPFA_ERR_CUDA;
   return mpfa_quantize_qkv(q_bf16, k_bf16, v_bf16, B, Nq, Nk, Hq, Hkv, d, compensate, T, q_out,
-                           qbar_out, k_out, v_out, ws, kScratchBytes, stream);
+                           qbar_out, k_out, v_out, nullptr, ws, kScratchBytes, stream);
 }

@@ -99,6 +99,22 @@ typedef struct {
     uint8_t *scales;
 } mpfa_rank1;
 
+/* Key-side smoothing outputs (an addition to the MpFA method, resting on the
+ * softmax's invariance to one shift of all logits of a row, the explainer's
+ * attention section).  kbar [B][Hkv][d] fp32: per (batch, KV head) and
+ * channel, the fp32 rounding of the fp64 mean (block order, sequential) of
+ * the keys' 128-row block means, each the correctly rounded fp32 mean of
+ * its block.  The keys are coded as K' = fp32(K - kbar) with s_k from
+ * amax(K').  lse_shift [B][Hq][Nq] fp32 (may be NULL): for every query row
+ * the logit part the smoothed keys leave out, q_eff . kbar / sqrt(d), where
+ * q_eff = s_q * (code * block scale of the row + the rank-one terms of its
+ * block); mpfa_prefill adds it to the LSE.  O does not depend on it.  Both
+ * device pointers, caller-owned. */
+typedef struct {
+    float *kbar;
+    float *lse_shift;
+} mpfa_ksmooth;
+
 /* Human-readable name of a status. */
 const char *mpfa_status_string(mpfa_status s);
 
@@ -108,9 +124,11 @@ const char *mpfa_status_string(mpfa_status s);
  * error state. */
 const char *mpfa_last_cuda_error(void);
 
-/* Bytes of device workspace mpfa_quantize_qkv needs (amax words and the
- * fp32 block means of Q when compensate != 0). */
-size_t mpfa_quantize_workspace_size(int B, int Nq, int Hq, int compensate);
+/* Bytes of device workspace mpfa_quantize_qkv needs (amax words, the fp32
+ * block means of Q when compensate != 0, the keys' block statistics when
+ * ksmooth != 0).  Nq = 0 / Nk = 0 for a call without queries / keys. */
+size_t mpfa_quantize_workspace_size(int B, int Nq, int Nk, int Hq, int Hkv, int compensate,
+                                    int ksmooth);
 
 /*
  * Online quantization of one attention layer's inputs (MpFA abstract: the QK
@@ -128,13 +146,15 @@ size_t mpfa_quantize_workspace_size(int B, int Nq, int Hq, int compensate);
  *   B*Hq*Nq and B*Hkv*Nk below 2^31 rows (the row index the kernels and the
  *   tensor-memory-access coordinates use is 32-bit).
  *   Tensor scales are computed over each whole tensor argument.
+ *   ksmooth: NULL, or key-side smoothing (see mpfa_ksmooth): needs k_bf16;
+ *   lse_shift, if given, needs q_bf16 and Hq % Hkv == 0.
  *   workspace: device buffer of at least mpfa_quantize_workspace_size bytes.
  */
 mpfa_status mpfa_quantize_qkv(const void *q_bf16, const void *k_bf16, const void *v_bf16,
                               int B, int Nq, int Nk, int Hq, int Hkv, int d, int compensate,
                               int T, mpfa_nvfp4 *q_out, mpfa_rank1 *qbar_out, mpfa_nvfp4 *k_out,
-                              mpfa_fp8 *v_out, void *workspace, size_t ws_bytes,
-                              mpfa_stream_t stream);
+                              mpfa_fp8 *v_out, const mpfa_ksmooth *ksmooth, void *workspace,
+                              size_t ws_bytes, mpfa_stream_t stream);
 
 /*
  * mpfa_quantize_qkv without a caller workspace.  The paper has no
@@ -144,7 +164,8 @@ mpfa_status mpfa_quantize_qkv(const void *q_bf16, const void *k_bf16, const void
  * its input and output tensors).  It allocates nothing; its scratch is a
  * fixed device array inside the library of 256 + 16 MiB bytes, which every
  * GPU that loads the library holds until the process exits.
- *   Arguments, layouts and results are those of mpfa_quantize_qkv.
+ *   Arguments, layouts and results are those of mpfa_quantize_qkv without
+ *   key-side smoothing.
  *   Limit: with compensate != 0 the block means of Q must fit, i.e.
  *   B * Hq * Nq / 128 <= 32768 query blocks; larger problems return
  *   MPFA_ERR_INVALID_ARG with nothing enqueued (use mpfa_quantize_qkv).
@@ -170,10 +191,13 @@ mpfa_status mpfa_quantize_qkv_noalloc(const void *q_bf16, const void *k_bf16,
  *   q/k/v from mpfa_quantize_qkv; qbar NULL iff compensate == 0.
  *   o_bf16 [B][N][Hq][d]; lse [B][Hq][N] natural-log sum-exp of the scaled
  *   logits (may be NULL).  N multiple of 128, Hq % Hkv == 0.
+ *   lse_shift: NULL, or mpfa_ksmooth.lse_shift of keys quantized with
+ *   key-side smoothing, added to the LSE.
  */
 mpfa_status mpfa_prefill(const mpfa_nvfp4 *q, const mpfa_rank1 *qbar, const mpfa_nvfp4 *k,
                          const mpfa_fp8 *v, int B, int N, int Hq, int Hkv, int d, int causal,
-                         int compensate, int T, void *o_bf16, float *lse, mpfa_stream_t stream);
+                         int compensate, int T, void *o_bf16, float *lse,
+                         const float *lse_shift, mpfa_stream_t stream);
 
 /* Bytes of device workspace mpfa_decode needs for kv_chunk (0 = the chunk
  * the library would choose). */
@@ -198,9 +222,12 @@ size_t mpfa_decode_workspace_size(int B, int Hq, int Hkv, int d, int Lmax, int k
  *   q_quant_out (optional, may be NULL): codes [B][Hq][64], scales
  *   [B][Hq][8] row-major, tensor scale; qbar_quant_out (optional):
  *   codes [B][Hkv][T][64], scales [B][Hkv][T][8].
+ *   kbar: NULL, or the mpfa_ksmooth.kbar [B][Hkv][d] the cache's keys were
+ *   smoothed with: the LSE then gets q_eff . kbar / sqrt(d) added (O is the
+ *   same either way).
  */
 mpfa_status mpfa_decode(const void *q_bf16, const mpfa_nvfp4 *k_cache, const mpfa_fp8 *v_cache,
-                        const int32_t *seqlens, int B, int Hq, int Hkv, int d, int Lmax,
+                        const float *kbar, const int32_t *seqlens, int B, int Hq, int Hkv, int d, int Lmax,
                         int compensate, int T, int kv_chunk, void *o_bf16, float *lse,
                         mpfa_nvfp4 *q_quant_out, mpfa_rank1 *qbar_quant_out, int *used_chunk,
                         void *workspace, size_t ws_bytes, mpfa_stream_t stream);
@@ -226,10 +253,12 @@ mpfa_status mpfa_decode(const void *q_bf16, const mpfa_nvfp4 *k_cache, const mpf
  *   cache; Lmax multiple of 128, 1 <= n_new <= Lmax, B*Hkv*Lmax below 2^31
  *   rows, d = 128 (else MPFA_ERR_UNSUPPORTED).  Host-checkable errors return
  *   MPFA_ERR_INVALID_ARG with nothing enqueued.
+ *   kbar: NULL, or the kbar of a cache built with key-side smoothing: the
+ *   new keys are then coded as fp32(K - kbar) like the cache's own rows.
  */
 mpfa_status mpfa_append_kv(const void *k_new_bf16, const void *v_new_bf16, const int32_t *seqlens,
                            int B, int n_new, int Hkv, int d, int Lmax, mpfa_nvfp4 *k_cache,
-                           mpfa_fp8 *v_cache, mpfa_stream_t stream);
+                           mpfa_fp8 *v_cache, const float *kbar, mpfa_stream_t stream);
 
 /* Failure-path self-test: enqueues a one-thread kernel that waits, with the
  * same bounded barrier wait every kernel uses, on an on-chip barrier that

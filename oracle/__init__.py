@@ -276,16 +276,48 @@ def quantize_q_prefill(Q: np.ndarray, compensate: bool, T: int = 2, nthreads: in
     return dict(qc=qc, qs=qs, qbc=qbc, qbs=qbs, s_q=s, qbar=qbar)
 
 
-def quantize_k(K: np.ndarray, nthreads: int = 0) -> dict:
-    """K [B, N, Hkv, d] -> kc [B,Hkv,N,d/2], ks [B,Hkv,N,d/16], s_k."""
+def key_channel_means(K: np.ndarray, nthreads: int = 0) -> np.ndarray:
+    """K-side smoothing vector (an addition to the pages' method, resting on
+    the softmax's invariance to a per-row shift of the logits, the
+    explainer's attention section): per (b, KV head) and channel c,
+    kbar_c = fp32(fp64(sum over the 128-key blocks, in block order, of the
+    block's fp32 mean) / number of blocks), each block mean being the
+    correctly rounded fp32 mean of its 128 keys (the rule of the query-side
+    block means).  K [B, N, Hkv, d] fp32 holding bf16 values, N a multiple
+    of 128 -> kbar [B, Hkv, d] fp32."""
     B, N, H, d = K.shape
+    assert N % QBLOCK == 0
+    kbar = np.empty((B, H, d), np.float32)
+    for b in range(B):
+        for h in range(H):
+            means, _ = block_means(np.ascontiguousarray(K[b, :, h, :]), QBLOCK, nthreads)
+            acc = np.zeros(d, np.float64)
+            for blk in range(means.shape[0]):        # sequential, in block order
+                acc = acc + means[blk].astype(np.float64)
+            kbar[b, h] = (acc / np.float64(means.shape[0])).astype(np.float32)
+    return kbar
+
+
+def quantize_k(K: np.ndarray, nthreads: int = 0, smooth: bool = False) -> dict:
+    """K [B, N, Hkv, d] -> kc [B,Hkv,N,d/2], ks [B,Hkv,N,d/16], s_k.
+
+    smooth=True (K-side smoothing): kbar = key_channel_means(K), the codes
+    are those of K' = fp32(K - kbar) with s_k from amax(K'), and kbar is
+    returned with them (the logits then lack q.kbar, the same for every key
+    of a query row, so O is unchanged and the LSE gets it back; see
+    lse_shift)."""
+    B, N, H, d = K.shape
+    kbar = None
+    if smooth:
+        kbar = key_channel_means(K, nthreads)
+        K = (np.asarray(K, np.float32) - kbar[:, None, :, :]).astype(np.float32)
     s = tensor_scale(_amax(K), NVFP4_QMAX)
     kc = np.empty((B, H, N, d // 2), np.uint8)
     ks = np.empty((B, H, N, d // 16), np.uint8)
     for b in range(B):
         for h in range(H):
             kc[b, h], ks[b, h] = nvfp4_quantize(np.ascontiguousarray(K[b, :, h, :]), s, nthreads)
-    return dict(kc=kc, ks=ks, s_k=s)
+    return dict(kc=kc, ks=ks, s_k=s, kbar=kbar)
 
 
 def quantize_v(V: np.ndarray) -> dict:
@@ -393,6 +425,35 @@ def _head_operands(qz, kz, vz, b, h, g):
     return q, qadd, k, v
 
 
+def query_effective(qz, b, h, g):
+    """The query rows the method multiplies, dequantized with the tensor
+    scale: s_q * (code * block scale of Q' (or Q) + the sum of the rank-one
+    terms of the row's block), fp64 [rows, d].  Prefill codes (qz from
+    quantize_q_prefill, rows = N) or decode codes (quantize_q_decode,
+    one row; the rank-one block is KV head h // g)."""
+    qc, qs = qz["qc"][b, h], qz["qs"][b, h]
+    if qc.ndim == 1:
+        qc, qs = qc[None], qs[None]
+    q = nvfp4_dequant(qc, qs)
+    if qz.get("qbc") is not None:
+        if qz["qbc"].ndim == 5:        # prefill: [B, Hq, blocks, T, d/2]
+            qb = _terms_sum(qz["qbc"][b, h], qz["qbs"][b, h])
+            q = q + np.repeat(qb, QBLOCK, axis=0)[: q.shape[0]]
+        else:                          # decode: [B, Hkv, T, d/2]
+            q = q + _terms_sum(qz["qbc"][b, h // g][None], qz["qbs"][b, h // g][None])
+    return q * np.float64(qz["s_q"])
+
+
+def lse_shift(qz, kz, b, h, g, d=D):
+    """K-side smoothing's LSE term of query head h of batch b: the logit
+    part q_eff . kbar / sqrt(d) that the smoothed keys leave out, the same
+    for every key of the row (fp64 [rows]); zero without smoothing."""
+    q = query_effective(qz, b, h, g)
+    if kz.get("kbar") is None:
+        return np.zeros(q.shape[0])
+    return q @ kz["kbar"][b, h // g].astype(np.float64) / math.sqrt(d)
+
+
 def prefill_emulate(qz, kz, vz, *, causal, heads=None, rows=None, nthreads=0):
     """Emulate the QK4PV8 prefill on the oracle's own codes.
 
@@ -407,8 +468,12 @@ def prefill_emulate(qz, kz, vz, *, causal, heads=None, rows=None, nthreads=0):
     out = {}
     for (b, h) in heads:
         q, qadd, k, v = _head_operands(qz, kz, vz, b, h, g)
-        out[(b, h)] = attn_online(q, qadd, k, v, score_scale=cs, out_scale=float(vz["s_v"]),
-                                  causal=causal, rows=rows, nthreads=nthreads)
+        o, lse = attn_online(q, qadd, k, v, score_scale=cs, out_scale=float(vz["s_v"]),
+                             causal=causal, rows=rows, nthreads=nthreads)
+        if kz.get("kbar") is not None:
+            sh = lse_shift(qz, kz, b, h, g)
+            lse = lse + (sh if rows is None else sh[np.asarray(rows)])
+        out[(b, h)] = (o, lse)
     return out
 
 
@@ -450,6 +515,8 @@ def decode_emulate(qz, kz, vz, seqlens, *, chunk, heads=None, nthreads=0):
         o, lse = attn_online(q, qadd, k, v, score_scale=cs, out_scale=float(vz["s_v"]),
                              causal=False, kv_len=int(seqlens[b]), chunk=chunk,
                              nthreads=nthreads)
+        if kz.get("kbar") is not None:
+            lse = lse + lse_shift(qz, kz, b, h, g)
         out[(b, h)] = (o[0], lse[0])
     return out
 

@@ -54,21 +54,23 @@ def test_host_side_validation_without_gpu(lib):
     f = lib.mpfa_prefill
     f.restype = ctypes.c_int
     # d != 128 -> unsupported; null tensors -> invalid
-    assert f(None, None, None, None, 1, 128, 1, 1, 64, 0, 0, 0, None, None, None) == 2
-    assert f(None, None, None, None, 1, 128, 1, 1, 128, 0, 0, 0, None, None, None) == 1
+    assert f(None, None, None, None, 1, 128, 1, 1, 64, 0, 0, 0, None, None, None, None) == 2
+    assert f(None, None, None, None, 1, 128, 1, 1, 128, 0, 0, 0, None, None, None, None) == 1
     q = lib.mpfa_quantize_qkv
     q.restype = ctypes.c_int
-    assert q(None, None, None, 1, 128, 128, 1, 1, 128, 0, 2, None, None, None, None, None, 0,
-             None) == 1
-    assert q(None, None, None, 1, 128, 128, 1, 1, 96, 0, 2, None, None, None, None, None, 0,
-             None) == 2
+    assert q(None, None, None, 1, 128, 128, 1, 1, 128, 0, 2, None, None, None, None, None, None,
+             0, None) == 1
+    assert q(None, None, None, 1, 128, 128, 1, 1, 96, 0, 2, None, None, None, None, None, None,
+             0, None) == 2
 
 
 def test_workspace_size_queries(lib):
     lib.mpfa_quantize_workspace_size.restype = ctypes.c_size_t
-    n0 = lib.mpfa_quantize_workspace_size(1, 256, 2, 0)
-    n1 = lib.mpfa_quantize_workspace_size(1, 256, 2, 1)
-    assert n1 - n0 == 2 * 2 * 128 * 4
+    n0 = lib.mpfa_quantize_workspace_size(1, 256, 384, 2, 1, 0, 0)
+    n1 = lib.mpfa_quantize_workspace_size(1, 256, 384, 2, 1, 1, 0)
+    n2 = lib.mpfa_quantize_workspace_size(1, 256, 384, 2, 1, 1, 1)
+    assert n1 - n0 == 2 * 2 * 128 * 4                  # Q block means
+    assert n2 - n1 == 1 * 3 * 3 * 128 * 4              # key block mean, max, min
 
 
 def _fake(addr):
@@ -93,38 +95,59 @@ def test_host_validation_rejects_bad_shapes_and_pointers(lib):
     f.restype = ctypes.c_int
     R = ctypes.byref
     # N not a multiple of 128
-    assert f(R(q), None, R(k), R(v), 1, 100, 4, 2, 128, 1, 0, 0, _fake(ok), None, None) == 1
+    assert f(R(q), None, R(k), R(v), 1, 100, 4, 2, 128, 1, 0, 0, _fake(ok), None, None, None) == 1
     # Hq % Hkv != 0
-    assert f(R(q), None, R(k), R(v), 1, 128, 5, 2, 128, 1, 0, 0, _fake(ok), None, None) == 1
+    assert f(R(q), None, R(k), R(v), 1, 128, 5, 2, 128, 1, 0, 0, _fake(ok), None, None,
+             None) == 1
     # misaligned output
-    assert f(R(q), None, R(k), R(v), 1, 128, 4, 2, 128, 1, 0, 0, _fake(ok + 2), None, None) == 1
+    assert f(R(q), None, R(k), R(v), 1, 128, 4, 2, 128, 1, 0, 0, _fake(ok + 2), None, None,
+             None) == 1
     # compensation without its terms, and T out of range
-    assert f(R(q), None, R(k), R(v), 1, 128, 4, 2, 128, 1, 1, 2, _fake(ok), None, None) == 1
-    assert f(R(q), None, R(k), R(v), 1, 128, 4, 2, 128, 1, 1, 3, _fake(ok), None, None) == 2
+    assert f(R(q), None, R(k), R(v), 1, 128, 4, 2, 128, 1, 1, 2, _fake(ok), None, None,
+             None) == 1
+    assert f(R(q), None, R(k), R(v), 1, 128, 4, 2, 128, 1, 1, 3, _fake(ok), None, None,
+             None) == 2
     d = lib.mpfa_decode
     d.restype = ctypes.c_int
     used = ctypes.c_int(0)
     # kv_chunk not a multiple of 128; Lmax not a multiple of 128
-    assert d(_fake(ok), R(k), R(v), _fake(ok), 2, 8, 2, 128, 256, 1, 2, 100, _fake(ok), None,
+    assert d(_fake(ok), R(k), R(v), None, _fake(ok), 2, 8, 2, 128, 256, 1, 2, 100, _fake(ok), None,
              None, None, R(used), _fake(ok), 1 << 20, None) == 1
-    assert d(_fake(ok), R(k), R(v), _fake(ok), 2, 8, 2, 128, 200, 1, 2, 0, _fake(ok), None,
+    assert d(_fake(ok), R(k), R(v), None, _fake(ok), 2, 8, 2, 128, 200, 1, 2, 0, _fake(ok), None,
              None, None, R(used), _fake(ok), 1 << 20, None) == 1
     # more than 16 query heads per KV head
-    assert d(_fake(ok), R(k), R(v), _fake(ok), 2, 64, 2, 128, 256, 1, 2, 0, _fake(ok), None,
+    assert d(_fake(ok), R(k), R(v), None, _fake(ok), 2, 64, 2, 128, 256, 1, 2, 0, _fake(ok), None,
              None, None, R(used), _fake(ok), 1 << 20, None) == 2
     # 2^31 cache rows or more (B * Hkv * Lmax)
-    assert d(_fake(ok), R(k), R(v), _fake(ok), 4096, 8, 8, 128, 1 << 16, 1, 2, 0, _fake(ok),
+    assert d(_fake(ok), R(k), R(v), None, _fake(ok), 4096, 8, 8, 128, 1 << 16, 1, 2, 0, _fake(ok),
              None, None, None, R(used), _fake(ok), ctypes.c_size_t(1 << 50), None) == 1
     # 2^31 rows or more in prefill
     assert f(R(q), None, R(k), R(v), 1024, 1 << 21, 4, 2, 128, 1, 0, 0, _fake(ok), None,
-             None) == 1
+             None, None) == 1
     # and in quantize (q rows; k/v rows)
     qq = lib.mpfa_quantize_qkv
     qq.restype = ctypes.c_int
     assert qq(_fake(ok), None, None, 1024, 1 << 21, 0, 4, 2, 128, 0, 2, R(q), None, None, None,
-              _fake(ok), ctypes.c_size_t(1 << 50), None) == 1
+              None, _fake(ok), ctypes.c_size_t(1 << 50), None) == 1
     assert qq(None, _fake(ok), _fake(ok), 1024, 0, 1 << 21, 4, 2, 128, 0, 2, None, None, R(k),
-              R(v), _fake(ok), ctypes.c_size_t(1 << 50), None) == 1
+              R(v), None, _fake(ok), ctypes.c_size_t(1 << 50), None) == 1
+
+    # key-side smoothing: needs the keys and a kbar buffer; its LSE term needs the queries
+    class KS(ctypes.Structure):
+        _fields_ = [("kbar", ctypes.c_void_p), ("lse_shift", ctypes.c_void_p)]
+
+    big = ctypes.c_size_t(1 << 40)
+    assert qq(_fake(ok), None, None, 1, 256, 256, 4, 2, 128, 0, 2, R(q), None, None, None,
+              R(KS(ok, ok)), _fake(ok), big, None) == 1
+    assert qq(None, _fake(ok), None, 1, 0, 256, 4, 2, 128, 0, 2, None, None, R(k), None,
+              R(KS(ok, ok)), _fake(ok), big, None) == 1
+    assert qq(None, _fake(ok), None, 1, 0, 256, 4, 2, 128, 0, 2, None, None, R(k), None,
+              R(KS(None, None)), _fake(ok), big, None) == 1
+    # a workspace without room for the key statistics
+    lib.mpfa_quantize_workspace_size.restype = ctypes.c_size_t
+    need = lib.mpfa_quantize_workspace_size(1, 0, 256, 4, 2, 0, 1)
+    assert qq(None, _fake(ok), None, 1, 0, 256, 4, 2, 128, 0, 2, None, None, R(k), None,
+              R(KS(ok, None)), _fake(ok), ctypes.c_size_t(need - 1), None) == 1
 
 
 def test_append_kv_host_validation(lib):
@@ -145,7 +168,7 @@ def test_append_kv_host_validation(lib):
     def call(**kw):
         x = {**args, **kw}
         return a(x["kn"], x["vn"], x["sl"], x["B"], x["n"], x["H"], x["d"], x["L"],
-                 kw.get("k", R(k)), kw.get("v", R(v)), None)
+                 kw.get("k", R(k)), kw.get("v", R(v)), None, None)
 
     assert call(d=64) == 2                      # head dim other than 128
     assert call(kn=None) == 1                   # null new K

@@ -18,6 +18,9 @@ pytestmark = pytest.mark.gpu
 
 CASES = [
     # name, config, heads, rows
+    # the tiny non-causal configuration exactly (no Q offset; K channel
+    # offsets and 4 outlier channels)
+    ("tiny_n256", mi.PREFILL["tiny_n256"], [(0, 0)], None),
     ("tiny_n256_qoffset", mi.PREFILL["tiny_n256_qoffset"], [(0, 0)], None),
     ("n2048_causal_qoffset", mi.custom_prefill(1, 8, 2, 2048, True, q_offset=True, name="n2048q"),
      [(0, 0), (0, 5)], np.arange(0, 2048, 7)),
@@ -27,11 +30,12 @@ CASES = [
 ]
 
 
-def _run(cfg, heads, rows, compensate, T):
+def _run(cfg, heads, rows, compensate, T, k_smooth=False):
     import flashattention_mpfa_quantize_gb300 as mp
     Q, K, V = mi.prefill_inputs(cfg, "cpu", 0)
     dev = torch.device("cuda:0")
-    z = mp.quantize_qkv(Q.to(dev), K.to(dev), V.to(dev), compensate=compensate, T=T)
+    z = mp.quantize_qkv(Q.to(dev), K.to(dev), V.to(dev), compensate=compensate, T=T,
+                        k_smooth=k_smooth)
     o, _ = mp.prefill(z, causal=cfg.causal)
     torch.cuda.synchronize()
     assert mp.get_error() == 0
@@ -48,14 +52,19 @@ def _run(cfg, heads, rows, compensate, T):
 @pytest.mark.parametrize("name,cfg,heads,rows", CASES, ids=[c[0] for c in CASES])
 def test_error_vs_exact(name, cfg, heads, rows):
     res = {}
-    for label, comp, T in [("off", False, 2), ("T1", True, 1), ("T2", True, 2)]:
-        got, want = _run(cfg, heads, rows, comp, T)
+    for label, comp, T, ks in [("off", False, 2, False), ("T1", True, 1, False),
+                               ("T2", True, 2, False), ("ks", False, 2, True),
+                               ("T2+ks", True, 2, True)]:
+        got, want = _run(cfg, heads, rows, comp, T, ks)
         res[label] = (rel_l2(got, want), cosine(got, want))
     red1 = (res["off"][0] - res["T1"][0]) / res["off"][0]
     red2 = (res["off"][0] - res["T2"][0]) / res["off"][0]
+    red3 = (res["off"][0] - res["T2+ks"][0]) / res["off"][0]
     print(f"\n{name}: rel-L2 / cosine vs exact: off {res['off'][0]:.4f} / {res['off'][1]:.5f}, "
-          f"T=1 {res['T1'][0]:.4f} / {res['T1'][1]:.5f}, T=2 {res['T2'][0]:.4f} / {res['T2'][1]:.5f}; "
-          f"reduction T=1 {red1:+.3f}, T=2 {red2:+.3f}")
+          f"T=1 {res['T1'][0]:.4f} / {res['T1'][1]:.5f}, T=2 {res['T2'][0]:.4f} / {res['T2'][1]:.5f}, "
+          f"K smoothing {res['ks'][0]:.4f} / {res['ks'][1]:.5f}, "
+          f"T=2 + K smoothing {res['T2+ks'][0]:.4f} / {res['T2+ks'][1]:.5f}; "
+          f"reduction T=1 {red1:+.3f}, T=2 {red2:+.3f}, T=2 + K smoothing {red3:+.3f}")
     if "plain" in name:
         for label in res:
             assert res[label][1] >= 0.99, (label, res[label])

@@ -622,3 +622,131 @@ def test_decode_compensation_exact_for_representable_group_means():
         np.testing.assert_array_equal(a[key][0], b[key][0])
         assert a[key][1] == b[key][1]
     assert not np.array_equal(a[(0, 0)][0], a[(0, g)][0])
+
+
+# --------------------------------------------------------------------------
+# K-side smoothing (an addition to the pages' method, resting on the
+# softmax's invariance to a per-row shift of the logits): kbar, K' and the
+# LSE term
+# --------------------------------------------------------------------------
+
+def _paired_blocks(rng, B, N, H, step, lim):
+    """[B, N, H, 128] values on a grid of `step` in [-lim, lim] whose every
+    128-key block of every (b, h) has exactly zero channel means (rows x and
+    -x inside each block)."""
+    half = np.clip(np.round(rng.standard_normal((B, N // 128, 64, H, 128)) * lim / 2 / step)
+                   * step, -lim, lim)
+    blocks = np.concatenate([half, -half], axis=2)           # [B, nblk, 128, H, 128]
+    return blocks.reshape(B, N, H, 128).astype(np.float32)
+
+
+def _exact_nvfp4_rows(rng, rows, s):
+    """[rows, 128] values NVFP4 represents exactly with tensor scale s (a 6 in
+    every 16-element block, the first block scale 448)."""
+    e4 = np.array([orc.e4m3_value(c) for c in range(0x30, 0x7F)])
+    vals16 = np.array([orc.e2m1_value(int(c)) for c in range(16)])
+    out = np.empty((rows, 128))
+    for r in range(rows):
+        codes = rng.integers(0, 16, 128)
+        codes[::16] = 7 + 8 * rng.integers(0, 2, 8)
+        sb = rng.choice(e4, 8)
+        sb[0] = 448.0
+        out[r] = vals16[codes] * np.repeat(sb, 16) * s
+    return out.astype(np.float32)
+
+
+def test_key_means_of_shifted_zero_mean_keys():
+    """K = K0 + c with every 128-key block of K0 at exactly zero channel
+    mean and c a per-(b, KV head) channel vector: kbar is c exactly, K' is
+    K0, so the smoothed codes, scales and s_k equal the unsmoothed ones of
+    K0.  A mean over the wrong axis, over the query heads, or a K' of
+    K + kbar breaks the equalities."""
+    rng = np.random.default_rng(201)
+    B, N, H = 2, 384, 3
+    K0 = _paired_blocks(rng, B, N, H, 0.25, 4.0)
+    c = (np.round(rng.standard_normal((B, H, 128)) * 8) / 4).clip(-8, 8).astype(np.float32)
+    K = (K0 + c[:, None]).astype(np.float32)
+    assert np.array_equal(_bf16(K), K) and np.array_equal(K - c[:, None], K0)
+    sm = orc.quantize_k(K, smooth=True)
+    ref = orc.quantize_k(K0)
+    np.testing.assert_array_equal(sm["kbar"], c)
+    assert sm["s_k"] == ref["s_k"]
+    # magnitudes: K0's -x = -0 where x = 0 codes a negative zero, K - c a positive one
+    np.testing.assert_array_equal(sm["kc"] & 0x77, ref["kc"] & 0x77)
+    np.testing.assert_array_equal(sm["ks"], ref["ks"])
+    assert orc.quantize_k(K)["kbar"] is None
+
+
+def test_key_means_are_the_mean_of_block_means():
+    """Keys constant inside each 128-key block (value v_blk per channel):
+    the block means are v_blk and kbar is their fp64 mean rounded to fp32,
+    here exact: (1 + 2 + 3 + 6) / 4 = 3 in channel 0, and a channel-dependent
+    closed form elsewhere."""
+    v = np.array([1.0, 2.0, 3.0, 6.0])
+    ch = np.arange(128) / 8.0 - 8.0                     # exact in bf16
+    K = np.empty((1, 512, 1, 128), np.float32)
+    for blk in range(4):
+        K[0, blk * 128:(blk + 1) * 128, 0, :] = v[blk] * (1.0 + 0 * ch) + ch
+    kb = orc.key_channel_means(K)[0, 0]
+    np.testing.assert_array_equal(kb, (3.0 + ch).astype(np.float32))
+
+
+def test_k_smoothing_keeps_o_and_moves_lse_by_the_dropped_logit():
+    """Exactly representable Q (so the dequantized query is Q itself) against
+    K = K0 + c: with K-side smoothing the emulated O is bit-identical to the
+    one on K0, and the LSE differs from it by exactly what fp64 attention on
+    the unquantized inputs says the shift c adds, q.c / sqrt(d) -- in
+    prefill (causal and not) and in split-KV decode."""
+    rng = np.random.default_rng(203)
+    B, N, Hq, Hkv = 1, 256, 4, 2
+    s = 2.0 ** -6
+    Q = _exact_nvfp4_rows(rng, B * N * Hq, s).reshape(B, N, Hq, 128)
+    K0 = _paired_blocks(rng, B, N, Hkv, 0.25, 4.0)
+    c = (np.round(rng.standard_normal((B, Hkv, 128)) * 8) / 4).clip(-8, 8).astype(np.float32)
+    K = (K0 + c[:, None]).astype(np.float32)
+    V = _bf16(rng.standard_normal((B, N, Hkv, 128)))
+    qz = orc.quantize_q_prefill(Q, False)
+    assert qz["s_q"] == np.float32(s)
+    np.testing.assert_array_equal(orc.query_effective(qz, 0, 1, 2), Q[0, :, 1, :])
+    kz_s, kz_0, vz = orc.quantize_k(K, smooth=True), orc.quantize_k(K0), orc.quantize_v(V)
+    for causal in (False, True):
+        a = orc.prefill_emulate(qz, kz_s, vz, causal=causal)
+        b = orc.prefill_emulate(qz, kz_0, vz, causal=causal)
+        ea = orc.prefill_exact(Q, K, V, causal=causal)
+        eb = orc.prefill_exact(Q, K0, V, causal=causal)
+        for key in a:
+            np.testing.assert_array_equal(a[key][0], b[key][0])
+            np.testing.assert_allclose(ea[key][0], eb[key][0], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(a[key][1] - b[key][1], ea[key][1] - eb[key][1],
+                                       rtol=0, atol=1e-9)
+            assert np.abs(a[key][1] - b[key][1]).max() > 0.1
+    # decode: the last query row of each head against the first L keys
+    q = Q[:, -1].copy()                                   # [B, Hq, 128]
+    qd = orc.quantize_q_decode(q, Hkv, False)
+    np.testing.assert_array_equal(orc.query_effective(qd, 0, 1, 2)[0], q[0, 1])
+    lens = np.array([200])
+    da = orc.decode_emulate(qd, kz_s, vz, lens, chunk=128)
+    db = orc.decode_emulate(qd, kz_0, vz, lens, chunk=128)
+    xa = orc.decode_exact(q, K, V, lens)
+    xb = orc.decode_exact(q, K0, V, lens)
+    for key in da:
+        np.testing.assert_array_equal(da[key][0], db[key][0])
+        assert abs((da[key][1] - db[key][1]) - (xa[key][1] - xb[key][1])) < 1e-9
+
+
+def test_k_smoothing_reduces_error_on_key_offsets():
+    """The tiny configuration (K channel offsets and four x20 outlier
+    channels): K-side smoothing lowers the emulated output's error against
+    exact fp64 attention, with and without the query-side term."""
+    import mpfa_inputs as mi
+    Q, K, V = mi.prefill_inputs(mi.PREFILL["tiny_n256"], "cpu", 0)
+    Qn, Kn, Vn = (t.float().numpy() for t in (Q, K, V))
+    ex = orc.prefill_exact(Qn, Kn, Vn, causal=False)[(0, 0)][0]
+    vz = orc.quantize_v(Vn)
+    for comp in (False, True):
+        qz = orc.quantize_q_prefill(Qn, comp)
+        e = {}
+        for sm in (False, True):
+            o = orc.prefill_emulate(qz, orc.quantize_k(Kn, smooth=sm), vz, causal=False)[(0, 0)][0]
+            e[sm] = _rel_l2(o, ex)
+        assert e[True] < 0.85 * e[False], (comp, e)
