@@ -86,6 +86,13 @@ _lib.mpfa_decode.argtypes = [_P, ctypes.POINTER(NVFP4), ctypes.POINTER(FP8), _P,
 _lib.mpfa_append_kv.restype = _I
 _lib.mpfa_append_kv.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, ctypes.POINTER(NVFP4),
                                 ctypes.POINTER(FP8), _P, _P]
+_lib.mpfa_decode_paged.restype = _I
+_lib.mpfa_decode_paged.argtypes = [_P, ctypes.POINTER(NVFP4), ctypes.POINTER(FP8), _P, _I, _I, _P,
+                                   _I, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.POINTER(NVFP4),
+                                   ctypes.POINTER(Rank1), ctypes.POINTER(_I), _P, _SZ, _P]
+_lib.mpfa_append_kv_paged.restype = _I
+_lib.mpfa_append_kv_paged.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                      ctypes.POINTER(NVFP4), ctypes.POINTER(FP8), _P]
 _lib.mpfa_get_error.restype = _I
 _lib.mpfa_get_error.argtypes = [_P]
 
@@ -300,3 +307,67 @@ def untile_scales(tiled: torch.Tensor, rows: int) -> torch.Tensor:
     j = torch.arange(8, device=tiled.device).view(1, -1)
     off = (r // 128) * 1024 + (j // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (j % 4)
     return tiled.view(-1)[off.view(-1)].view(rows, 8)
+
+
+# --------------------------------------------------------------------------
+# paged KV pool
+# --------------------------------------------------------------------------
+
+def quantize_pool(k_pages, v_pages, workspace=None):
+    """A paged pool from bf16 K / V pages [num_pages, 128, Hkv, 128]: page p
+    holds, for every KV head, 128 token rows (see include/mpfa.h)."""
+    assert k_pages.shape[1] == 128 and v_pages.shape == k_pages.shape
+    pool = quantize_qkv(None, k_pages, v_pages, workspace=workspace)
+    pool["num_pages"] = k_pages.shape[0]
+    return pool
+
+
+def decode_paged(q, pool, block_table, seqlens, *, compensate=True, T=2, kv_chunk=0, out=None,
+                 lse=None, want_lse=True, workspace=None):
+    """Split-KV decode over a paged pool: block_table int32 [B, max_pages] on
+    the device (page of each sequence's 128-token block), seqlens int32 [B].
+    Returns dict(o, lse, chunk)."""
+    B, Hq, _ = q.shape
+    Hkv, num_pages = pool["Hkv"], pool["num_pages"]
+    max_pages = block_table.shape[1]
+    dev = q.device
+    assert q.dtype == torch.bfloat16 and q.is_contiguous()
+    assert block_table.dtype == torch.int32 and block_table.is_contiguous()
+    assert block_table.shape[0] == B and block_table.device == dev
+    assert seqlens.dtype == torch.int32 and seqlens.device == dev
+    if out is None:
+        out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+    ws_bytes = decode_workspace_bytes(B, Hq, Hkv, 128 * max_pages, kv_chunk)
+    if workspace is None or workspace.numel() < ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ks = _nvfp4(pool["k"])
+    vs = FP8(pool["v"]["codes"].data_ptr(), pool["v"]["scale"].data_ptr())
+    used = ctypes.c_int(0)
+    st = _lib.mpfa_decode_paged(_ptr(q), ctypes.byref(ks), ctypes.byref(vs), _ptr(block_table),
+                                num_pages, max_pages, _ptr(seqlens), B, Hq, Hkv, D,
+                                int(bool(compensate)), int(T), int(kv_chunk), _ptr(out),
+                                _ptr(lse), None, None, ctypes.byref(used), _ptr(workspace),
+                                workspace.numel(), _stream(dev))
+    _check(st, "mpfa_decode_paged")
+    return dict(o=out, lse=lse, chunk=used.value, _workspace=workspace)
+
+
+def append_kv_paged(k_new, v_new, pool, block_table, seqlens):
+    """Quantize-on-append into a paged pool: token seqlens[b] + t of sequence
+    b goes to row (seqlens[b] + t) % 128 of page block_table[b][(...) / 128],
+    coded with the pool's own tensor scales."""
+    B, n_new, Hkv, d = k_new.shape
+    dev = k_new.device
+    for t in (k_new, v_new):
+        assert t.dtype == torch.bfloat16 and t.is_contiguous() and t.shape == (B, n_new, Hkv, D)
+    assert block_table.dtype == torch.int32 and block_table.shape[0] == B
+    assert seqlens.dtype == torch.int32 and seqlens.numel() == B
+    ks = _nvfp4(pool["k"])
+    vs = FP8(pool["v"]["codes"].data_ptr(), pool["v"]["scale"].data_ptr())
+    st = _lib.mpfa_append_kv_paged(_ptr(k_new), _ptr(v_new), _ptr(seqlens), _ptr(block_table),
+                                   pool["num_pages"], block_table.shape[1], B, n_new, Hkv, d,
+                                   ctypes.byref(ks), ctypes.byref(vs), _stream(dev))
+    _check(st, "mpfa_append_kv_paged")
+    return pool

@@ -213,11 +213,18 @@ size_t mpfa_decode_workspace_size(int B, int Hq, int Hkv, int d, int Lmax, int k
   return mpfa::decode_workspace_bytes(B, Hq, Hkv, nsplit);
 }
 
-mpfa_status mpfa_decode(const void* q_bf16, const mpfa_nvfp4* k_cache, const mpfa_fp8* v_cache,
-                        const float* kbar, const int32_t* seqlens, int B, int Hq, int Hkv, int d, int Lmax,
-                        int compensate, int T, int kv_chunk, void* o_bf16, float* lse,
-                        mpfa_nvfp4* q_quant_out, mpfa_rank1* qbar_quant_out, int* used_chunk,
-                        void* workspace, size_t ws_bytes, mpfa_stream_t stream) {
+}  // extern "C"
+
+// Shared by mpfa_decode (block_table null: contiguous [B][Hkv][Lmax] cache)
+// and mpfa_decode_paged (pool rows [num_pages][Hkv][128], Lmax = 128 * max_pages).
+static mpfa_status decode_impl(const void* q_bf16, const mpfa_nvfp4* k_cache,
+                               const mpfa_fp8* v_cache, const float* kbar,
+                               const int32_t* block_table, int num_pages, int max_pages,
+                               const int32_t* seqlens, int B, int Hq, int Hkv, int d, int Lmax,
+                               int compensate, int T, int kv_chunk, void* o_bf16, float* lse,
+                               mpfa_nvfp4* q_quant_out, mpfa_rank1* qbar_quant_out,
+                               int* used_chunk, void* workspace, size_t ws_bytes,
+                               mpfa_stream_t stream) {
   if (d != 128) return MPFA_ERR_UNSUPPORTED;
   if (compensate && T != 1 && T != 2) return MPFA_ERR_UNSUPPORTED;
   if (!ok_ptr(q_bf16) || !k_cache || !v_cache || !seqlens || B <= 0 || Hq <= 0 || Hkv <= 0 ||
@@ -227,7 +234,11 @@ mpfa_status mpfa_decode(const void* q_bf16, const mpfa_nvfp4* k_cache, const mpf
       !ok_ptr(v_cache->codes) || !v_cache->tensor_scale)
     return MPFA_ERR_INVALID_ARG;
   if (Hq / Hkv > 16) return MPFA_ERR_UNSUPPORTED;
-  if ((uint64_t)B * Hkv * Lmax >= (1ull << 31)) return MPFA_ERR_INVALID_ARG;
+  if (!block_table && (uint64_t)B * Hkv * Lmax >= (1ull << 31)) return MPFA_ERR_INVALID_ARG;
+  if (block_table && (num_pages <= 0 || max_pages <= 0 ||
+                      (uint64_t)num_pages * Hkv * 128 >= (1ull << 31) ||
+                      (uint64_t)B * max_pages >= (1ull << 31)))
+    return MPFA_ERR_INVALID_ARG;
   int sms = mpfa::sm_count(mpfa::current_device());
   if (sms <= 0) sms = 148;
   const int chunk = kv_chunk > 0 ? kv_chunk : mpfa::decode_default_chunk(B, Hkv, Lmax, sms);
@@ -243,6 +254,9 @@ mpfa_status mpfa_decode(const void* q_bf16, const mpfa_nvfp4* k_cache, const mpf
   a.s_v = v_cache->tensor_scale;
   a.seqlens = seqlens;
   a.kbar = kbar;
+  a.block_table = block_table;
+  a.num_pages = num_pages;
+  a.max_pages = max_pages;
   a.B = B;
   a.Hq = Hq;
   a.Hkv = Hkv;
@@ -284,9 +298,39 @@ mpfa_status mpfa_decode(const void* q_bf16, const mpfa_nvfp4* k_cache, const mpf
   return from_cuda(mpfa::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-mpfa_status mpfa_append_kv(const void* k_new_bf16, const void* v_new_bf16, const int32_t* seqlens,
-                           int B, int n_new, int Hkv, int d, int Lmax, mpfa_nvfp4* k_cache,
-                           mpfa_fp8* v_cache, const float* kbar, mpfa_stream_t stream) {
+extern "C" {
+
+mpfa_status mpfa_decode(const void* q_bf16, const mpfa_nvfp4* k_cache, const mpfa_fp8* v_cache,
+                        const float* kbar, const int32_t* seqlens, int B, int Hq, int Hkv, int d,
+                        int Lmax, int compensate, int T, int kv_chunk, void* o_bf16, float* lse,
+                        mpfa_nvfp4* q_quant_out, mpfa_rank1* qbar_quant_out, int* used_chunk,
+                        void* workspace, size_t ws_bytes, mpfa_stream_t stream) {
+  return decode_impl(q_bf16, k_cache, v_cache, kbar, nullptr, 0, 0, seqlens, B, Hq, Hkv, d, Lmax,
+                     compensate, T, kv_chunk, o_bf16, lse, q_quant_out, qbar_quant_out,
+                     used_chunk, workspace, ws_bytes, stream);
+}
+
+mpfa_status mpfa_decode_paged(const void* q_bf16, const mpfa_nvfp4* k_pool, const mpfa_fp8* v_pool,
+                              const int32_t* block_table, int num_pages, int max_pages,
+                              const int32_t* seqlens, int B, int Hq, int Hkv, int d,
+                              int compensate, int T, int kv_chunk, void* o_bf16, float* lse,
+                              mpfa_nvfp4* q_quant_out, mpfa_rank1* qbar_quant_out,
+                              int* used_chunk, void* workspace, size_t ws_bytes,
+                              mpfa_stream_t stream) {
+  if (!block_table) return MPFA_ERR_INVALID_ARG;
+  if (max_pages <= 0 || max_pages > (1 << 30) / 128) return MPFA_ERR_INVALID_ARG;
+  return decode_impl(q_bf16, k_pool, v_pool, nullptr, block_table, num_pages, max_pages, seqlens,
+                     B, Hq, Hkv, d, 128 * max_pages, compensate, T, kv_chunk, o_bf16, lse,
+                     q_quant_out, qbar_quant_out, used_chunk, workspace, ws_bytes, stream);
+}
+
+}  // extern "C"
+
+static mpfa_status append_impl(const void* k_new_bf16, const void* v_new_bf16,
+                               const int32_t* seqlens, const int32_t* block_table, int num_pages,
+                               int max_pages, int B, int n_new, int Hkv, int d, int Lmax,
+                               mpfa_nvfp4* k_cache, mpfa_fp8* v_cache, const float* kbar,
+                               mpfa_stream_t stream) {
   if (d != 128) return MPFA_ERR_UNSUPPORTED;
   if (!ok_ptr(k_new_bf16) || !ok_ptr(v_new_bf16) || !seqlens || !k_cache || !v_cache ||
       B <= 0 || n_new <= 0 || Hkv <= 0 || Lmax <= 0 || Lmax % 128 || n_new > Lmax)
@@ -294,7 +338,11 @@ mpfa_status mpfa_append_kv(const void* k_new_bf16, const void* v_new_bf16, const
   if (!ok_ptr(k_cache->codes) || !ok_ptr(k_cache->scales) || !k_cache->tensor_scale ||
       !ok_ptr(v_cache->codes) || !v_cache->tensor_scale)
     return MPFA_ERR_INVALID_ARG;
-  if ((uint64_t)B * Hkv * Lmax >= (1ull << 31) || (uint64_t)B * n_new * Hkv >= (1ull << 31))
+  if ((!block_table && (uint64_t)B * Hkv * Lmax >= (1ull << 31)) ||
+      (uint64_t)B * n_new * Hkv >= (1ull << 31))
+    return MPFA_ERR_INVALID_ARG;
+  if (block_table && (num_pages <= 0 || max_pages <= 0 ||
+                      (uint64_t)num_pages * Hkv * 128 >= (1ull << 31)))
     return MPFA_ERR_INVALID_ARG;
   mpfa::AppendArgs a = {};
   a.k_new = k_new_bf16;
@@ -310,9 +358,31 @@ mpfa_status mpfa_append_kv(const void* k_new_bf16, const void* v_new_bf16, const
   a.vc = v_cache->codes;
   a.s_v = v_cache->tensor_scale;
   a.kbar = kbar;
+  a.block_table = block_table;
+  a.num_pages = num_pages;
+  a.max_pages = max_pages;
   a.err = status_ptr();
   if (!a.err) return MPFA_ERR_CUDA;
   return from_cuda(mpfa::launch_append(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" {
+
+mpfa_status mpfa_append_kv(const void* k_new_bf16, const void* v_new_bf16, const int32_t* seqlens,
+                           int B, int n_new, int Hkv, int d, int Lmax, mpfa_nvfp4* k_cache,
+                           mpfa_fp8* v_cache, const float* kbar, mpfa_stream_t stream) {
+  return append_impl(k_new_bf16, v_new_bf16, seqlens, nullptr, 0, 0, B, n_new, Hkv, d, Lmax,
+                     k_cache, v_cache, kbar, stream);
+}
+
+mpfa_status mpfa_append_kv_paged(const void* k_new_bf16, const void* v_new_bf16,
+                                 const int32_t* seqlens, const int32_t* block_table,
+                                 int num_pages, int max_pages, int B, int n_new, int Hkv, int d,
+                                 mpfa_nvfp4* k_pool, mpfa_fp8* v_pool, mpfa_stream_t stream) {
+  if (!block_table) return MPFA_ERR_INVALID_ARG;
+  if (max_pages <= 0 || max_pages > (1 << 30) / 128) return MPFA_ERR_INVALID_ARG;
+  return append_impl(k_new_bf16, v_new_bf16, seqlens, block_table, num_pages, max_pages, B, n_new,
+                     Hkv, d, 128 * max_pages, k_pool, v_pool, nullptr, stream);
 }
 
 mpfa_status mpfa_selftest_wait_timeout(unsigned long long limit_ns, mpfa_stream_t stream) {

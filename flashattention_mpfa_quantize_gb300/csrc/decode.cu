@@ -222,16 +222,60 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // split-major order: every unit's first split is dispatched before any
-  // second split, and so on, so the shorter tail splits of variable-length
-  // sequences (and the empty splits past a sequence's end) come last and
-  // fill in behind the full ones instead of extending the kernel's tail
   const int units = a.B * a.Hkv;
-  const int split = blockIdx.x / units;
-  const int bk = blockIdx.x % units;  // b * Hkv + kv head
-  const int b = bk / a.Hkv;
+  const int items = units * a.nsplit;
   const int g = a.Hq / a.Hkv;
   const int T = a.compensate ? a.T : 0;
+  auto bar = [&](int i) { return sbase + kOffBar + 8u * (uint32_t)i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc + 8);
+  volatile int* item_slot = reinterpret_cast<volatile int*>(smem + kOffMisc + 16);
+  float* red = reinterpret_cast<float*>(smem + kOffRed);
+
+  // Persistent: the CTA takes (KV unit, split) items from a global counter
+  // until they run out, so a slot freed by a short split takes the next item
+  // at once.  Items are numbered split-major (every unit's first split
+  // before any second split), so the shorter tail splits of variable-length
+  // sequences and the empty splits past a sequence's end come last.  Between
+  // items the whole CTA synchronises: every asynchronous copy and product of
+  // the item has been waited for by then, so the barriers are re-initialised
+  // for the next item and the tensor memory is reused.
+  if (threadIdx.x == 0) *abort_flag = 0;
+  if (warp == 5) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  if (warp == 4 && lane == 0) {
+    prefetch_tensormap(&map_k);
+    prefetch_tensormap(&map_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  for (;;) {
+  if (threadIdx.x == 0) {
+    *item_slot = atomicAdd(a.work, 1);
+    mbar_init(bar(kBarQReady), 128);
+    mbar_init(bar(kBarSFull0), 1);
+    mbar_init(bar(kBarSFull0 + 1), 1);
+    mbar_init(bar(kBarPReady0), 128);
+    mbar_init(bar(kBarPReady0 + 1), 128);
+    mbar_init(bar(kBarODone), 1);
+    mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarPFree0), 1);
+    mbar_init(bar(kBarPFree0 + 1), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(kBarKFull0 + s), 1);
+      mbar_init(bar(kBarVFull0 + s), 1);
+      mbar_init(bar(kBarKvEmpty0 + s), 1);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const int item = *item_slot;
+  if (item >= items || *abort_flag) break;
+  const int split = item / units;
+  const int bk = item % units;  // b * Hkv + kv head
+  const int b = bk / a.Hkv;
   // 0 <= seqlens[b] <= Lmax is the caller's contract; a length outside it is
   // clamped (so no split reads past its own cache rows) and recorded as
   // MPFA_ERR_INVALID_ARG in the status word
@@ -249,42 +293,8 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
         a.part_o[(row * a.nsplit + split) * 128 + threadIdx.x] = 0.0f;
         if (threadIdx.x == 0) a.part_lse[row * a.nsplit + split] = -INFINITY;
       }
-    return;
-  }
-
-  auto bar = [&](int i) { return sbase + kOffBar + 8u * (uint32_t)i; };
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc + 8);
-  float* red = reinterpret_cast<float*>(smem + kOffRed);
-
-  if (threadIdx.x == 0) {
-    *abort_flag = 0;
-    mbar_init(bar(kBarQReady), 128);
-    mbar_init(bar(kBarSFull0), 1);
-    mbar_init(bar(kBarSFull0 + 1), 1);
-    mbar_init(bar(kBarPReady0), 128);
-    mbar_init(bar(kBarPReady0 + 1), 128);
-    mbar_init(bar(kBarODone), 1);
-    mbar_init(bar(kBarDrain), 1);
-    mbar_init(bar(kBarPFree0), 1);
-    mbar_init(bar(kBarPFree0 + 1), 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(kBarKFull0 + s), 1);
-      mbar_init(bar(kBarVFull0 + s), 1);
-      mbar_init(bar(kBarKvEmpty0 + s), 1);
-    }
-    fence_barrier_init();
-  }
-  if (warp == 5) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == 4) {
+  } else if (warp == 4) {
     if (lane == 0) {
-      prefetch_tensormap(&map_k);
-      prefetch_tensormap(&map_v);
       const int row0 = bk * a.Lmax + k0;
       int issued = 0;
       for (int j = 0; j < ntiles; ++j) {
@@ -292,7 +302,18 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
         if (j >= kStages &&
             !mbar_wait_tf(bar(kBarKvEmpty0 + s), ((j / kStages) - 1) & 1, a.err, abort_flag))
           break;
-        const int row = row0 + j * 128;
+        // contiguous cache: rows of (b, KV head) at bk * Lmax; paged pool:
+        // key tile k0/128 + j of sequence b lives in page block_table[b][.],
+        // whose KV head's 128 rows start at (page * Hkv + head) * 128
+        int row = row0 + j * 128;
+        if (a.block_table) {
+          int page = a.block_table[(size_t)b * a.max_pages + k0 / 128 + j];
+          if (page < 0 || page >= a.num_pages) {  // a bad entry reads page 0, and is reported
+            record_error(a.err, kErrInvalidArg);
+            page = 0;
+          }
+          row = (page * a.Hkv + bk % a.Hkv) * 128;
+        }
         mbar_expect_tx(bar(kBarKFull0 + s), 8192 + 1024);
         tma_load_2d(sbase + kOffK + s * 8192, &map_k, 0, row, bar(kBarKFull0 + s));
         bulk_load(sbase + kOffKs + s * 1024, a.ks + (size_t)row * 8, 1024, bar(kBarKFull0 + s));
@@ -585,6 +606,11 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
       }
     }
   }
+  // the item is done in every role; item_slot and the barriers are rewritten next
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  }
 
   tc_fence_before();
   __syncthreads();
@@ -657,22 +683,24 @@ static int split_ctas_per_sm(int dev) {
   return occ;
 }
 
-// Chunk (keys per split) for B x Hkv units of Lmax keys: the split count that
-// minimises  waves x (128-key tiles per CTA + a fixed per-CTA cost), where a
-// wave is one CTA in every resident slot.  The fixed cost (query codes,
-// TMEM allocation, pipeline fill and drain, partial results) is taken as 4
-// tiles' time.
+// Chunk (keys per split) for B x Hkv units of Lmax keys.  The split kernel
+// is persistent with a dynamic item queue, so its time is about
+//   (all tiles + a fixed cost per item) / resident slots  +  one item
+// (the last item taken finishes alone).  The fixed cost (query codes,
+// barrier set-up, pipeline fill and drain, partial results) is taken as
+// 8 tiles' time; lengths are assumed to be Lmax.  The split count that
+// minimises this is used.
 int decode_default_chunk(int B, int Hkv, int Lmax, int num_sms) {
-  constexpr long long kCtaCostTiles = 4;
-  const long long units = (long long)B * Hkv;
-  const long long slots = (long long)split_ctas_per_sm(current_device()) * num_sms;
+  constexpr double kItemCostTiles = 8.0;
+  const double units = (double)B * Hkv;
+  const double slots = (double)split_ctas_per_sm(current_device()) * num_sms;
   const long long tiles = (Lmax + 127) / 128;
-  long long best_n = 1, best_cost = -1;
+  long long best_n = 1;
+  double best_cost = -1.0;
   for (long long n = 1; n <= tiles; ++n) {
-    const long long per_cta = (tiles + n - 1) / n;
-    if (n > 1 && (tiles + per_cta - 1) / per_cta < n) continue;  // same chunk as a smaller n
-    const long long waves = (units * n + slots - 1) / slots;
-    const long long cost = waves * (per_cta + kCtaCostTiles);
+    const long long per_item = (tiles + n - 1) / n;
+    if (n > 1 && (tiles + per_item - 1) / per_item < n) continue;  // same chunk as a smaller n
+    const double cost = units * ((double)tiles + n * kItemCostTiles) / slots + (double)per_item;
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best_n = n;
@@ -691,7 +719,8 @@ size_t decode_workspace_bytes(int B, int Hq, int Hkv, int nsplit) {
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   CUtensorMap mk, mv;
-  const uint64_t rows = (uint64_t)a.B * a.Hkv * a.Lmax;
+  const uint64_t rows = a.block_table ? (uint64_t)a.num_pages * a.Hkv * 128
+                                      : (uint64_t)a.B * a.Hkv * a.Lmax;
   if (!make_map_2d_u8(&mk, a.kc, 64, rows, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map_2d_u8(&mv, a.vc, 128, rows, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
@@ -701,13 +730,20 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
                                   current_device(), attr_set);
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = cudaMemsetAsync(a.amax, 0, sizeof(unsigned), stream);
+  // the amax word and the split kernel's item counter (same 256-byte slot)
+  cudaError_t e = cudaMemsetAsync(a.amax, 0, 256, stream);
   if (e != cudaSuccess) return e;
   dq_stats_kernel<<<a.B * a.Hkv, 128, 0, stream>>>(a);
   const int rows_q = a.B * a.Hq + (a.compensate ? a.B * a.Hkv : 0);
   dq_quant_kernel<<<(rows_q * 8 + 127) / 128, 128, 0, stream>>>(a);
-  split_kernel<<<a.B * a.Hkv * a.nsplit, kThreads, kSmemBytes, stream>>>(
-      mk, mv, a, (float)(1.4426950408889634 / std::sqrt(128.0)));
+  // persistent: one CTA per resident slot (or fewer if there are fewer items)
+  const int items = a.B * a.Hkv * a.nsplit;
+  const int sms = sm_count(current_device());
+  const int slots = split_ctas_per_sm(current_device()) * (sms > 0 ? sms : 1);
+  DecodeArgs ka = a;
+  ka.work = reinterpret_cast<int*>(a.amax + 32);
+  split_kernel<<<items < slots ? items : slots, kThreads, kSmemBytes, stream>>>(
+      mk, mv, ka, (float)(1.4426950408889634 / std::sqrt(128.0)));
   combine_kernel<<<a.B * a.Hq, 128, 0, stream>>>(a);
   return cudaGetLastError();
 }

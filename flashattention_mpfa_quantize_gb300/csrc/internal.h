@@ -66,6 +66,9 @@ struct AppendArgs {
   uint8_t* vc;
   const float* s_v;
   const float* kbar;  // [B][Hkv][128] channel means of a smoothed cache, or null
+  // paged pool (see DecodeArgs), or null block_table
+  const int32_t* block_table;
+  int num_pages, max_pages;
   int* err;
 };
 
@@ -96,6 +99,10 @@ struct DecodeArgs {
   const float* s_v;
   const int32_t* seqlens;
   const float* kbar;  // [B][Hkv][128] channel means of a smoothed cache, or null
+  // paged pool (null block_table: contiguous [B][Hkv][Lmax] cache): cache
+  // rows [num_pages][Hkv][128], block_table [B][max_pages], Lmax = 128 * max_pages
+  const int32_t* block_table;
+  int num_pages, max_pages;
   int B, Hq, Hkv, Lmax, compensate, T, chunk, nsplit;
   void* o;     // bf16 [B][Hq][128]
   float* lse;  // [B][Hq] or null
@@ -108,6 +115,7 @@ struct DecodeArgs {
   float* part_o;       // [B][Hq][nsplit][128]
   float* part_lse;     // [B][Hq][nsplit]
   float* q_kbar;       // [B][Hq + Hkv]: code-unit dot products with kbar (kbar only)
+  int* work;           // split kernel's item counter (zeroed by the launch)
   int* err;
 };
 

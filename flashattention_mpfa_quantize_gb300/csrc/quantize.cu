@@ -731,8 +731,21 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
     const int pos0 = in ? a.seqlens[b] : 0;
     const bool fits = pos0 >= 0 && pos0 <= a.Lmax - a.n_new;
     if (in && !fits && t == 0 && h == 0 && j == 0) record_error(a.err, kErrInvalidArg);
-    const bool store = in && fits;
-    const size_t r = ((size_t)b * a.Hkv + h) * a.Lmax + (size_t)(store ? pos0 + t : 0);
+    bool store = in && fits;
+    size_t r = ((size_t)b * a.Hkv + h) * a.Lmax + (size_t)(store ? pos0 + t : 0);
+    if (a.block_table && store) {
+      // paged pool: row pos of sequence b is row pos % 128 of page
+      // block_table[b][pos / 128], whose KV head h rows start at (page * Hkv + h) * 128
+      const int pos = pos0 + t;
+      const int page = a.block_table[(size_t)b * a.max_pages + pos / 128];
+      if (page < 0 || page >= a.num_pages) {
+        if (j == 0) record_error(a.err, kErrInvalidArg);
+        store = false;
+        r = 0;
+      } else {
+        r = ((size_t)page * a.Hkv + h) * 128 + (size_t)(pos % 128);
+      }
+    }
     float x[16];
     {
       uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;

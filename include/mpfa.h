@@ -260,6 +260,47 @@ mpfa_status mpfa_append_kv(const void *k_new_bf16, const void *v_new_bf16, const
                            int B, int n_new, int Hkv, int d, int Lmax, mpfa_nvfp4 *k_cache,
                            mpfa_fp8 *v_cache, const float *kbar, mpfa_stream_t stream);
 
+/*
+ * Paged KV pool (the MXAttention blog's section on quantized KV caches: KV
+ * quantized when written, its block scales in a pool of their own; the MpFA
+ * abstract's decode partitioning).  The pool holds num_pages pages of 128
+ * tokens; page p holds, for every KV head h, 128 rows of codes at pool rows
+ * (p * Hkv + h) * 128 .. +127:
+ *   k_pool: codes [num_pages][Hkv][128][64], block scales in the 128-row
+ *   tile layout over those rows (one 1 KB tile per page and head, a pool of
+ *   its own), tensor scale; v_pool: codes [num_pages][Hkv][128][128],
+ *   tensor scale.  mpfa_quantize_qkv(NULL, K, V, B = num_pages, Nk = 128,
+ *   ...) on bf16 K, V [num_pages][128][Hkv][d] writes exactly this layout.
+ *   block_table [B][max_pages] int32 (device): page of each sequence's
+ *   128-token block; sequence b's token t is row t % 128 of page
+ *   block_table[b][t / 128].  Entries past a sequence's length are not
+ *   read.  An entry outside [0, num_pages) is reported as
+ *   MPFA_ERR_INVALID_ARG in the device status word (the decode reads page 0
+ *   in its place, the append writes nothing for it).
+ * Key-side smoothing is not offered for a pool: its kbar is one vector per
+ * sequence and KV head, while the pool's codes have no sequence.
+ */
+
+/* Split-KV decode over a paged pool: as mpfa_decode with Lmax =
+ * 128 * max_pages and the cache rows looked up through block_table.
+ * Workspace: mpfa_decode_workspace_size(B, Hq, Hkv, d, 128 * max_pages,
+ * kv_chunk). */
+mpfa_status mpfa_decode_paged(const void *q_bf16, const mpfa_nvfp4 *k_pool, const mpfa_fp8 *v_pool,
+                              const int32_t *block_table, int num_pages, int max_pages,
+                              const int32_t *seqlens, int B, int Hq, int Hkv, int d,
+                              int compensate, int T, int kv_chunk, void *o_bf16, float *lse,
+                              mpfa_nvfp4 *q_quant_out, mpfa_rank1 *qbar_quant_out,
+                              int *used_chunk, void *workspace, size_t ws_bytes,
+                              mpfa_stream_t stream);
+
+/* Quantize-on-append into a paged pool: as mpfa_append_kv with Lmax =
+ * 128 * max_pages and token t of sequence b written to row t % 128 of page
+ * block_table[b][t / 128] (the caller assigns the pages first). */
+mpfa_status mpfa_append_kv_paged(const void *k_new_bf16, const void *v_new_bf16,
+                                 const int32_t *seqlens, const int32_t *block_table,
+                                 int num_pages, int max_pages, int B, int n_new, int Hkv, int d,
+                                 mpfa_nvfp4 *k_pool, mpfa_fp8 *v_pool, mpfa_stream_t stream);
+
 /* Failure-path self-test: enqueues a one-thread kernel that waits, with the
  * same bounded barrier wait every kernel uses, on an on-chip barrier that
  * nothing arrives on.  After limit_ns nanoseconds (1 .. 2e9) the wait gives up

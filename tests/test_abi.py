@@ -182,3 +182,41 @@ def test_append_kv_host_validation(lib):
     assert call(v=R(F8(ok, None))) == 1         # cache without its tensor scale
     assert call(B=4096, H=8, L=1 << 16) == 1    # 2^31 cache rows or more
 
+
+
+def test_paged_entry_points_host_validation(lib):
+    """mpfa_decode_paged / mpfa_append_kv_paged reject a missing block table,
+    non-positive pool sizes and pools of 2^31 rows or more before any CUDA
+    call."""
+    class NV(ctypes.Structure):
+        _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                    ("tensor_scale", ctypes.c_void_p)]
+
+    class F8(ctypes.Structure):
+        _fields_ = [("codes", ctypes.c_void_p), ("tensor_scale", ctypes.c_void_p)]
+
+    ok = 0x10000
+    k, v, R = NV(ok, ok, ok), F8(ok, ok), ctypes.byref
+    d = lib.mpfa_decode_paged
+    d.restype = ctypes.c_int
+    used = ctypes.c_int(0)
+
+    def dec(table=_fake(ok), pages=8, maxp=4, dh=128):
+        return d(_fake(ok), R(k), R(v), table, pages, maxp, _fake(ok), 2, 8, 2, dh, 1, 2, 0,
+                 _fake(ok), None, None, None, R(used), _fake(ok), ctypes.c_size_t(1 << 40), None)
+
+    assert dec(dh=64) == 2
+    assert dec(table=None) == 1
+    assert dec(pages=0) == 1
+    assert dec(maxp=0) == 1
+    assert dec(pages=1 << 24) == 1        # 2^24 pages x 2 heads x 128 rows = 2^32
+    a = lib.mpfa_append_kv_paged
+    a.restype = ctypes.c_int
+
+    def app(table=_fake(ok), pages=8, maxp=4, n=1):
+        return a(_fake(ok), _fake(ok), _fake(ok), table, pages, maxp, 2, n, 2, 128, R(k), R(v), None)
+
+    assert app(table=None) == 1
+    assert app(pages=-1) == 1
+    assert app(n=513) == 1                # more new tokens than 4 pages hold
+    assert app(pages=1 << 24) == 1

@@ -23,10 +23,10 @@ CASES = [
     ("tiny_n256", mi.PREFILL["tiny_n256"], [(0, 0)], None),
     ("tiny_n256_qoffset", mi.PREFILL["tiny_n256_qoffset"], [(0, 0)], None),
     ("n2048_causal_qoffset", mi.custom_prefill(1, 8, 2, 2048, True, q_offset=True, name="n2048q"),
-     [(0, 0), (0, 5)], np.arange(0, 2048, 7)),
+     [(0, h) for h in range(8)], np.arange(0, 2048, 7)),
     ("n2048_causal_plain", mi.custom_prefill(1, 8, 2, 2048, True, k_offset=False, k_outliers=0,
                                              v_outlier_p=0.0, name="n2048p"),
-     [(0, 0), (0, 5)], np.arange(0, 2048, 7)),
+     [(0, h) for h in range(8)], np.arange(0, 2048, 7)),
 ]
 
 

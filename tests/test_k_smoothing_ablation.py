@@ -1,11 +1,12 @@
-"""Ablation on the CPU with the oracle's quantizers: per-channel K smoothing
-on top of the method's Q-side rank-one term.  K' = K - kbar (kbar the exact
-mean of each channel over all keys of a KV head) is quantized instead of K.
-The dropped term q.kbar is the same for every key of a query row, so the
-softmax, the reference-max rule (which only looks at differences) and O are
-unchanged by leaving it out; only the LSE would need it added back.  K's
-NVFP4 error dominates on the synthetic inputs (channel offsets and outlier
-channels), so removing the channel means should cut the output error."""
+"""Ablation on the CPU with the oracle: key-side smoothing (the oracle's
+quantize_k(smooth=True), kbar the keys' channel means) on top of the
+method's Q-side rank-one term.  The dropped term q.kbar is the same for
+every key of a query row, so the softmax, the reference-max rule (which only
+looks at differences) and O are unchanged by leaving it out; the LSE gets it
+back.  K's NVFP4 error dominates on these synthetic inputs (channel offsets
+and outlier channels), so removing the channel means cuts the output error
+here; it does not on every draw (the N=2048 case of the GPU accuracy table
+gets worse)."""
 import numpy as np
 import pytest
 
@@ -21,10 +22,9 @@ def ablation(cfg, seed=0):
     vz = orc.quantize_v(Vn)
     exact = orc.prefill_exact(Qn.astype(np.float64), Kn.astype(np.float64), Vn.astype(np.float64),
                               causal=cfg.causal)
-    kbar = Kn.astype(np.float64).mean(axis=1, keepdims=True)      # [B,1,Hkv,d]
-    Ks = (Kn.astype(np.float64) - kbar).astype(np.float32)
     out = {}
-    for name, kz in (("q_smoothing", orc.quantize_k(Kn)), ("q_and_k_smoothing", orc.quantize_k(Ks))):
+    for name, kz in (("q_smoothing", orc.quantize_k(Kn)),
+                     ("q_and_k_smoothing", orc.quantize_k(Kn, smooth=True))):
         emu = orc.prefill_emulate(qz, kz, vz, causal=cfg.causal)
         got = np.concatenate([emu[key][0] for key in sorted(emu)])
         want = np.concatenate([exact[key][0] for key in sorted(emu)])
