@@ -333,16 +333,16 @@ def prefill_roofline(cfg, pre_ms, peaks):
 
 
 def time_prefill(mp, cfg, Q, K, V, flush, stream, steps, warmup, compensate=True, T=T_TERMS,
-                 clocks=None):
+                 clocks=None, k_smooth=False):
     """Quantize + prefill of `cfg` timed with CUDA events on the launching
     stream, L2 flushed before every step.  Returns (step, quantize, prefill)
     mean ms."""
-    z = mp.quantize_qkv(Q, K, V, compensate=compensate, T=T)
+    z = mp.quantize_qkv(Q, K, V, compensate=compensate, T=T, k_smooth=k_smooth)
     ws = z["_workspace"]
     o, lse = mp.prefill(z, causal=cfg.causal)
     for _ in range(max(warmup, 3)):
         flush.zero_()
-        z = mp.quantize_qkv(Q, K, V, compensate=compensate, T=T, workspace=ws)
+        z = mp.quantize_qkv(Q, K, V, compensate=compensate, T=T, k_smooth=k_smooth, workspace=ws)
         mp.prefill(z, causal=cfg.causal, out=o, lse=lse)
     torch.cuda.synchronize()
     if mp.get_error() != 0:
@@ -356,7 +356,7 @@ def time_prefill(mp, cfg, Q, K, V, flush, stream, steps, warmup, compensate=True
     for ev in evs:
         flush.zero_()
         ev[0].record(stream)
-        z = mp.quantize_qkv(Q, K, V, compensate=compensate, T=T, workspace=ws)
+        z = mp.quantize_qkv(Q, K, V, compensate=compensate, T=T, k_smooth=k_smooth, workspace=ws)
         ev[1].record(stream)
         mp.prefill(z, causal=cfg.causal, out=o, lse=lse)
         ev[2].record(stream)
@@ -414,8 +414,7 @@ def run_gpu(args):
     extra = {}
     if args.only is None:
         few = max(3, min(args.steps, 5))
-        roofline["compensation"] = compensation_cost(mp, cfg, Q, K, V, flush, stream, few,
-                                                     quant_ms, pre_ms)
+        roofline["compensation"] = compensation_cost(mp, cfg, Q, K, V, flush, stream, few)
         extra["bf16_sdpa"] = bf16_sdpa_baseline(Q, K, V, cfg, flush, stream, few, flops,
                                                 step_ms, pre_ms)
         e2e = run_e2e(mp, dev, stream, cfg, Q, K, V, max(3, min(args.steps, 20)))
@@ -518,18 +517,29 @@ def bf16_sdpa_baseline(Q, K, V, cfg, flush, stream, steps, flops, step_ms, pre_m
             "speedup_of_step": ms / step_ms, "speedup_of_prefill_kernel": ms / pre_ms}
 
 
-def compensation_cost(mp, cfg, Q, K, V, flush, stream, steps, quant_on_ms, pre_on_ms):
-    """Quantize and prefill times with the rank-one compensation off and with
-    one term, against the timed step's (compensation on, two terms)."""
-    _, q_off, p_off = time_prefill(mp, cfg, Q, K, V, flush, stream, steps, 2, compensate=False)
-    _, q_1, p_1 = time_prefill(mp, cfg, Q, K, V, flush, stream, steps, 2, compensate=True, T=1)
-    return {"steps": steps, "quantize_ms_off": q_off, "prefill_ms_off": p_off,
-            "quantize_ms_T1": q_1, "prefill_ms_T1": p_1,
-            "quantize_ms_T2": quant_on_ms, "prefill_ms_T2": pre_on_ms,
-            "prefill_overhead_pct_T1": 100.0 * (p_1 / p_off - 1.0),
-            "prefill_overhead_pct_T2": 100.0 * (pre_on_ms / p_off - 1.0),
-            "step_overhead_pct_T1": 100.0 * ((q_1 + p_1) / (q_off + p_off) - 1.0),
-            "step_overhead_pct_T2": 100.0 * ((quant_on_ms + pre_on_ms) / (q_off + p_off) - 1.0)}
+def compensation_cost(mp, cfg, Q, K, V, flush, stream, steps):
+    """Quantize and prefill times with the rank-one compensation off, with one
+    and with two terms, and with two terms plus key-side smoothing, timed in
+    interleaved rounds (so clock and power drift hit every variant alike)."""
+    variants = {"off": dict(compensate=False), "T1": dict(compensate=True, T=1),
+                "T2": dict(compensate=True, T=2),
+                "T2_ksmooth": dict(compensate=True, T=2, k_smooth=True)}
+    acc = {k: ([], []) for k in variants}
+    for _ in range(steps):
+        for k, kw in variants.items():
+            _, q, p = time_prefill(mp, cfg, Q, K, V, flush, stream, 1, 1, **kw)
+            acc[k][0].append(q)
+            acc[k][1].append(p)
+    out = {"rounds": steps}
+    for k in variants:
+        out[f"quantize_ms_{k}"] = statistics.mean(acc[k][0])
+        out[f"prefill_ms_{k}"] = statistics.mean(acc[k][1])
+    p_off, q_off = out["prefill_ms_off"], out["quantize_ms_off"]
+    for k in ("T1", "T2", "T2_ksmooth"):
+        out[f"prefill_overhead_pct_{k}"] = 100.0 * (out[f"prefill_ms_{k}"] / p_off - 1.0)
+        out[f"step_overhead_pct_{k}"] = 100.0 * ((out[f"quantize_ms_{k}"] + out[f"prefill_ms_{k}"])
+                                                 / (q_off + p_off) - 1.0)
+    return out
 
 
 def run_decode(mp, dev, stream, peaks, flush, args, cfg):
