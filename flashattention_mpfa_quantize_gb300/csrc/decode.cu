@@ -114,6 +114,7 @@ __device__ __forceinline__ void nvfp4_block(const float (&x)[16], float s, uint2
 
 __global__ void __launch_bounds__(128) dq_stats_kernel(DecodeArgs a) {
   __shared__ unsigned red[4];
+  pdl_trigger();
   const int bk = blockIdx.x;  // b * Hkv + kv head
   const int g = a.Hq / a.Hkv;
   const int c = threadIdx.x;
@@ -156,6 +157,8 @@ __device__ __forceinline__ float codes_dot(const uint2& codes, const float* w) {
 // (a mean row: over its T terms), which combine_kernel turns into the LSE
 // term q_eff . kbar / sqrt(d).
 __global__ void __launch_bounds__(128) dq_quant_kernel(DecodeArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int g = a.Hq / a.Hkv;
   const float s = tensor_scale(a.amax[0], 2688.0f);
   if (blockIdx.x == 0 && threadIdx.x == 0) *a.s_q = s;
@@ -250,6 +253,9 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the query codes and the item counter come from the kernels before
+  pdl_wait();
+  pdl_trigger();
 
   for (;;) {
   if (threadIdx.x == 0) {
@@ -626,6 +632,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const __grid_constant__
 // ---------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
+  pdl_wait();
   const size_t row = blockIdx.x;  // b * Hq + h
   const int c = threadIdx.x;
   float lmax = -INFINITY;
@@ -735,16 +742,21 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   dq_stats_kernel<<<a.B * a.Hkv, 128, 0, stream>>>(a);
   const int rows_q = a.B * a.Hq + (a.compensate ? a.B * a.Hkv : 0);
-  dq_quant_kernel<<<(rows_q * 8 + 127) / 128, 128, 0, stream>>>(a);
+  // the kernels after the statistics may start while their predecessor
+  // finishes (each waits for it before reading its results)
+  e = launch_pdl(dq_quant_kernel, dim3((rows_q * 8 + 127) / 128), dim3(128), 0, stream, a);
+  if (e != cudaSuccess) return e;
   // persistent: one CTA per resident slot (or fewer if there are fewer items)
   const int items = a.B * a.Hkv * a.nsplit;
   const int sms = sm_count(current_device());
   const int slots = split_ctas_per_sm(current_device()) * (sms > 0 ? sms : 1);
   DecodeArgs ka = a;
   ka.work = reinterpret_cast<int*>(a.amax + 32);
-  split_kernel<<<items < slots ? items : slots, kThreads, kSmemBytes, stream>>>(
-      mk, mv, ka, (float)(1.4426950408889634 / std::sqrt(128.0)));
-  combine_kernel<<<a.B * a.Hq, 128, 0, stream>>>(a);
+  e = launch_pdl(split_kernel, dim3(items < slots ? items : slots), dim3(kThreads), kSmemBytes,
+                 stream, mk, mv, ka, (float)(1.4426950408889634 / std::sqrt(128.0)));
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(combine_kernel, dim3(a.B * a.Hq), dim3(128), 0, stream, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

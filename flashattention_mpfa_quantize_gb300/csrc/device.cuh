@@ -206,6 +206,15 @@ __device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, in
   }
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel of the stream is still
+// running; pdl_wait() blocks until that kernel has completed and its memory
+// is visible (it returns at once when nothing precedes), pdl_trigger() lets
+// the next such kernel start launching once every CTA of this grid has
+// called it or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

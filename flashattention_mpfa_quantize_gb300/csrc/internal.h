@@ -3,6 +3,7 @@
 #pragma once
 
 #include <atomic>
+#include <utility>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -26,6 +27,24 @@ cudaError_t set_smem_once(const void* func, int bytes, int dev, std::atomic<bool
 
 // Everything the two quantization passes need.  Pointers are device pointers;
 // a tensor whose input pointer is null is skipped.
+// Launch with programmatic stream serialization: the kernel may begin (up
+// to its pdl_wait()) while the stream's previous kernel finishes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 struct QuantArgs {
   const void* q;  // bf16 [B][Nq][Hq][128]
   const void* k;  // bf16 [B][Nk][Hkv][128]

@@ -213,6 +213,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the codes and tensor scales come from the quantization kernels before
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == kWarpTma) {
     // ---------------- TMA producer (whole warp) ----------------
@@ -818,8 +821,9 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   // persistent: one CTA per SM (shared memory and TMEM admit one), each
   // walking its share of the work items
   const unsigned grid = (unsigned)(p.items < sms ? p.items : sms);
-  prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mo, p);
-  return cudaGetLastError();
+  // may start (barriers, tensor memory) while the quantization finishes
+  return launch_pdl(prefill_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream, mq, mk, mv,
+                    mo, p);
 }
 
 }  // namespace mpfa

@@ -329,6 +329,7 @@ __device__ __forceinline__ void block_stats(const __nv_bfloat16* x, int B, int N
 __global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm)
     stats_kernel(QuantArgs a, int nq_blocks, int nk_blocks, int nv_blocks) {
   __shared__ unsigned red[kStatsThreads / 32];
+  pdl_trigger();
   // per warp: the 32 lanes' column partials, transposed through shared memory
   __shared__ float xpose[kStatsThreads / 32][32][33];
   int bid = blockIdx.x;
@@ -366,6 +367,8 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm)
 // column's largest |x - kbar| is at its largest or smallest x).
 __global__ void __launch_bounds__(128) kbar_kernel(QuantArgs a) {
   __shared__ unsigned red[4];
+  pdl_wait();
+  pdl_trigger();
   const int bh = blockIdx.x, c = threadIdx.x;
   const int nblk = a.Nk / 128;
   const float* st = a.kstat + (size_t)bh * nblk * 384;
@@ -405,6 +408,8 @@ __device__ __forceinline__ float codes_dot(const uint2& codes, const float (&w)[
 // query row), with a register budget of its own.
 template <bool kSmooth>
 __global__ void __launch_bounds__(kThreads, kSmooth ? 5 : 6) quant_kernel(QuantArgs a) {
+  pdl_wait();   // the statistics (and key means) of the kernels before
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int warps_total = gridDim.x * (kThreads / 32);
   const int gwarp = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
@@ -707,6 +712,8 @@ __global__ void __launch_bounds__(kThreads, kSmooth ? 5 : 6) quant_kernel(QuantA
 // blocks by shuffles, so every lane takes part in every step and the
 // out-of-range and overrunning rows are masked, not skipped.
 __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
+  pdl_wait();   // the cache and its tensor scales may come from the kernel before
+  pdl_trigger();
   const float sk = *a.s_k, sv = *a.s_v;
   const bool vfast = sv >= kDivLo && sv <= kDivHi;
   const float ysv = __frcp_rn(sv);
@@ -850,15 +857,16 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
   if (a.k && a.ksmooth) {
-    kbar_kernel<<<a.B * a.Hkv, 128, 0, stream>>>(a);
-    e = cudaGetLastError();
+    e = launch_pdl(kbar_kernel, dim3(a.B * a.Hkv), dim3(128), 0, stream, a);
     if (e != cudaSuccess) return e;
   }
   dim3 grid(sms * 8, 4);
+  // the coding pass may start while the statistics finish (it waits for them)
   if (a.ksmooth)
-    quant_kernel<true><<<grid, kThreads, 0, stream>>>(a);
+    e = launch_pdl(quant_kernel<true>, grid, dim3(kThreads), 0, stream, a);
   else
-    quant_kernel<false><<<grid, kThreads, 0, stream>>>(a);
+    e = launch_pdl(quant_kernel<false>, grid, dim3(kThreads), 0, stream, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -867,7 +875,9 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
   if (units == 0) return cudaSuccess;
   const size_t need = (units + kThreads - 1) / kThreads;
   const size_t cap = (size_t)num_sms() * 8;
-  append_kernel<<<(unsigned)(need < cap ? need : cap), kThreads, 0, stream>>>(a);
+  cudaError_t e = launch_pdl(append_kernel, dim3((unsigned)(need < cap ? need : cap)),
+                             dim3(kThreads), 0, stream, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
