@@ -6,13 +6,59 @@ looks at differences) and O are unchanged by leaving it out; the LSE gets it
 back.  K's NVFP4 error dominates on these synthetic inputs (channel offsets
 and outlier channels), so removing the channel means cuts the output error
 here; it does not on every draw (the N=2048 case of the GPU accuracy table
-gets worse)."""
+gets worse).  The scope table's third variant, per-block key smoothing with
+the Q.kbar_block^T term added back as extra NVFP4 terms, is emulated here
+from the oracle's primitives (no kernel implements it)."""
 import numpy as np
 import pytest
 
 import mpfa_inputs as mi
 import oracle as orc
 from helpers import np_f32, rel_l2
+
+
+def _block_smoothed_keys(Kn, T=2):
+    """Keys with per-block smoothing and the Q.kbar_block^T term added back
+    (the scope table's third compensation variant): per (b, KV head) and
+    128-key block, kbar_blk = the block's fp32 mean, K' = fp32(K - kbar_blk)
+    coded in NVFP4, kbar_blk kept as T NVFP4 terms (the query-side rule with
+    the roles swapped), all sharing one tensor scale s_k from max(amax(K'),
+    amax(kbar_blk)).  The product with the keys is then q . (K' + sum of the
+    terms), so the effective keys (code units) are returned with s_k."""
+    B, N, H, d = Kn.shape
+    means, kp = {}, {}
+    amax = np.float32(0.0)
+    for b in range(B):
+        for h in range(H):
+            mb, xp = orc.block_means(np.ascontiguousarray(Kn[b, :, h, :]), orc.QBLOCK)
+            means[(b, h)], kp[(b, h)] = mb, xp
+            amax = max(amax, np.float32(np.abs(xp).max()), np.float32(np.abs(mb).max()))
+    s = orc.tensor_scale(amax, orc.NVFP4_QMAX)
+    keff = {}
+    for key in means:
+        c, sc = orc.nvfp4_quantize(kp[key], s)
+        tc, ts = orc.rank_one_terms(means[key], s, T)
+        terms = 0.0
+        for t in range(T):
+            terms = terms + orc.nvfp4_dequant(np.ascontiguousarray(tc[:, t]),
+                                              np.ascontiguousarray(ts[:, t]))
+        keff[key] = orc.nvfp4_dequant(c, sc) + np.repeat(terms, orc.QBLOCK, axis=0)
+    return keff, s
+
+
+def _emulate_with_keys(qz, keff, s_k, vz, causal, Hq, Hkv):
+    g = Hq // Hkv
+    cs = orc.score_scale_log2(qz["s_q"], s_k)
+    out = {}
+    for (b, hk), k in keff.items():
+        for h in range(hk * g, (hk + 1) * g):
+            q = orc.nvfp4_dequant(qz["qc"][b, h], qz["qs"][b, h])
+            qb = orc._terms_sum(qz["qbc"][b, h], qz["qbs"][b, h])
+            qadd = np.repeat(qb, orc.QBLOCK, axis=0)[: q.shape[0]]
+            v = orc.fp8_dequant(vz["vc"][b, hk])
+            out[(b, h)] = orc.attn_online(q, qadd, k, v, score_scale=cs,
+                                          out_scale=float(vz["s_v"]), causal=causal)
+    return out
 
 
 def ablation(cfg, seed=0):
@@ -29,6 +75,11 @@ def ablation(cfg, seed=0):
         got = np.concatenate([emu[key][0] for key in sorted(emu)])
         want = np.concatenate([exact[key][0] for key in sorted(emu)])
         out[name] = rel_l2(got, want)
+    keff, s_k = _block_smoothed_keys(Kn)
+    emu = _emulate_with_keys(qz, keff, s_k, vz, cfg.causal, cfg.Hq, cfg.Hkv)
+    got = np.concatenate([emu[key][0] for key in sorted(emu)])
+    want = np.concatenate([exact[key][0] for key in sorted(emu)])
+    out["q_and_k_block_smoothing"] = rel_l2(got, want)
     return out
 
 
@@ -45,3 +96,6 @@ def test_k_smoothing_reduces_error(name):
     r = ablation(CASES[name])
     print(name, {k: round(v, 4) for k, v in r.items()})
     assert r["q_and_k_smoothing"] < r["q_smoothing"]
+    # the per-block form removes the channel offsets too (and adapts to
+    # blocks); its rank-one term carries the block means back exactly enough
+    assert r["q_and_k_block_smoothing"] < r["q_smoothing"]
