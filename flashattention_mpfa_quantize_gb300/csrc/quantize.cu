@@ -61,38 +61,55 @@ __device__ __forceinline__ float div_rn(float x, float d, float y) {
   return __fmaf_rn(__fmaf_rn(-d, q0, x), y, q0);
 }
 
+// Two quotients of div_rn at once (packed fp32; nd = -d, y = RN(1/d)).
+__device__ __forceinline__ float2 div_rn2(float2 x, float2 nd, float2 y) {
+  const float2 q0 = __fmul2_rn(x, y);
+  return __ffma2_rn(__ffma2_rn(nd, q0, x), y, q0);
+}
+
+// Eight E2M1 codes (element 2i in the low nibble of byte i) of four pairs.
+__device__ __forceinline__ uint32_t e2m1x8(float2 a, float2 b, float2 c, float2 d) {
+  uint32_t r;
+  asm("{\n.reg .b8 t0, t1, t2, t3;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 t2, %6, %5;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 t3, %8, %7;\n"
+      "mov.b32 %0, {t0, t1, t2, t3};\n}"
+      : "=r"(r)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y), "f"(d.x), "f"(d.y));
+  return r;
+}
+
 // One NVFP4 block of 16 fp32 values with tensor scale s: eight code bytes
-// (element 2i in the low nibble of byte i) and the E4M3 block scale.
+// (element 2i in the low nibble of byte i) and the E4M3 block scale.  The
+// quotients are computed two at a time in packed fp32 operations (each half
+// rounds on its own, so every quotient is the scalar one).
 __device__ __forceinline__ void nvfp4_block(const float (&x)[16], float s, uint2& codes,
                                             uint32_t& sb) {
   float bamax = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) bamax = fmaxf(bamax, fabsf(x[i]));
+  for (int i = 0; i < 16; i += 2) bamax = fmax3(bamax, fabsf(x[i]), fabsf(x[i + 1]));
   float t = __fdiv_rn(bamax, __fmul_rn(6.0f, s));
   sb = e4m3_pos(t);
   uint32_t w0 = 0, w1 = 0;
   if (sb != 0) {
     const float denom = __fmul_rn(e4m3_value(sb), s);
+    float2 q[8];
     if (denom >= kDivLo && denom <= kDivHi && bamax <= 3.40282347e38f) {
       const float y = __frcp_rn(denom);
+      const float2 y2 = make_float2(y, y), nd2 = make_float2(-denom, -denom);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        uint32_t byte = e2m1x2(div_rn(x[2 * i], denom, y), div_rn(x[2 * i + 1], denom, y));
-        if (i < 4)
-          w0 |= byte << (8 * i);
-        else
-          w1 |= byte << (8 * (i - 4));
+        q[i] = div_rn2(make_float2(x[2 * i], x[2 * i + 1]), nd2, y2);
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        uint32_t byte = e2m1x2(__fdiv_rn(x[2 * i], denom), __fdiv_rn(x[2 * i + 1], denom));
-        if (i < 4)
-          w0 |= byte << (8 * i);
-        else
-          w1 |= byte << (8 * (i - 4));
-      }
+      for (int i = 0; i < 8; ++i)
+        q[i] = make_float2(__fdiv_rn(x[2 * i], denom), __fdiv_rn(x[2 * i + 1], denom));
     }
+    w0 = e2m1x8(q[0], q[1], q[2], q[3]);
+    w1 = e2m1x8(q[4], q[5], q[6], q[7]);
   }
   codes = make_uint2(w0, w1);
 }
@@ -217,25 +234,43 @@ __device__ __forceinline__ void block_stats(const __nv_bfloat16* x, int B, int N
     if (unit + nblocks < units) load_unit(unit + nblocks, wn);
     const int blk = unit % nblk, bh = unit / nblk;
     const int h = bh % H, b = bh / H;
-    // column max |x| and min (|x| - 1) (zero -> 0xFFFF) on bf16 bit
-    // patterns, two columns per 32-bit word, over the 16 lanes of the
-    // column group
+    // per column over the 16 lanes of the column group: the largest and
+    // smallest value (bf16 pairs, two columns per 32-bit word; a NaN makes
+    // both NaN, which sends the column to the fp64 path) and the smallest
+    // nonzero magnitude minus one (zero -> 0xFFFF)
+    uint32_t hx[4], hn[4];
     float C[8];
     bool bad[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      uint32_t mx = 0, mn = 0xFFFFFFFFu;
+      uint32_t mn = 0xFFFFFFFFu;
+      __nv_bfloat162 vx = __halves2bfloat162(__ushort_as_bfloat16(0xFF80), __ushort_as_bfloat16(0xFF80));
+      __nv_bfloat162 vn = __halves2bfloat162(__ushort_as_bfloat16(0x7F80), __ushort_as_bfloat16(0x7F80));
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const uint32_t mag = word(w[k], j) & 0x7FFF7FFFu;
-        mx = __vmaxu2(mx, mag);
-        mn = __vminu2(mn, __vsub2(mag, 0x00010001u));
+        const uint32_t wv = word(w[k], j);
+        const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&wv);
+        vx = __hmax2_nan(vx, v);
+        vn = __hmin2_nan(vn, v);
+        mn = __vminu2(mn, __vsub2(wv & 0x7FFF7FFFu, 0x00010001u));
       }
+      uint32_t ux = *reinterpret_cast<uint32_t*>(&vx), un = *reinterpret_cast<uint32_t*>(&vn);
 #pragma unroll
       for (int o = 2; o < 32; o <<= 1) {
-        mx = __vmaxu2(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const uint32_t ox = __shfl_xor_sync(0xffffffffu, ux, o);
+        const uint32_t on = __shfl_xor_sync(0xffffffffu, un, o);
         mn = __vminu2(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        vx = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&ux),
+                         *reinterpret_cast<const __nv_bfloat162*>(&ox));
+        vn = __hmin2_nan(*reinterpret_cast<const __nv_bfloat162*>(&un),
+                         *reinterpret_cast<const __nv_bfloat162*>(&on));
+        ux = *reinterpret_cast<uint32_t*>(&vx);
+        un = *reinterpret_cast<uint32_t*>(&vn);
       }
+      hx[j] = ux;
+      hn[j] = un;
+      // largest magnitude of each column: max(|largest|, |smallest|)
+      const uint32_t mx = __vmaxu2(ux & 0x7FFF7FFFu, un & 0x7FFF7FFFu);
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const uint32_t cmx = e ? mx >> 16 : mx & 0xFFFFu, cmn = e ? mn >> 16 : mn & 0xFFFFu;
@@ -245,30 +280,30 @@ __device__ __forceinline__ void block_stats(const __nv_bfloat16* x, int B, int N
         C[2 * j + e] = bad[2 * j + e] ? 0.0f : __uint_as_float(((uint32_t)(E + 7) << 23) | 0x400000u);
       }
     }
-    // per column: the two sums and the extremes over the lane's 8 rows,
-    // stored as lane-major partials [lane][quantity * 8 + column]
+    // per column: the two sums over the lane's 8 rows, rows paired in the
+    // two halves of packed fp32 operations (each half rounds on its own, so
+    // every sum is the same exact value), stored lane-major [lane][column]
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
-      float s0 = 0.0f, s1 = 0.0f, xmx = -INFINITY, xmn = INFINITY;
+      const float2 cp = make_float2(C[t], C[t]), cn = make_float2(-C[t], -C[t]);
+      const float2 m1 = make_float2(-1.0f, -1.0f);
+      float2 s0 = make_float2(0.0f, 0.0f), s1 = make_float2(0.0f, 0.0f);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t wv = word(w[k], t >> 1);
-        const float x = __uint_as_float((t & 1) ? (wv & 0xFFFF0000u) : (wv << 16));
-        const float hi = __fsub_rn(__fadd_rn(x, C[t]), C[t]);
-        s0 = __fadd_rn(s0, hi);
-        s1 = __fadd_rn(s1, __fsub_rn(x, hi));
-        xmx = fmaxf(xmx, x);
-        xmn = fminf(xmn, x);
+      for (int k = 0; k < 8; k += 2) {
+        const uint32_t wa = word(w[k], t >> 1), wb = word(w[k + 1], t >> 1);
+        const float2 x = (t & 1) ? make_float2(bf16_hi(wa), bf16_hi(wb))
+                                 : make_float2(bf16_lo(wa), bf16_lo(wb));
+        const float2 hi = __fadd2_rn(__fadd2_rn(x, cp), cn);
+        s0 = __fadd2_rn(s0, hi);
+        s1 = __fadd2_rn(s1, __ffma2_rn(hi, m1, x));
       }
-      xp[lane][t] = s0;
-      xp[lane][8 + t] = s1;
-      xp[lane][16 + t] = xmx;
-      xp[lane][24 + t] = xmn;
+      xp[lane][t] = __fadd_rn(s0.x, s0.y);
+      xp[lane][8 + t] = __fadd_rn(s1.x, s1.y);
     }
     __syncwarp();
     // lane L < 16 finishes column group 2w + (L & 1), column t = L >> 1:
-    // sums and extremes over the 16 lanes of that group
-    float s0 = 0.0f, s1 = 0.0f, xmx = -INFINITY, xmn = INFINITY;
+    // sums over the 16 lanes of that group
+    float s0 = 0.0f, s1 = 0.0f;
     const int gsel = lane & 1, tc = (lane >> 1) & 7;
     if (lane < 16) {
 #pragma unroll
@@ -276,11 +311,17 @@ __device__ __forceinline__ void block_stats(const __nv_bfloat16* x, int B, int N
         const float* row = xp[2 * i + gsel];
         s0 = __fadd_rn(s0, row[tc]);
         s1 = __fadd_rn(s1, row[8 + tc]);
-        xmx = fmaxf(xmx, row[16 + tc]);
-        xmn = fminf(xmn, row[24 + tc]);
       }
     }
     __syncwarp();   // xpose is rewritten by the next unit
+    // the column's extremes (every lane of the group holds them)
+    float xmx = 0.0f, xmn = 0.0f;
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+      if (t == tc) {
+        xmx = (t & 1) ? bf16_hi(hx[t >> 1]) : bf16_lo(hx[t >> 1]);
+        xmn = (t & 1) ? bf16_hi(hn[t >> 1]) : bf16_lo(hn[t >> 1]);
+      }
     // the column's flag (lane L belongs to column group 2w + (L & 1) itself)
     bool cbad = false;
 #pragma unroll
@@ -514,7 +555,11 @@ __global__ void __launch_bounds__(kThreads, kSmooth ? 5 : 6) quant_kernel(QuantA
           }
           if (a.compensate) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] = __fsub_rn(x[i], m[i]);
+            for (int i = 0; i < 16; i += 2) {
+              const float2 d2 = __fadd2_rn(make_float2(x[i], x[i + 1]), make_float2(-m[i], -m[i + 1]));
+              x[i] = d2.x;
+              x[i + 1] = d2.y;
+            }
           }
           const size_t r = bh * a.Nq + blk * 128 + 8 * step + 4 * h2 + ri;  // output row
           uint2 codes;
@@ -662,12 +707,15 @@ __global__ void __launch_bounds__(kThreads, kSmooth ? 5 : 6) quant_kernel(QuantA
       uint32_t w[4];
       float xm = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) xm = fmaxf(xm, fabsf(x[i]));
+      for (int i = 0; i < 16; i += 2) xm = fmax3(xm, fabsf(x[i]), fabsf(x[i + 1]));
       if (fast && xm <= 3.40282347e38f) {
+        const float2 y2 = make_float2(ys, ys), nd2 = make_float2(-s, -s);
 #pragma unroll
-        for (int t = 0; t < 4; ++t)
-          w[t] = e4m3x4(div_rn(x[4 * t], s, ys), div_rn(x[4 * t + 1], s, ys),
-                        div_rn(x[4 * t + 2], s, ys), div_rn(x[4 * t + 3], s, ys));
+        for (int t = 0; t < 4; ++t) {
+          const float2 u0 = div_rn2(make_float2(x[4 * t], x[4 * t + 1]), nd2, y2);
+          const float2 u1 = div_rn2(make_float2(x[4 * t + 2], x[4 * t + 3]), nd2, y2);
+          w[t] = e4m3x4(u0.x, u0.y, u1.x, u1.y);
+        }
       } else {
 #pragma unroll
         for (int t = 0; t < 4; ++t)
