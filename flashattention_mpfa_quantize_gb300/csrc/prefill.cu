@@ -100,8 +100,7 @@ enum : int {
   kBarKFull0 = kBarSRead0 + kKStages,  // +K stage
   kBarVFull0 = kBarKFull0 + kKStages,  // +V stage
   kBarODone0 = kBarVFull0 + kVStages,  // +V stage: PV_g (V stage g % 3) completed
-  kBarMax0 = kBarODone0 + kVStages,    // +2*quadrant+parity: reference max handed to that parity
-  kNumBars = kBarMax0 + 8,
+  kNumBars = kBarODone0 + kVStages,
 };
 
 // shared memory layout (offsets from a 1024-byte aligned base)
@@ -120,8 +119,10 @@ constexpr uint32_t kOffOst = kOffOnes + 16384;
 constexpr uint32_t kOffQs = kOffOst + 2 * 32768;         // 2 Q buffers x 1 KB
 constexpr uint32_t kOffQbs = kOffQs + 2 * 1024;               // 2 Q buffers x 2 terms x 1 KB
 constexpr uint32_t kOffKs = kOffQbs + 2 * 2048;               // kKStages x 1 KB
-constexpr uint32_t kOffMax = kOffKs + kKStages * 1024;        // 128 floats: reference max per row
-constexpr uint32_t kOffBar = kOffMax + 512;
+// per row the reference max and the stream index of the tile it follows,
+// one 64-bit word (bits 0-31 the fp32 max, 32-63 the tile index)
+constexpr uint32_t kOffMax = kOffKs + kKStages * 1024;
+constexpr uint32_t kOffBar = kOffMax + 1024;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemUsed = kOffMisc + 64;
 // More than half an SM's shared memory, so a single CTA owns the SM and its
@@ -205,10 +206,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarVFull0 + s), 1);
       mbar_init(bar(kBarODone0 + s), 1);
     }
-    for (int i = 0; i < 8; ++i) mbar_init(bar(kBarMax0 + i), 1);
     fence_barrier_init();
   }
   if (warp == kWarpMma) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  if (threadIdx.x < 128)   // no tile index yet
+    reinterpret_cast<volatile unsigned long long*>(smem + kOffMax)[threadIdx.x] = ~0ull;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -574,13 +576,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; item_of(p, k, it); ++k) gtot += it.nkv;
     }
     // Tiles g = par, par + 2, ... of the stream; the owner of tile g hands
-    // the row's reference max to the owner of tile g+1 (bar kBarMax0 +
-    // 2*quadrant + receiving parity; one hand-over per phase, and a phase
-    // cannot run ahead because the next hand-over needs the reply).  At an
-    // item's first tile the value handed over is ignored.
-    float* mrow = reinterpret_cast<float*>(smem + kOffMax);
-    const uint32_t bar_in = bar(kBarMax0 + 2 * quad + par);
-    const uint32_t bar_out = bar(kBarMax0 + 2 * quad + (par ^ 1));
+    // the row's reference max to the owner of tile g+1 through the row's
+    // shared slot, tagged with g (the receiver polls for the tag; a slot
+    // cannot be overwritten before it is read, since the next value needs
+    // the reply).  No barrier: the value is the only thing passed, so
+    // relaxed 64-bit accesses suffice.  At an item's first tile the value
+    // handed over is ignored.
+    volatile unsigned long long* mslot =
+        reinterpret_cast<volatile unsigned long long*>(smem + kOffMax) + row;
     const float cs = __fmul_rn(__fmul_rn(*a.s_q, *a.s_k), p.log2e_rsqrt_d);
     bool ok = true;
     int g0 = 0;
@@ -632,11 +635,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  fmax3(fmax3(pm[12], pm[13], pm[14]), pm[15], -INFINITY));
         // reference max of the row after tile g-1, from that tile's owner
         if (g > 0) {
-          if (!__all_sync(0xffffffffu, mbar_wait(bar_in, ((g - 1) >> 1) & 1, a.err, abort_flag))) {
-            ok = false;
-            break;
+          // the row's slot holds tile g-1's value once its index reads g-1
+          // (one aligned 64-bit word: value and index arrive together)
+          unsigned long long v = *mslot;
+          bool got = (uint32_t)(v >> 32) == (uint32_t)(g - 1);
+          if (!__all_sync(0xffffffffu, got)) {
+            const unsigned long long t0 = globaltimer();
+            for (int it = 0; !got; ++it) {
+              v = *mslot;
+              got = (uint32_t)(v >> 32) == (uint32_t)(g - 1);
+              if (!got && (it & 63) == 63) {
+                if (*abort_flag) break;
+                if (globaltimer() - t0 > kWaitLimitNs) {
+                  record_error(a.err, kErrTimeout);
+                  *abort_flag = 1;
+                  break;
+                }
+              }
+            }
+            if (!__all_sync(0xffffffffu, got)) {
+              ok = false;
+              break;
+            }
           }
-          const float mi = mrow[row];
+          const float mi = __uint_as_float((uint32_t)v);
           if (j > 0) m = mi;
         }
         // cs > 0, so max_i(S_i * cs) == (max_i S_i) * cs exactly.  The
@@ -645,11 +667,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // are done.
         const float tmax = __fmul_rn(smax, cs);
         const float mn = (m == -INFINITY || tmax > m + kRescaleTau) ? tmax : m;
-        if (g + 1 < gtot) {
-          mrow[row] = mn;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_out);
-        }
+        if (g + 1 < gtot)
+          *mslot = ((unsigned long long)(uint32_t)g << 32) | __float_as_uint(mn);
         const float alpha = (m == -INFINITY) ? 0.0f : (mn == m ? 1.0f : ex2(m - mn));
         const float bias = kPShift - mn;  // P8 = E4M3(2^(t - m) * 2^kPShift)
         const float2 cs2 = make_float2(cs, cs), bias2 = make_float2(bias, bias);

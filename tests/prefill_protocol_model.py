@@ -16,7 +16,11 @@ random, and the model checks:
 - every read sees the version the reader expects (K_g for QK_g, the item's Q
   for its products, P_g for PV_g, O accumulated over exactly the item's
   earlier tiles for a rescale or the epilogue, the reference max of tile
-  g-1 for tile g).
+  g-1 for tile g);
+- the reference max is handed between a quadrant's two softmax warps
+  through one shared slot per row tagged with the tile index (the reader
+  polls for tag g-1), and a warp never overwrites a value the other warp
+  has not taken.
 
 Barrier phases are tracked as counts, so each wait states the phase it means
 (`phase`); the kernel passes its parity.  `drop` removes named waits, so a
@@ -64,6 +68,7 @@ class _Sim:
         self.writes = {}       # resource -> [(end, version)] of issued writes
         self.inflight = {}     # resource -> [(kind, end, who)]
         self.async_ends = {}   # issuing thread -> completion times of its async ops
+        self.tags = {}         # tagged shared slot -> tile index it holds
 
     def bar(self, name, count):
         self.bars[name] = _Bar(name, count)
@@ -118,8 +123,6 @@ def run(items, T, seed, drop=()):
     for s in range(KV):
         S.bar(("VFull", s), 1)
         S.bar(("ODone", s), 1)
-    for i in range(8):
-        S.bar(("Max", i), 1)
     starts, g = [], 0
     for (_, n) in items:
         starts.append((g, n))
@@ -130,6 +133,11 @@ def run(items, T, seed, drop=()):
         if name in drop:
             return ("step",)
         return ("wait", bar, phase)
+
+    def wait_tag(name, slot, tag):
+        if name in drop:
+            return ("step",)
+        return ("tag", slot, tag)
 
     def producer():
         def load_q(k):
@@ -303,7 +311,6 @@ def run(items, T, seed, drop=()):
         S.access(("Ones", par, quad), "W", 0, who, new="ones")
         S.bars["Ones"].arrive(32)
         yield ("step",)
-        bar_in, bar_out = ("Max", 2 * quad + par), ("Max", 2 * quad + (par ^ 1))
         for k, (g0, n) in enumerate(starts):
             qt = items[k][0]
             for j in range(0 if (g0 & 1) == par else 1, n, 2):
@@ -313,14 +320,17 @@ def run(items, T, seed, drop=()):
                 S.access(("S", bk), "R", 0, who, expect=("S", g))
                 S.bars[("SRead", g % KK)].arrive(1)
                 yield ("step",)
+                slot = ("mslot", quad)
                 if g > 0:
-                    yield wait("hand_over", bar_in, (g - 1) >> 1)
-                    if S.version.get(("mrow", quad)) != ("m", g - 1):
-                        raise ProtocolError(f"{who} tile {g} reads the max of "
-                                            f"{S.version.get(('mrow', quad))}")
+                    yield wait_tag("hand_over", slot, g - 1)
+                    if S.tags.get(slot) != g - 1:
+                        raise ProtocolError(f"{who} tile {g} reads the max of tile "
+                                            f"{S.tags.get(slot)}")
                 if g + 1 < gtot:
-                    S.version[("mrow", quad)] = ("m", g)
-                    S.bars[bar_out].arrive(1)
+                    if S.tags.get(slot) != (g - 1 if g > 0 else None):
+                        raise ProtocolError(f"{who} tile {g} overwrites the max of tile "
+                                            f"{S.tags.get(slot)} before it was taken")
+                    S.tags[slot] = g
                 yield ("step",)
                 if j > 0 and rng.random() < 0.3:   # the reference max moved: rescale O
                     yield wait("rescale_o", ("ODone", (g - 1) % KV), (g - 1) // KV)
@@ -364,6 +374,10 @@ def run(items, T, seed, drop=()):
             if w is None:
                 runnable.append(r)
                 continue
+            if w[0] == "tag":
+                if S.tags.get(w[1]) == w[2]:
+                    runnable.append(r)
+                continue
             bar, phase = w
             done = S.bars[bar].done
             if done >= phase + 2:
@@ -385,6 +399,8 @@ def run(items, T, seed, drop=()):
                 if S.bars[bar].done >= phase + 2:
                     raise ProtocolError(f"{r}: wait on {bar} phase {phase} aliased")
                 blocked[r] = (bar, phase)
+            elif act[0] == "tag":
+                blocked[r] = act
             S.t += 1
         elif S.events or any(held[r] > S.t for r in live):
             t_held = min([held[r] for r in live if held[r] > S.t], default=None)
