@@ -615,6 +615,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i)
               if (32 * c + i > row) sr[c][i] = 0xFF800000u;  // -inf
         }
+        // the partner's value, read before the max tree so the load's latency
+        // is hidden (polled again below if it was not there yet)
+        const unsigned long long v_early = *mslot;
         // tile max over the row's 128 keys (3-input max tree)
         float pm[16];
 #pragma unroll
@@ -637,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (g > 0) {
           // the row's slot holds tile g-1's value once its index reads g-1
           // (one aligned 64-bit word: value and index arrive together)
-          unsigned long long v = *mslot;
+          unsigned long long v = v_early;
           bool got = (uint32_t)(v >> 32) == (uint32_t)(g - 1);
           if (!__all_sync(0xffffffffu, got)) {
             const unsigned long long t0 = globaltimer();
