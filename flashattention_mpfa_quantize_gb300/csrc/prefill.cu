@@ -122,7 +122,11 @@ constexpr uint32_t kOffKs = kOffQbs + 2 * 2048;               // kKStages x 1 KB
 // per row the reference max and the stream index of the tile it follows,
 // one 64-bit word (bits 0-31 the fp32 max, 32-63 the tile index)
 constexpr uint32_t kOffMax = kOffKs + kKStages * 1024;
-constexpr uint32_t kOffBar = kOffMax + 1024;
+// per QK issuer, the last stream tile of an item whose products it has seen
+// complete (a counter: the copier of the next item polls it instead of a
+// barrier phase that could be two completions behind)
+constexpr uint32_t kOffQkDone = kOffMax + 1024;
+constexpr uint32_t kOffBar = kOffQkDone + 64;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemUsed = kOffMisc + 64;
 // More than half an SM's shared memory, so a single CTA owns the SM and its
@@ -158,6 +162,31 @@ __device__ __forceinline__ bool item_of(const Params& p, int k, Item& it) {
   it.bh = i % bh_count;
   it.nkv = p.a.causal ? it.qt + 1 : p.q_tiles;
   return true;
+}
+
+__device__ __forceinline__ int ld_acquire_s32(const int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_s32(int* p, int v) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+// Bounded per-thread poll until *p >= want (false on timeout or abort).
+__device__ __forceinline__ bool poll_ge(const int* p, int want, int* err, volatile int* abort) {
+  if (ld_acquire_s32(p) >= want) return true;
+  const unsigned long long t0 = globaltimer();
+  for (int it = 0;; ++it) {
+    if (ld_acquire_s32(p) >= want) return true;
+    if ((it & 63) == 63) {
+      if (*abort) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        record_error(err, kErrTimeout);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -211,6 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpMma) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   if (threadIdx.x < 128)   // no tile index yet
     reinterpret_cast<volatile unsigned long long*>(smem + kOffMax)[threadIdx.x] = ~0ull;
+  int* qk_done = reinterpret_cast<int*>(smem + kOffQkDone);
+  if (threadIdx.x < 2) qk_done[threadIdx.x] = -1;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -479,11 +510,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (copier) {
           // the item's Q is in buffer buf, and every score product reading
           // the TMEM Q scales of the previous item has completed: the other
-          // thread's QK_{g0-1} (its bank's next commit needs these scales)
-          // and this thread's QK_{g0-2} (waited for through S_{g0-2})
+          // thread's QK_{g0-1} (its bank's next commit needs these scales;
+          // the other thread says so through its counter) and this thread's
+          // QK_{g0-2} (waited for through S_{g0-2})
           ok = mbar_wait_w(bar(kBarQFull0 + buf), (k >> 1) & 1, abort_flag) &&
-               (g0 < 1 || mbar_wait_w(bar(kBarSFull0 + ((g0 - 1) & 1)), ((g0 - 1) >> 1) & 1,
-                                      abort_flag)) &&
+               (g0 < 1 ||
+                __all_sync(0xffffffffu, poll_ge(qk_done + (par ^ 1), g0 - 1, a.err, abort_flag))) &&
                wait_sread(g0);
           if (!ok) break;
           tc_fence_after();
@@ -506,6 +538,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int g = g0 + (copier ? 2 : 1); ok && g < g0 + n; g += 2) {
           if (!wait_sread(g) || !issue_qk(g, buf)) ok = false;
+        }
+        // the last tile this thread issued in the item: once its products
+        // have landed, say so to the other thread.  Its own latest phase
+        // cannot be two behind: that tile was issued after S of its tile
+        // two back had been read.
+        const int last = ((g0 + n - 1) & 1) == par ? g0 + n - 1 : g0 + n - 2;
+        if (ok && last >= g0) {
+          ok = mbar_wait_w(bar(kBarSFull0 + par), (last >> 1) & 1, abort_flag);
+          if (ok && lane == 0) st_release_s32(qk_done + par, last);
+          __syncwarp();
         }
         // this thread's products of item k done with Q buffer buf
         tc_commit_w(bar(kBarQEmpty0 + buf));

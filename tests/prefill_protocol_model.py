@@ -10,8 +10,9 @@ copies and MMAs complete after random latencies and the roles interleave at
 random, and the model checks:
 
 - every wait eventually passes (no deadlock);
-- a wait never runs on a phase that the barrier has already left twice
-  (mbarrier parity waits cannot tell phase p from phase p + 2);
+- a wait never runs on a phase that the barrier has already left twice, nor
+  while the barrier is still two or more phases short of it (a parity wait
+  cannot tell phase p from p + 2, nor from p - 2: it would pass at once);
 - no buffer is read or written while a conflicting write is in flight;
 - every read sees the version the reader expects (K_g for QK_g, the item's Q
   for its products, P_g for PV_g, O accumulated over exactly the item's
@@ -23,7 +24,8 @@ random, and the model checks:
   has not taken.
 
 Barrier phases are tracked as counts, so each wait states the phase it means
-(`phase`); the kernel passes its parity.  `drop` removes named waits, so a
+(`phase`); the kernel passes its parity.  A thread's tensor-core commits
+arrive in the order it issued them.  `drop` removes named waits, so a
 test can check that each of them is needed.
 """
 import random
@@ -69,6 +71,7 @@ class _Sim:
         self.inflight = {}     # resource -> [(kind, end, who)]
         self.async_ends = {}   # issuing thread -> completion times of its async ops
         self.tags = {}         # tagged shared slot -> tile index it holds
+        self.last_commit = {}  # issuing thread -> time its latest commit arrives
 
     def bar(self, name, count):
         self.bars[name] = _Bar(name, count)
@@ -99,8 +102,11 @@ class _Sim:
         self.async_ends.setdefault(who, []).append(end)
 
     def commit(self, who, bar):
-        # arrives once every earlier asynchronous op of this thread completed
+        # arrives once every earlier asynchronous op of this thread completed,
+        # and after this thread's earlier commits (they signal in order)
         end = max(self.async_ends.get(who, []) + [self.t]) + self.rng.randint(1, 30)
+        end = max(end, self.last_commit.get(who, 0) + 1)
+        self.last_commit[who] = end
         self.events.append((end, lambda: self.bars[bar].arrive()))
 
 
@@ -138,6 +144,11 @@ def run(items, T, seed, drop=()):
         if name in drop:
             return ("step",)
         return ("tag", slot, tag)
+
+    def wait_ge(name, slot, tag):
+        if name in drop:
+            return ("step",)
+        return ("ge", slot, tag)
 
     def producer():
         def load_q(k):
@@ -190,6 +201,9 @@ def run(items, T, seed, drop=()):
             done = S.bars[bar].done
             if done >= phase + 2:
                 raise ProtocolError(f"producer: test on {bar} phase {phase} aliased")
+            if done < phase and (phase - done) % 2 == 1:
+                raise ProtocolError(f"producer: test on {bar} phase {phase} would pass two "
+                                    f"phases early (done {done})")
             return done >= phase + 1
 
         def issue_k(g):
@@ -254,7 +268,9 @@ def run(items, T, seed, drop=()):
             if copier:
                 yield wait("q_full", ("QFull", buf), k >> 1)
                 if g0 >= 1:
-                    yield wait("prev_item_qk", ("SFull", (g0 - 1) & 1), (g0 - 1) >> 1)
+                    # the other issuer's products up to tile g0-1 (the last
+                    # of the previous item on its bank) have completed
+                    yield wait_ge("prev_item_qk", ("qkdone", par ^ 1), g0 - 1)
                 if g0 >= 2:
                     yield wait("s_read", ("SRead", (g0 - 2) % KK), (g0 - 2) // KK)
                 e = S.access(("SfQ",), "W", S.lat(), who, new=("SfQ", k))
@@ -273,6 +289,13 @@ def run(items, T, seed, drop=()):
                 if g >= 2:
                     yield wait("s_read", ("SRead", (g - 2) % KK), (g - 2) // KK)
                 yield from issue_qk(g, buf, k)
+            # the last tile this thread issued in the item: once its products
+            # have landed (its own latest phase), say so to the other thread
+            mine = [g for g in range(g0, g0 + n) if (g & 1) == par]
+            if mine:
+                last = mine[-1]
+                yield wait("qk_own", ("SFull", last & 1), last >> 1)
+                S.tags[("qkdone", par)] = last
             S.commit(who, ("QEmpty", buf))
 
     def pv():
@@ -378,10 +401,17 @@ def run(items, T, seed, drop=()):
                 if S.tags.get(w[1]) == w[2]:
                     runnable.append(r)
                 continue
+            if w[0] == "ge":
+                if S.tags.get(w[1], -1) >= w[2]:
+                    runnable.append(r)
+                continue
             bar, phase = w
             done = S.bars[bar].done
             if done >= phase + 2:
                 raise ProtocolError(f"{r}: wait on {bar} phase {phase} aliased (done {done})")
+            if done < phase and (phase - done) % 2 == 1:
+                raise ProtocolError(f"{r}: wait on {bar} phase {phase} would pass two phases "
+                                    f"early (done {done})")
             if done == phase + 1:
                 runnable.append(r)
         if runnable and (not S.events or rng.random() < 0.7):
@@ -398,8 +428,12 @@ def run(items, T, seed, drop=()):
                 bar, phase = act[1], act[2]
                 if S.bars[bar].done >= phase + 2:
                     raise ProtocolError(f"{r}: wait on {bar} phase {phase} aliased")
+                d0 = S.bars[bar].done
+                if d0 < phase and (phase - d0) % 2 == 1:
+                    raise ProtocolError(f"{r}: wait on {bar} phase {phase} would pass two phases "
+                                        f"early (done {d0})")
                 blocked[r] = (bar, phase)
-            elif act[0] == "tag":
+            elif act[0] in ("tag", "ge"):
                 blocked[r] = act
             S.t += 1
         elif S.events or any(held[r] > S.t for r in live):

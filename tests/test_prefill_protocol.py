@@ -31,7 +31,7 @@ def test_protocol_edge_streams():
 @pytest.mark.parametrize("name", ["q_full", "q_empty", "prev_item_qk", "q_sf", "ones",
                                   "o_free", "hand_over", "epilogue", "p_bank", "rescale_o",
                                   "s_read", "k_full", "k_ring", "v_full", "v_ring", "s_full",
-                                  "p_ready"])
+                                  "p_ready", "qk_own"])
 def test_each_wait_is_needed(name):
     for items, T, seed in _cases(400, 2):
         try:
