@@ -2,7 +2,7 @@
 
 Each ``csrc/*.cu`` translation unit compiles in parallel; the objects link
 into ``flashattention_mpfa_quantize_gb300/libmpfa.so``.  The CUDA runtime is
-linked statically; the driver's tensor-map encoder is looked up at run time,
+linked statically; the CUDA driver's tensor-map encoder is looked up at run time,
 so the library needs no ``-lcuda``.
 """
 from __future__ import annotations

@@ -9,7 +9,7 @@
 
 namespace mpfa {
 
-// The driver's encoder, looked up once (function-local static: thread-safe
+// The CUDA driver's encoder, looked up once (function-local static: thread-safe
 // initialization).
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() {
