@@ -331,6 +331,19 @@ def quantize_v(V: np.ndarray) -> dict:
     return dict(vc=vc, s_v=s)
 
 
+def quantize_v_fp4(V: np.ndarray) -> dict:
+    """V [B, N, Hkv, d] fp32 for the full-FP4 PV ablation: NVFP4 of V^T along
+    the keys (the reduction dimension of P V), 16-key blocks, one tensor
+    scale s_v = fp32(amax(V) / 2688).  Codes [B, Hkv, d, N/2], block scales
+    [B, Hkv, d, N/16] (E4M3 bytes), logical row-major."""
+    B, N, H, d = V.shape
+    s = tensor_scale(_amax(V), NVFP4_QMAX)
+    vt = np.ascontiguousarray(np.transpose(V, (0, 2, 3, 1))).reshape(B * H * d, N)
+    codes, scales = nvfp4_quantize(vt, s)
+    return {"vc4": codes.reshape(B, H, d, N // 2), "vs4": scales.reshape(B, H, d, N // 16),
+            "s_v": s}
+
+
 def quantize_q_decode(q: np.ndarray, Hkv: int, compensate: bool, T: int = 2) -> dict:
     """Decode query q [B, Hq, d]: the rank-one block is the g = Hq/Hkv query
     heads that share one KV head.  Returns qc [B,Hq,d/2], qs [B,Hq,d/16],
@@ -367,8 +380,10 @@ def attn_online(q, qadd, k, v, *, score_scale, out_scale, causal, kv_len=None, c
                 round_p=True, p_shift=P_SHIFT, tau=RESCALE_TAU, rows=None, nthreads=0):
     """Tiled online-softmax attention of one head (see orc_attn_online).
     q, qadd [nq,d] fp64 (qadd may be None), k, v [nk,d] fp64.  P is stored as
-    E4M3(2^p_shift p); the row's reference max moves only when a tile's max
-    exceeds it by more than tau (tau = 0: the exact running max)."""
+    E4M3(2^p_shift p) (round_p 1 or True), left unrounded (0 or False), or in
+    NVFP4 per 16-key block (2, the full-FP4 ablation); the row's reference
+    max moves only when a tile's max exceeds it by more than tau (tau = 0:
+    the exact running max)."""
     q = np.ascontiguousarray(q, np.float64)
     k = np.ascontiguousarray(k, np.float64)
     v = np.ascontiguousarray(v, np.float64)
@@ -380,7 +395,7 @@ def attn_online(q, qadd, k, v, *, score_scale, out_scale, causal, kv_len=None, c
     lse = np.empty(rows.size, np.float64)
     _L().orc_attn_online(_p(q), None if qa is None else _p(qa), _p(k), _p(v), nq, nk, d,
                          float(score_scale), float(out_scale), int(bool(causal)),
-                         nk if kv_len is None else int(kv_len), int(chunk), int(bool(round_p)),
+                         nk if kv_len is None else int(kv_len), int(chunk), int(round_p),
                          float(p_shift), float(tau), _p(rows), rows.size, _p(o), _p(lse), nthreads)
     return o, lse
 
@@ -421,7 +436,7 @@ def _head_operands(qz, kz, vz, b, h, g):
         qb = _terms_sum(qz["qbc"][b, h], qz["qbs"][b, h])           # [nblocks, d]
         qadd = np.repeat(qb, QBLOCK, axis=0)[: q.shape[0]]
     k = nvfp4_dequant(kz["kc"][b, hk], kz["ks"][b, hk])
-    v = fp8_dequant(vz["vc"][b, hk])
+    v = None if vz is None else fp8_dequant(vz["vc"][b, hk])
     return q, qadd, k, v
 
 
@@ -457,8 +472,10 @@ def lse_shift(qz, kz, b, h, g, d=D):
 def prefill_emulate(qz, kz, vz, *, causal, heads=None, rows=None, nthreads=0):
     """Emulate the QK4PV8 prefill on the oracle's own codes.
 
-    qz/kz/vz from quantize_q_prefill / quantize_k / quantize_v.  heads: list
-    of (b, h) (default all); rows: query rows per head (default all).
+    qz/kz/vz from quantize_q_prefill / quantize_k / quantize_v, or vz from
+    quantize_v_fp4 for the full-FP4 PV ablation (P in NVFP4 per 16-key
+    block, V^T in NVFP4 along the keys).  heads: list of (b, h) (default
+    all); rows: query rows per head (default all).
     Returns {(b, h): (o fp64 [nrows, d] before the bf16 cast, lse [nrows])}."""
     B, Hq, N = qz["qc"].shape[:3]
     Hkv = kz["kc"].shape[1]
@@ -466,10 +483,16 @@ def prefill_emulate(qz, kz, vz, *, causal, heads=None, rows=None, nthreads=0):
     cs = score_scale_log2(qz["s_q"], kz["s_k"])
     heads = [(b, h) for b in range(B) for h in range(Hq)] if heads is None else heads
     out = {}
+    fp4 = "vc4" in vz
     for (b, h) in heads:
-        q, qadd, k, v = _head_operands(qz, kz, vz, b, h, g)
+        if fp4:
+            q, qadd, k, _ = _head_operands(qz, kz, None, b, h, g)
+            v = nvfp4_dequant(vz["vc4"][b, h // g], vz["vs4"][b, h // g]).T
+        else:
+            q, qadd, k, v = _head_operands(qz, kz, vz, b, h, g)
         o, lse = attn_online(q, qadd, k, v, score_scale=cs, out_scale=float(vz["s_v"]),
-                             causal=causal, rows=rows, nthreads=nthreads)
+                             causal=causal, round_p=2 if fp4 else 1, rows=rows,
+                             nthreads=nthreads)
         if kz.get("kbar") is not None:
             sh = lse_shift(qz, kz, b, h, g)
             lse = lse + (sh if rows is None else sh[np.asarray(rows)])

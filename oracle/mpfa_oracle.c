@@ -327,7 +327,15 @@ void orc_block_mean(const float *x, int g, int64_t ld, int d, float *qbar, float
  *   visited in tiles of 128 keys in ascending order with its own reference
  *   max m and sum l.  Per tile, with M = max_j t_ij:
  *        m' = M if m = -inf or M > m + tau, else m;  alpha = 2^(m - m')
- *        p_ij = 2^(t_ij - m'),  P_ij = round_p ? E4M3(2^s p_ij) : 2^s p_ij
+ *        p_ij = 2^(t_ij - m'), and with x_ij = 2^s p_ij
+ *          round_p = 0: P_ij = x_ij
+ *          round_p = 1: P_ij = E4M3(x_ij)                (the method: FP8 P)
+ *          round_p = 2: P_ij = NVFP4 of x_ij in fp32 (full-FP4 ablation):
+ *            per block of 16 keys (key index / 16, so blocks never straddle
+ *            a 128-key tile) the quantizer rule with tensor scale
+ *            s_p = fp32(2^(s + tau) / 2688), the largest x a tile can
+ *            produce mapped to 6 * 448; P_ij = code value * fp32(sb * s_p);
+ *            masked keys count as 0
  *        l = alpha l + sum_j P_ij,  acc = alpha acc + sum_j P_ij v_j
  *   (tau = 0 is the FlashAttention-2 running max.)
  *   Chunk result: o_s = out_scale * acc / l, lse_s = ln2 (m + log2(l) - s).
@@ -393,10 +401,35 @@ static void orc_attn_row(int64_t ri, void *vctx)
             l *= alpha;
             for (int x = 0; x < d; x++)
                 acc[x] *= alpha;
+            double pt[128];
             for (int64_t j = ts; j < te; j++) {
                 double p = exp2(t[j - ts] - mn + c->p_shift);
-                if (c->round_p)
+                if (c->round_p == 1)
                     p = orc_e4m3_value(orc_e4m3_encode(p));
+                pt[j - ts] = p;
+            }
+            if (c->round_p == 2) {
+                /* NVFP4 per 16-key block of the tile, in fp32 */
+                const float s_p = (float)(exp2(c->p_shift + c->tau) / 2688.0);
+                for (int64_t b0 = ts; b0 < te; b0 += 16) {
+                    int64_t b1 = b0 + 16 < te ? b0 + 16 : te;
+                    float xb[16], bamax = 0.0f;
+                    for (int64_t j = b0; j < b1; j++) {
+                        xb[j - b0] = (float)pt[j - ts];
+                        if (xb[j - b0] > bamax)
+                            bamax = xb[j - b0];
+                    }
+                    int sb = orc_e4m3_encode((double)(bamax / (6.0f * s_p)));
+                    float denom = (float)orc_e4m3_value(sb) * s_p;
+                    for (int64_t j = b0; j < b1; j++)
+                        pt[j - ts] = sb == 0 ? 0.0
+                                             : orc_e2m1_value(orc_e2m1_encode(
+                                                   (double)(xb[j - b0] / denom))) *
+                                                   (double)denom;
+                }
+            }
+            for (int64_t j = ts; j < te; j++) {
+                double p = pt[j - ts];
                 l += p;
                 const double *vj = c->v + j * d;
                 for (int x = 0; x < d; x++)

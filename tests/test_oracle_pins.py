@@ -750,3 +750,134 @@ def test_k_smoothing_reduces_error_on_key_offsets():
             o = orc.prefill_emulate(qz, orc.quantize_k(Kn, smooth=sm), vz, causal=False)[(0, 0)][0]
             e[sm] = _rel_l2(o, ex)
         assert e[True] < 0.85 * e[False], (comp, e)
+
+
+# --------------------------------------------------------------------------
+# full-FP4 PV ablation (P and V^T in NVFP4)
+# --------------------------------------------------------------------------
+
+def _nvfp4_p_direct(x, s_p):
+    """P in NVFP4 written out independently: per 16 values the E4M3 block
+    scale (torch's cast) of fp32(max / fp32(6 s_p)), the fp32 divisor
+    fp32(sb * s_p), E2M1 by the rint grid; returns the dequantized values."""
+    x = np.asarray(x, np.float32)
+    out = np.zeros(x.shape, np.float64)
+    six_s = np.float32(np.float32(6.0) * np.float32(s_p))
+    for b0 in range(0, x.shape[-1], 16):
+        blk = x[..., b0:b0 + 16]
+        bamax = blk.max(axis=-1, keepdims=True)
+        sb = _e4m3(np.float32(bamax / six_s))
+        denom = (sb.astype(np.float32) * np.float32(s_p)).astype(np.float32)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            y = np.where(sb > 0, (blk / denom).astype(np.float32), 0.0)
+        out[..., b0:b0 + 16] = _rne_grid_e2m1(y) * denom.astype(np.float64)
+    return out
+
+
+@pytest.mark.parametrize("n", [16, 100, 128])
+def test_single_tile_fp4_p_direct_formula(n):
+    """One KV tile with P in NVFP4 (round_p = 2): x = fp32(2^4 2^(t - max t)),
+    P = NVFP4(x) with s_p = fp32(2^(4 + tau) / 2688) written out with torch's
+    e4m3 cast and the rint E2M1 grid; O = sum P v / sum P,
+    LSE = ln2 (max t + log2 sum P - 4)."""
+    q, k, v = _rand_qkv(n, seed=400 + n, scale=1.3)
+    o1, l1 = orc.attn_online(q, None, k, v, score_scale=LOG2E_RSQRT_D, out_scale=1.0,
+                             causal=False, round_p=2)
+    t = (q @ k.T) * LOG2E_RSQRT_D
+    m = t.max(axis=1, keepdims=True)
+    x = (np.exp2(t - m + P_SHIFT_READING)).astype(np.float32)
+    pad = (-n) % 16
+    xp = np.pad(x, ((0, 0), (0, pad)))
+    s_p = np.float32(2.0 ** (P_SHIFT_READING + TAU_READING) / 2688.0)
+    p4 = _nvfp4_p_direct(xp, s_p)[:, :n]
+    o2 = (p4 @ v) / p4.sum(axis=1, keepdims=True)
+    l2 = math.log(2) * (m[:, 0] + np.log2(p4.sum(axis=1)) - P_SHIFT_READING)
+    np.testing.assert_allclose(o1, o2, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, atol=1e-12)
+
+
+def test_fp4_v_quantizer_is_nvfp4_of_v_transposed():
+    """quantize_v_fp4 codes the keys of each (b, KV head, channel) row with
+    the pinned NVFP4 quantizer at s_v = fp32(amax(V) / 2688)."""
+    rng = np.random.default_rng(5)
+    V = (rng.standard_normal((2, 256, 2, 128)) * np.exp(rng.uniform(-2, 2, (1, 256, 1, 1)))).astype(np.float32)
+    vz = orc.quantize_v_fp4(V)
+    assert vz["s_v"] == np.float32(np.float32(np.abs(V).max()) / np.float32(2688.0))
+    for b in range(2):
+        for h in range(2):
+            c, sc = orc.nvfp4_quantize(np.ascontiguousarray(V[b, :, h, :].T), vz["s_v"])
+            np.testing.assert_array_equal(vz["vc4"][b, h], c)
+            np.testing.assert_array_equal(vz["vs4"][b, h], sc)
+
+
+def test_fp4_pv_constant_v_gives_constant_o():
+    """With V constant, every V^T code and block scale are equal, so the
+    full-FP4 emulation's O is that one dequantized value on every row,
+    causal, over several tiles: the same P codes enter l and PV."""
+    B, N, Hq, Hkv = 1, 384, 2, 1
+    rng = np.random.default_rng(6)
+    Q = rng.standard_normal((B, N, Hq, 128)).astype(np.float32)
+    K = rng.standard_normal((B, N, Hkv, 128)).astype(np.float32)
+    V = np.full((B, N, Hkv, 128), 0.75, np.float32)
+    qz, kz = orc.quantize_q_prefill(Q, True, 2), orc.quantize_k(K)
+    vz = orc.quantize_v_fp4(V)
+    val = orc.nvfp4_dequant(vz["vc4"][0, 0], vz["vs4"][0, 0]) * np.float64(vz["s_v"])
+    assert np.all(val == val.flat[0])
+    em = orc.prefill_emulate(qz, kz, vz, causal=True)
+    for key, (o, _) in em.items():
+        # exact up to the fp64 rounding of sum P v against v sum P
+        np.testing.assert_allclose(o, np.full_like(o, val.flat[0]), rtol=1e-14, atol=0)
+
+
+def test_fp4_pv_uniform_scores_average_v():
+    """Q = 0: every visible score is 0, so every P code is the same and O is
+    the plain mean of the visible rows of the dequantized V^T (closed form);
+    LSE = ln(visible keys) up to the rounding of P (x = 16 maps to code 6 of
+    a block scale 28)."""
+    B, N, Hkv = 1, 256, 1
+    rng = np.random.default_rng(7)
+    Q = np.zeros((B, N, 1, 128), np.float32)
+    K = rng.standard_normal((B, N, Hkv, 128)).astype(np.float32)
+    V = rng.standard_normal((B, N, Hkv, 128)).astype(np.float32)
+    qz, kz = orc.quantize_q_prefill(Q, False, 2), orc.quantize_k(K)
+    vz = orc.quantize_v_fp4(V)
+    vd = (orc.nvfp4_dequant(vz["vc4"][0, 0], vz["vs4"][0, 0]) * np.float64(vz["s_v"])).T
+    (o, lse), = orc.prefill_emulate(qz, kz, vz, causal=True).values()
+    want = np.cumsum(vd, axis=0) / np.arange(1, N + 1)[:, None]
+    np.testing.assert_allclose(o, want, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, np.log(np.arange(1, N + 1)), atol=1e-6)
+
+
+@pytest.mark.parametrize("delta", [2.5, 3.9, 4.5])
+def test_two_tile_fp4_p_reference_max(delta):
+    """Two KV tiles with P in NVFP4: while tile 1's max stays within tau of
+    tile 0's, x reaches 2^(4 + delta) under the stale reference and the
+    tensor scale s_p = 2^(4 + tau) / 2688 keeps the block scales unsaturated
+    (a smaller s_p would clip them at 448); past tau the reference moves and
+    tile 0 is rescaled by 2^-delta.  Direct formula as in the one-tile pin."""
+    rng = np.random.default_rng(int(delta * 10) + 90)
+    t0 = rng.uniform(-6, 0, 128)
+    t0[5] = 0.0
+    t1 = rng.uniform(-6, 0, 128) + delta
+    t1[77] = delta
+    tt = np.concatenate([t0, t1])
+    q = np.zeros((1, 128)); q[0, 0] = 1.0
+    k = np.zeros((256, 128)); k[:, 0] = tt
+    v = rng.standard_normal((256, 128))
+    o1, l1 = orc.attn_online(q, None, k, v, score_scale=1.0, out_scale=1.0, causal=False,
+                             round_p=2)
+    s_p = np.float32(2.0 ** (P_SHIFT_READING + TAU_READING) / 2688.0)
+    sh = 2.0 ** P_SHIFT_READING
+    if delta <= TAU_READING:
+        p4 = _nvfp4_p_direct((np.exp2(tt) * sh).astype(np.float32)[None], s_p)[0]
+        o2 = p4 @ v / p4.sum()
+        l2 = math.log(2) * (math.log2(p4.sum()) - P_SHIFT_READING)
+        assert p4[128:].max() > sh                 # beyond a fresh maximum's 16
+    else:
+        p0 = _nvfp4_p_direct((np.exp2(t0) * sh).astype(np.float32)[None], s_p)[0]
+        p1 = _nvfp4_p_direct((np.exp2(t1 - delta) * sh).astype(np.float32)[None], s_p)[0]
+        alpha = 2.0 ** -delta
+        o2 = (alpha * (p0 @ v[:128]) + p1 @ v[128:]) / (alpha * p0.sum() + p1.sum())
+        l2 = math.log(2) * (delta + math.log2(alpha * p0.sum() + p1.sum()) - P_SHIFT_READING)
+    np.testing.assert_allclose(o1[0], o2, rtol=1e-12, atol=1e-13)
+    assert abs(l1[0] - l2) < 1e-12
