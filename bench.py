@@ -417,6 +417,8 @@ def run_gpu(args):
         roofline["compensation"] = compensation_cost(mp, cfg, Q, K, V, flush, stream, few)
         extra["bf16_sdpa"] = bf16_sdpa_baseline(Q, K, V, cfg, flush, stream, few, flops,
                                                 step_ms, pre_ms)
+        extra["pv_fp4_ablation"] = pv_fp4_ablation(mp, cfg, Q, K, V, flush, stream,
+                                                   max(2, min(args.steps, 3)))
         e2e = run_e2e(mp, dev, stream, cfg, Q, K, V, max(3, min(args.steps, 20)))
         launches += 3 * max(3, min(args.steps, 20)) + 6
     else:
@@ -539,6 +541,78 @@ def compensation_cost(mp, cfg, Q, K, V, flush, stream, steps):
         out[f"prefill_overhead_pct_{k}"] = 100.0 * (out[f"prefill_ms_{k}"] / p_off - 1.0)
         out[f"step_overhead_pct_{k}"] = 100.0 * ((out[f"quantize_ms_{k}"] + out[f"prefill_ms_{k}"])
                                                  / (q_off + p_off) - 1.0)
+    return out
+
+
+def pv_fp4_ablation(mp, cfg, Q, K, V, flush, stream, steps):
+    """The MpFA abstract's trade-off measured: the method's FP8 PV step
+    (quantize Q, K, V + prefill) against the full-FP4 PV step (quantize Q, K;
+    V^T in NVFP4; the FP4-PV prefill kernel), timed in interleaved rounds with
+    CUDA events, L2 flushed before each; and both outputs' rel-L2 against
+    torch's bf16 attention on four query heads (context for the accuracy
+    side; the parity tests check each kernel against the oracle)."""
+    z8 = mp.quantize_qkv(Q, K, V, compensate=True, T=T_TERMS)
+    z4 = mp.quantize_qkv(Q, K, None, compensate=True, T=T_TERMS)
+    vt = mp.quantize_v_fp4(V)
+    o8, l8 = mp.prefill(z8, causal=cfg.causal)
+    o4, l4 = mp.prefill_fp4pv(z4, vt, causal=cfg.causal)
+    ws8, ws4, wsv = z8["_workspace"], z4["_workspace"], vt["_workspace"]
+
+    def step8():
+        z = mp.quantize_qkv(Q, K, V, compensate=True, T=T_TERMS, workspace=ws8)
+        mp.prefill(z, causal=cfg.causal, out=o8, lse=l8)
+
+    def step4():
+        z = mp.quantize_qkv(Q, K, None, compensate=True, T=T_TERMS, workspace=ws4)
+        v4 = mp.quantize_v_fp4(V, workspace=wsv)
+        mp.prefill_fp4pv(z, v4, causal=cfg.causal, out=o4, lse=l4)
+
+    def kern8():
+        mp.prefill(z8, causal=cfg.causal, out=o8, lse=l8)
+
+    def kern4():
+        mp.prefill_fp4pv(z4, vt, causal=cfg.causal, out=o4, lse=l4)
+
+    fns = {"step_pv8": step8, "step_pv4": step4, "prefill_pv8": kern8, "prefill_pv4": kern4}
+    for f in fns.values():
+        for _ in range(2):
+            flush.zero_()
+            f()
+    torch.cuda.synchronize()
+    acc = {k: [] for k in fns}
+    for _ in range(steps):
+        for k, f in fns.items():
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            f()
+            b.record(stream)
+            b.synchronize()
+            acc[k].append(a.elapsed_time(b))
+    if mp.get_error() != 0:
+        raise RuntimeError("device status word set in the PV precision ablation")
+    out = {"rounds": steps}
+    for k in fns:
+        out[f"{k}_ms"] = statistics.mean(acc[k])
+    out["prefill_ratio_pv4_over_pv8"] = out["prefill_pv4_ms"] / out["prefill_pv8_ms"]
+    out["step_ratio_pv4_over_pv8"] = out["step_pv4_ms"] / out["step_pv8_ms"]
+    q, k, v = (t.transpose(1, 2) for t in (Q, K, V))
+    g = cfg.Hq // cfg.Hkv
+    heads = list(range(0, cfg.Hq, max(1, cfg.Hq // 4)))[:4]
+    num8 = num4 = den = 0.0
+    for h in heads:
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q[:, h:h + 1].contiguous(), k[:, h // g:h // g + 1].contiguous(),
+            v[:, h // g:h // g + 1].contiguous(), is_causal=cfg.causal).float()[:, 0]
+        num8 += (o8[:, :, h].float() - ref).pow(2).sum().item()
+        num4 += (o4[:, :, h].float() - ref).pow(2).sum().item()
+        den += ref.pow(2).sum().item()
+        del ref
+    out["heads"] = heads
+    out["rel_l2_vs_bf16_sdpa_pv8"] = (num8 / den) ** 0.5
+    out["rel_l2_vs_bf16_sdpa_pv4"] = (num4 / den) ** 0.5
+    del z8, z4, vt, o8, o4, l8, l4
+    torch.cuda.empty_cache()
     return out
 
 

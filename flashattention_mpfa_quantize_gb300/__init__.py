@@ -77,6 +77,12 @@ _lib.mpfa_prefill.restype = _I
 _lib.mpfa_prefill.argtypes = [ctypes.POINTER(NVFP4), ctypes.POINTER(Rank1),
                               ctypes.POINTER(NVFP4), ctypes.POINTER(FP8), _I, _I, _I, _I, _I,
                               _I, _I, _I, _P, _P, _P, _P]
+_lib.mpfa_quantize_v_fp4.restype = _I
+_lib.mpfa_quantize_v_fp4.argtypes = [_P, _I, _I, _I, _I, ctypes.POINTER(NVFP4), _P, _SZ, _P]
+_lib.mpfa_prefill_fp4pv.restype = _I
+_lib.mpfa_prefill_fp4pv.argtypes = [ctypes.POINTER(NVFP4), ctypes.POINTER(Rank1),
+                                    ctypes.POINTER(NVFP4), ctypes.POINTER(NVFP4), _I, _I, _I, _I,
+                                    _I, _I, _I, _I, _P, _P, _P]
 _lib.mpfa_decode_workspace_size.restype = _SZ
 _lib.mpfa_decode_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I]
 _lib.mpfa_decode.restype = _I
@@ -221,6 +227,48 @@ def prefill(qz, *, causal, out=None, lse=None, want_lse=True):
                            int(comp), int(qz["T"]), _ptr(out), _ptr(lse),
                            _ptr(qz.get("lse_shift")), _stream(dev))
     _check(st, "mpfa_prefill")
+    return out, lse
+
+
+def quantize_v_fp4(v, *, workspace=None):
+    """Full-FP4 PV ablation: V^T of bf16 v [B,Nk,Hkv,128] in NVFP4 along the
+    keys.  Returns dict(codes u8 [B,Hkv,128,Nk/2], scales u8 (one 1 KB tile
+    per 128-key tile), scale f32[1])."""
+    assert v.dtype == torch.bfloat16 and v.is_contiguous() and v.shape[-1] == D
+    B, Nk, Hkv = v.shape[0], v.shape[1], v.shape[2]
+    dev = v.device
+    out = dict(codes=torch.empty(B, Hkv, D, Nk // 2, dtype=torch.uint8, device=dev),
+               scales=torch.empty(B * Hkv * (Nk // 128) * 1024, dtype=torch.uint8, device=dev),
+               scale=torch.empty(1, dtype=torch.float32, device=dev))
+    if workspace is None or workspace.numel() < 256:
+        workspace = torch.empty(256, dtype=torch.uint8, device=dev)
+    vt = _nvfp4(out)
+    st = _lib.mpfa_quantize_v_fp4(_ptr(v), B, Nk, Hkv, D, ctypes.byref(vt), _ptr(workspace),
+                                  workspace.numel(), _stream(dev))
+    _check(st, "mpfa_quantize_v_fp4")
+    out["_workspace"] = workspace
+    return out
+
+
+def prefill_fp4pv(qz, vt, *, causal, out=None, lse=None, want_lse=True):
+    """The prefill with the full-FP4 PV of the ablation: q, k (and qbar) from
+    quantize_qkv, vt from quantize_v_fp4.  Returns (o, lse) as prefill."""
+    B, N, Hq, Hkv = qz["B"], qz["Nq"], qz["Hq"], qz["Hkv"]
+    assert qz["Nk"] == N, "prefill takes N_q == N_k"
+    assert qz.get("lse_shift") is None, "the full-FP4 PV kernel takes no key-side smoothing"
+    dev = qz["q"]["codes"].device
+    if out is None:
+        out = torch.empty(B, N, Hq, D, dtype=torch.bfloat16, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty(B, Hq, N, dtype=torch.float32, device=dev)
+    qs, ks, vs = _nvfp4(qz["q"]), _nvfp4(qz["k"]), _nvfp4(vt)
+    comp = qz["compensate"]
+    rb = Rank1(qz["qbar"]["codes"].data_ptr(), qz["qbar"]["scales"].data_ptr()) if comp else None
+    st = _lib.mpfa_prefill_fp4pv(ctypes.byref(qs), ctypes.byref(rb) if rb is not None else None,
+                                 ctypes.byref(ks), ctypes.byref(vs), B, N, Hq, Hkv, D,
+                                 int(bool(causal)), int(comp), int(qz["T"]), _ptr(out), _ptr(lse),
+                                 _stream(dev))
+    _check(st, "mpfa_prefill_fp4pv")
     return out, lse
 
 

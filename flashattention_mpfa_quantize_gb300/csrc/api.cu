@@ -162,18 +162,47 @@ mpfa_status mpfa_quantize_qkv(const void* q_bf16, const void* k_bf16, const void
   return from_cuda(mpfa::launch_quantize(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-mpfa_status mpfa_prefill(const mpfa_nvfp4* q, const mpfa_rank1* qbar, const mpfa_nvfp4* k,
-                         const mpfa_fp8* v, int B, int N, int Hq, int Hkv, int d, int causal,
-                         int compensate, int T, void* o_bf16, float* lse,
-                         const float* lse_shift, mpfa_stream_t stream) {
+mpfa_status mpfa_quantize_v_fp4(const void* v_bf16, int B, int Nk, int Hkv, int d,
+                                mpfa_nvfp4* vt_out, void* workspace, size_t ws_bytes,
+                                mpfa_stream_t stream) {
+  if (d != 128) return MPFA_ERR_UNSUPPORTED;
+  if (B <= 0 || Nk <= 0 || Nk % 128 || Hkv <= 0 || !ok_ptr(v_bf16) || !vt_out ||
+      !ok_ptr(vt_out->codes) || !ok_ptr(vt_out->scales) || !vt_out->tensor_scale)
+    return MPFA_ERR_INVALID_ARG;
+  if ((uint64_t)B * Hkv * Nk >= (1ull << 31)) return MPFA_ERR_INVALID_ARG;
+  if (!ok_ptr(workspace) || ws_bytes < 256) return MPFA_ERR_INVALID_ARG;
+  mpfa::QuantArgs a = {};
+  a.B = B;
+  a.Nk = Nk;
+  a.Hkv = Hkv;
+  a.v = v_bf16;
+  a.vtc = vt_out->codes;
+  a.vts = vt_out->scales;
+  a.s_v = vt_out->tensor_scale;
+  a.amax = static_cast<unsigned*>(workspace);
+  a.err = status_ptr();
+  if (!a.err) return MPFA_ERR_CUDA;
+  return from_cuda(mpfa::launch_quantize_vt(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+namespace {
+
+// The checks and argument set both prefill entries share; vc/vts/s_v are
+// the V operand of either kernel.
+mpfa_status prefill_common(const mpfa_nvfp4* q, const mpfa_rank1* qbar, const mpfa_nvfp4* k,
+                           const uint8_t* vc, const uint8_t* vts, const float* s_v, int pv4,
+                           int B, int N, int Hq, int Hkv, int d, int causal, int compensate, int T,
+                           void* o_bf16, float* lse, const float* lse_shift, mpfa_stream_t stream) {
   if (d != 128) return MPFA_ERR_UNSUPPORTED;
   if (compensate && T != 1 && T != 2) return MPFA_ERR_UNSUPPORTED;
-  if (!q || !k || !v || B <= 0 || N <= 0 || N % 128 || Hq <= 0 || Hkv <= 0 || Hq % Hkv)
+  if (!q || !k || B <= 0 || N <= 0 || N % 128 || Hq <= 0 || Hkv <= 0 || Hq % Hkv)
     return MPFA_ERR_INVALID_ARG;
   if (!ok_ptr(q->codes) || !ok_ptr(q->scales) || !q->tensor_scale || !ok_ptr(k->codes) ||
-      !ok_ptr(k->scales) || !k->tensor_scale || !ok_ptr(v->codes) || !v->tensor_scale ||
-      !ok_ptr(o_bf16))
+      !ok_ptr(k->scales) || !k->tensor_scale || !ok_ptr(vc) || !s_v || !ok_ptr(o_bf16))
     return MPFA_ERR_INVALID_ARG;
+  if (pv4 && !ok_ptr(vts)) return MPFA_ERR_INVALID_ARG;
   if (compensate && (!qbar || !ok_ptr(qbar->codes) || !qbar->scales))
     return MPFA_ERR_INVALID_ARG;
   if ((uint64_t)B * Hq * N >= (1ull << 31) || (uint64_t)B * Hkv * N >= (1ull << 31))
@@ -187,8 +216,10 @@ mpfa_status mpfa_prefill(const mpfa_nvfp4* q, const mpfa_rank1* qbar, const mpfa
   a.kc = k->codes;
   a.ks = k->scales;
   a.s_k = k->tensor_scale;
-  a.vc = v->codes;
-  a.s_v = v->tensor_scale;
+  a.vc = vc;
+  a.vts = pv4 ? vts : nullptr;
+  a.s_v = s_v;
+  a.pv4 = pv4;
   a.B = B;
   a.N = N;
   a.Hq = Hq;
@@ -202,6 +233,28 @@ mpfa_status mpfa_prefill(const mpfa_nvfp4* q, const mpfa_rank1* qbar, const mpfa
   a.err = status_ptr();
   if (!a.err) return MPFA_ERR_CUDA;
   return from_cuda(mpfa::launch_prefill(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+mpfa_status mpfa_prefill(const mpfa_nvfp4* q, const mpfa_rank1* qbar, const mpfa_nvfp4* k,
+                         const mpfa_fp8* v, int B, int N, int Hq, int Hkv, int d, int causal,
+                         int compensate, int T, void* o_bf16, float* lse,
+                         const float* lse_shift, mpfa_stream_t stream) {
+  return prefill_common(q, qbar, k, v ? v->codes : nullptr, nullptr,
+                        v ? v->tensor_scale : nullptr, 0, B, N, Hq, Hkv, d, causal, compensate,
+                        T, o_bf16, lse, lse_shift, stream);
+}
+
+mpfa_status mpfa_prefill_fp4pv(const mpfa_nvfp4* q, const mpfa_rank1* qbar, const mpfa_nvfp4* k,
+                               const mpfa_nvfp4* vt, int B, int N, int Hq, int Hkv, int d,
+                               int causal, int compensate, int T, void* o_bf16, float* lse,
+                               mpfa_stream_t stream) {
+  return prefill_common(q, qbar, k, vt ? vt->codes : nullptr, vt ? vt->scales : nullptr,
+                        vt ? vt->tensor_scale : nullptr, 1, B, N, Hq, Hkv, d, causal,
+                        compensate, T, o_bf16, lse, nullptr, stream);
 }
 
 size_t mpfa_decode_workspace_size(int B, int Hq, int Hkv, int d, int Lmax, int kv_chunk) {

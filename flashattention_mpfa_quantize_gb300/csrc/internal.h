@@ -68,10 +68,16 @@ struct QuantArgs {
   float* qbar;     // [B][Hq][Nq/128][128] fp32 block means (compensate only)
   float* kstat;    // [B][Hkv][Nk/128][3][128]: block mean, max, min of K (ksmooth only)
   int* err;
+  // full-FP4 PV ablation (launch_quantize_vt only): V^T in NVFP4 along the
+  // keys, codes [B][Hkv][128][Nk/2], block scales one 1 KB tile per
+  // (b, KV head, 128-key tile) in the tensor core's scale-copy order;
+  // tensor scale into s_v
+  uint8_t *vtc, *vts;
 };
 
 size_t quant_workspace_bytes(int B, int Nq, int Nk, int Hq, int Hkv, int compensate, int ksmooth);
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream);
+cudaError_t launch_quantize_vt(const QuantArgs& a, cudaStream_t stream);
 
 // Quantize-on-append into a decode cache: new rows of K and V, quantized with
 // the cache's tensor scales, written at rows seqlens[b] + t.
@@ -99,9 +105,13 @@ struct PrefillArgs {
   const uint8_t *qbc, *qbs;  // rank-one terms (null when compensate == 0)
   const uint8_t *kc, *ks;
   const float* s_k;
+  // V codes: E4M3 [B][Hkv][N][128]; with pv4, NVFP4 V^T codes
+  // [B][Hkv][128][N/2] and their block scales (vts, 1 KB per 128-key tile)
   const uint8_t* vc;
+  const uint8_t* vts;
   const float* s_v;
   int B, N, Hq, Hkv, causal, compensate, T;
+  int pv4;     // 1: P and V in NVFP4 (the full-FP4 PV kernel)
   void* o;     // bf16 [B][N][Hq][128]
   float* lse;  // [B][Hq][N] or null
   const float* lse_shift;  // [B][Hq][N] added to the LSE (K-side smoothing), or null

@@ -86,6 +86,18 @@ constexpr uint32_t kColS0 = 0, kColO = 256, kColL = 384, kColP0 = 416, kColSfQ =
 // requires)
 __device__ __forceinline__ uint32_t col_sf_k(int i) { return i == 0 ? 408u : 496u; }
 
+// Full-FP4 PV ablation (the kPv4 kernel): P codes in shared memory (two
+// banks of 128 rows x 64 bytes, 64-byte swizzle, over the ones atom's region),
+// P block scales in V stage 0's unused tail, the all-ones operand of the row
+// sum (16 rows of E2M1 1.0 and their E4M3 1.0 scales) in V stage 1's tail
+// (a V^T stage uses only its first 9 KB); TMEM: the P scales of bank b at
+// 416 + 8b, the V^T scales of slot b at 432 + 8b, the ones' scales at 448
+// (the FP8 kernel's P banks).  P = NVFP4 of x = 2^(t - m + 4) with the fixed
+// tensor scale fp32(2^8 / 2688): the largest x a tile can produce, 2^(4+tau),
+// maps to 6 * 448.
+constexpr float kLog2SP4 = -3.3923173959064714f;   // log2(fp32(256 / 2688))
+constexpr uint32_t kColSfP4 = 416, kColSfV4 = 432, kColSfOnes4 = 448;
+
 // barrier indices
 enum : int {
   kBarQFull0 = 0,                      // +Q buffer: Q tile, scales and rank-one operand in smem
@@ -136,6 +148,12 @@ static_assert(kSmemUsed + 1024 <= kSmemBytes, "shared memory layout overflow");
 // every address a tcgen05 descriptor holds fits its 14-bit field (16-byte
 // units) even after the 1 KB alignment of the dynamic shared base
 static_assert(kOffMax + 2048 <= (1u << 18), "descriptor address field overflow");
+constexpr uint32_t kOffP4 = kOffOnes;                          // 2 x 8 KB P codes
+constexpr uint32_t kOffP4s = kOffV + 9216;                     // 2 x 1 KB P scales
+constexpr uint32_t kOffOnes4 = kOffV + kVStageBytes + 9216;    // 1 KB of E2M1 1.0
+constexpr uint32_t kOffOnes4s = kOffOnes4 + 1024;              // 1 KB of E4M3 1.0
+static_assert(kOffP4s + 2048 <= kOffV + kVStageBytes && kOffOnes4s + 1024 <= kOffV + 2 * kVStageBytes,
+              "FP4 PV operands overflow their V stage tails");
 
 struct Params {
   PrefillArgs a;
@@ -189,12 +207,33 @@ __device__ __forceinline__ bool poll_ge(const int* p, int want, int* err, volati
   }
 }
 
+// Eight E2M1 codes (element 2i in the low nibble of byte i).
+__device__ __forceinline__ uint32_t e2m1x8(const float* q) {
+  uint32_t r;
+  asm("{\n.reg .b8 t0, t1, t2, t3;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 t2, %6, %5;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 t3, %8, %7;\n"
+      "mov.b32 %0, {t0, t1, t2, t3};\n}"
+      : "=r"(r)
+      : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+  return r;
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
+__device__ __forceinline__ float rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <bool kPv4>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_k,
@@ -355,9 +394,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto issue_v = [&](int g) {
       const int s = g % kVStages;
       if (lane == 0) {
-        mbar_expect_tx(bar(kBarVFull0 + s), 16384);
-        tma_load_2d(sbase + kOffV + s * kVStageBytes, &map_v, 0, cv.row0 + (g - cv.g0) * 128,
-                    bar(kBarVFull0 + s));
+        if constexpr (kPv4) {
+          // V^T tile: 128 channel rows x 128 keys (64 bytes) and its 1 KB
+          // of block scales
+          const int bhk = cv.row0 / a.N, t = g - cv.g0;
+          mbar_expect_tx(bar(kBarVFull0 + s), 8192 + 1024);
+          tma_load_2d(sbase + kOffV + s * kVStageBytes, &map_v, 64 * t, bhk * 128,
+                      bar(kBarVFull0 + s));
+          bulk_load(sbase + kOffV + s * kVStageBytes + 8192,
+                    a.vts + ((size_t)bhk * (a.N / 128) + t) * 1024, 1024, bar(kBarVFull0 + s));
+        } else {
+          mbar_expect_tx(bar(kBarVFull0 + s), 16384);
+          tma_load_2d(sbase + kOffV + s * kVStageBytes, &map_v, 0, cv.row0 + (g - cv.g0) * 128,
+                      bar(kBarVFull0 + s));
+        }
       }
       v_issued = g + 1;
     };
@@ -565,7 +615,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         return __all_sync(0xffffffffu, mbar_wait(b, parity, a.err, ab));
       };
       const uint32_t id_pv = idesc_fp8(128, 144, 0, 1);   // 128 V columns + 16 ones
+      const uint32_t id_pv4 = idesc_nvfp4(128, 128), id_l4 = idesc_nvfp4(128, 16);
       bool ok = mbar_wait_w(bar(kBarOnes), 0, abort_flag);
+      if constexpr (kPv4) {
+        // the ones operand's block scales (all E4M3 1.0), copied once
+        if (ok) {
+          tc_fence_after();
+          for (int kc = 0; kc < 2; ++kc)
+            tmem_cp_32x128b_x4_w(tmem_w + kColSfOnes4 + 4 * kc,
+                                 smem_desc(sbase + kOffOnes4s + 512 * kc, 128, 128, kSwizzleNone));
+        }
+      }
       int g0 = 0;
       Item it;
       for (int k = 0; ok && item_of(p, k, it); ++k) {
@@ -581,15 +641,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t pcol = tmem_w + kColP0 + 32 * bp;
           const uint32_t voff = kOffV + sp * kVStageBytes;
-          // the N = 144 operand: V's 128-byte atom, then the ones atom at a
-          // leading offset of kOffOnes - voff bytes (the same 32-key
-          // sub-tile offset in both)
-          for (int kk = 0; kk < 4; ++kk)
-            mma_fp8_ts_w(tmem_w + kColO, pcol + 8 * kk,
-                       smem_desc(sbase + voff + 4096 * kk, kOffOnes - voff, 1024, kSwizzle128B),
-                       id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          if constexpr (kPv4) {
+            // P_g's and V_g^T's block scales into TMEM (their slots' last
+            // reader, PV_{g-2}, completed before the softmax published P_g);
+            // then O += P V^T and l += P 1 in block-scaled FP4, K = 64 keys
+            // per product
+            const uint32_t sfa = tmem_w + kColSfP4 + 8 * bp, sfb = tmem_w + kColSfV4 + 8 * bp;
+            for (int kc = 0; kc < 2; ++kc) {
+              tmem_cp_32x128b_x4_w(sfa + 4 * kc, smem_desc(sbase + kOffP4s + 1024 * bp + 512 * kc,
+                                                           128, 128, kSwizzleNone));
+              tmem_cp_32x128b_x4_w(sfb + 4 * kc, smem_desc(sbase + voff + 8192 + 512 * kc, 128, 128,
+                                                           kSwizzleNone));
+            }
+            const uint64_t da = smem_desc(sbase + kOffP4 + 8192 * bp, 16, 512, kSwizzle64B);
+            const uint64_t db = smem_desc(sbase + voff, 16, 512, kSwizzle64B);
+            const uint64_t d1 = smem_desc(sbase + kOffOnes4, 16, 512, kSwizzle64B);
+            mma_nvfp4_ss_w(tmem_w + kColO, da, db, id_pv4, sfa, sfb, j > 0 ? 1u : 0u);
+            mma_nvfp4_ss_w(tmem_w + kColO, da + 2u, db + 2u, id_pv4, sfa + 4, sfb + 4, 1u);
+            mma_nvfp4_ss_w(tmem_w + kColL, da, d1, id_l4, sfa, tmem_w + kColSfOnes4,
+                           j > 0 ? 1u : 0u);
+            mma_nvfp4_ss_w(tmem_w + kColL, da + 2u, d1 + 2u, id_l4, sfa + 4,
+                           tmem_w + kColSfOnes4 + 4, 1u);
+          } else {
+            const uint32_t pcol = tmem_w + kColP0 + 32 * bp;
+            // the N = 144 operand: V's 128-byte atom, then the ones atom at a
+            // leading offset of kOffOnes - voff bytes (the same 32-key
+            // sub-tile offset in both)
+            for (int kk = 0; kk < 4; ++kk)
+              mma_fp8_ts_w(tmem_w + kColO, pcol + 8 * kk,
+                           smem_desc(sbase + voff + 4096 * kk, kOffOnes - voff, 1024, kSwizzle128B),
+                           id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          }
           tc_commit_w(bar(kBarODone0 + sp));
         }
         g0 += it.nkv;
@@ -604,7 +687,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     // the ones atom of the PV operand (E4M3 1.0 = 0x38; every byte equal,
     // so the 128-byte swizzle leaves it unchanged), written once
-    {
+    if constexpr (kPv4) {
+      // the row sum's operand: 16 rows of E2M1 1.0 (code 2) and their E4M3
+      // 1.0 block scales (every byte equal, so any layout reads the same)
+      uint4* ones = reinterpret_cast<uint4*>(smem + kOffOnes4);
+      uint4* ones_s = reinterpret_cast<uint4*>(smem + kOffOnes4s);
+      for (int i = threadIdx.x; i < 1024 / 16; i += kSoftmaxThreads) {
+        ones[i] = make_uint4(0x22222222u, 0x22222222u, 0x22222222u, 0x22222222u);
+        ones_s[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
+      }
+    } else {
       uint4* ones = reinterpret_cast<uint4*>(smem + kOffOnes);
       for (int i = threadIdx.x; i < 16384 / 16; i += kSoftmaxThreads)
         ones[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
@@ -674,10 +766,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         fmaxf(__uint_as_float(sr[e >> 5][(e + 6) & 31]),
                               __uint_as_float(sr[e >> 5][(e + 7) & 31])));
         }
-        const float smax = fmax3(fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]),
-                                       fmax3(pm[6], pm[7], pm[8])),
-                                 fmax3(pm[9], pm[10], pm[11]),
-                                 fmax3(fmax3(pm[12], pm[13], pm[14]), pm[15], -INFINITY));
+        // (FP4 P keeps the eight 16-key block maxima for its block scales)
+        float bmx[8];
+        float smax;
+        if constexpr (kPv4) {
+#pragma unroll
+          for (int kb = 0; kb < 8; ++kb) bmx[kb] = fmaxf(pm[2 * kb], pm[2 * kb + 1]);
+          smax = fmax3(fmax3(bmx[0], bmx[1], bmx[2]), fmax3(bmx[3], bmx[4], bmx[5]),
+                       fmaxf(bmx[6], bmx[7]));
+        } else {
+          smax = fmax3(fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]),
+                             fmax3(pm[6], pm[7], pm[8])),
+                       fmax3(pm[9], pm[10], pm[11]),
+                       fmax3(fmax3(pm[12], pm[13], pm[14]), pm[15], -INFINITY));
+        }
         // reference max of the row after tile g-1, from that tile's owner
         if (g > 0) {
           // the row's slot holds tile g-1's value once its index reads g-1
@@ -717,20 +819,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float alpha = (m == -INFINITY) ? 0.0f : (mn == m ? 1.0f : ex2(m - mn));
         const float bias = kPShift - mn;  // P8 = E4M3(2^(t - m) * 2^kPShift)
         const float2 cs2 = make_float2(cs, cs), bias2 = make_float2(bias, bias);
-        uint32_t pw[32];
+        uint32_t pw[kPv4 ? 18 : 32];
+        if constexpr (!kPv4) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int w = 0; w < 8; ++w) {
-            // two scores per packed fp32 FMA
-            const float2 t0 = __ffma2_rn(
-                make_float2(__uint_as_float(sr[c][4 * w]), __uint_as_float(sr[c][4 * w + 1])),
-                cs2, bias2);
-            const float2 t1 = __ffma2_rn(
-                make_float2(__uint_as_float(sr[c][4 * w + 2]), __uint_as_float(sr[c][4 * w + 3])),
-                cs2, bias2);
-            pw[8 * c + w] = e4m3x4(ex2(t0.x), ex2(t0.y), ex2(t1.x), ex2(t1.y));
+            for (int w = 0; w < 8; ++w) {
+              // two scores per packed fp32 FMA
+              const float2 t0 = __ffma2_rn(
+                  make_float2(__uint_as_float(sr[c][4 * w]), __uint_as_float(sr[c][4 * w + 1])),
+                  cs2, bias2);
+              const float2 t1 = __ffma2_rn(
+                  make_float2(__uint_as_float(sr[c][4 * w + 2]), __uint_as_float(sr[c][4 * w + 3])),
+                  cs2, bias2);
+              pw[8 * c + w] = e4m3x4(ex2(t0.x), ex2(t0.y), ex2(t1.x), ex2(t1.y));
+            }
+        } else {
+          // x = 2^(t - m + 4) in NVFP4 per 16 keys with the fixed tensor
+          // scale s_p = fp32(2^8 / 2688): block scale sb = E4M3(max x /
+          // (6 s_p)), 1 / (6 s_p) = 1.75, with max x = x at the block's
+          // largest score (x grows with the score; the block maxima come
+          // from the tile's max tree); code = E2M1(x / (value(sb) s_p)),
+          // the quotient as x * (10.5 / value(sb)) (1 / s_p = 10.5) on
+          // packed pairs.
+          // pw[0..15]: 8 codes per word in key order; pw[16..17]: the block
+          // scales of keys 0-63 and 64-127, four per word
+          pw[16] = pw[17] = 0u;
+#pragma unroll
+          for (int kb = 0; kb < 8; ++kb) {
+            const float bamax = ex2(__fmaf_rn(bmx[kb], cs, bias));
+            const uint32_t sb = e4m3_pos(__fmul_rn(bamax, 1.75f));
+            const float y = sb != 0u ? __fmul_rn(10.5f, rcp(e4m3_value(sb))) : 0.0f;
+            const float2 y2 = make_float2(y, y);
+            float q[16];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint32_t* sv = &sr[kb >> 1][16 * (kb & 1) + 2 * i];
+              const float2 t2 = __ffma2_rn(
+                  make_float2(__uint_as_float(sv[0]), __uint_as_float(sv[1])), cs2, bias2);
+              const float2 q2 = __fmul2_rn(make_float2(ex2(t2.x), ex2(t2.y)), y2);
+              q[2 * i] = q2.x;
+              q[2 * i + 1] = q2.y;
+            }
+            pw[2 * kb] = e2m1x8(q);
+            pw[2 * kb + 1] = e2m1x8(q + 8);
+            pw[16 + (kb >> 2)] |= sb << (8 * (kb & 3));
           }
+        }
         // correction: O and L scale by alpha once PV_{g-1} has landed (PV_g is
         // issued only after this tile's P is published)
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
@@ -764,12 +899,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        tc_fence_after();
-        tmem_st32(tmem + lane_off + kColP0 + 32 * bk, pw);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarPReady0 + bk));
+        if constexpr (kPv4) {
+          // the row's 64 code bytes into P bank g % 2 in the 64-byte swizzle
+          // of the MMA operand, its block-scale words in the scale-copy order
+          uint8_t* prow = smem + kOffP4 + 8192 * bk + 64 * row;
+          const int swz = (row >> 1) & 3;
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4)
+            *reinterpret_cast<uint4*>(prow + 16 * (c4 ^ swz)) =
+                make_uint4(pw[4 * c4], pw[4 * c4 + 1], pw[4 * c4 + 2], pw[4 * c4 + 3]);
+#pragma unroll
+          for (int kc = 0; kc < 2; ++kc)
+            *reinterpret_cast<uint32_t*>(smem + kOffP4s + 1024 * bk + 512 * kc + (row & 31) * 16 +
+                                         ((row >> 5) & 3) * 4) = pw[16 + kc];
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarPReady0 + bk));
+        } else {
+          tc_fence_after();
+          tmem_st32(tmem + lane_off + kColP0 + 32 * bk, pw);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarPReady0 + bk));
+        }
         m = mn;
       }
       if (!ok) break;
@@ -836,7 +989,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // natural-log LSE of the scaled logits; with key-side smoothing
           // plus the row's dropped logit part q_eff . kbar / sqrt(d)
           const size_t li = (size_t)it.bh * a.N + grow;
-          const float lse = 0.69314718055994531f * (m + __log2f(l) - kPShift);
+          // (with FP4 P the row sum counts code * block scale: times s_p)
+          const float lse = 0.69314718055994531f *
+                            (m + __log2f(l) + (kPv4 ? kLog2SP4 : 0.0f) - kPShift);
           a.lse[li] = a.lse_shift ? lse + a.lse_shift[li] : lse;
         }
       }
@@ -860,18 +1015,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mo;
   const uint64_t qrows = (uint64_t)a.B * a.Hq * a.N, kvrows = (uint64_t)a.B * a.Hkv * a.N;
+  // V: E4M3 rows of 128 channels, 128-key boxes; or (pv4) V^T rows of N/2
+  // code bytes per channel, boxes of 128 keys (64 bytes) x 128 channels
+  const bool mv_ok =
+      a.pv4 ? make_map_2d_u8_box(&mv, a.vc, (uint64_t)a.N / 2, (uint64_t)a.N / 2,
+                                 (uint64_t)a.B * a.Hkv * 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B)
+            : make_map_2d_u8(&mv, a.vc, 128, kvrows, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!make_map_2d_u8(&mq, a.qc, 64, qrows, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_map_2d_u8(&mk, a.kc, 64, kvrows, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_map_2d_u8(&mv, a.vc, 128, kvrows, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d_u8(&mk, a.kc, 64, kvrows, 128, CU_TENSOR_MAP_SWIZZLE_64B) || !mv_ok ||
       !make_map_2d_u8_box(&mo, a.o, (uint64_t)a.Hq * 256, (uint64_t)a.Hq * 256,
                           (uint64_t)a.B * a.N, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  static std::atomic<bool> attr_set[kMaxDevices];
+  static std::atomic<bool> attr_set[2][kMaxDevices];
   const int dev = current_device();
   if (dev < 0) return cudaErrorInvalidDevice;
+  auto* kernel = a.pv4 ? prefill_kernel<true> : prefill_kernel<false>;
   {
-    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(prefill_kernel), kSmemBytes, dev,
-                                  attr_set);
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kernel), kSmemBytes, dev,
+                                  attr_set[a.pv4 ? 1 : 0]);
     if (e != cudaSuccess) return e;
   }
   Params p;
@@ -886,8 +1047,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   // walking its share of the work items
   const unsigned grid = (unsigned)(p.items < sms ? p.items : sms);
   // may start (barriers, tensor memory) while the quantization finishes
-  return launch_pdl(prefill_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream, mq, mk, mv,
-                    mo, p);
+  return launch_pdl(kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream, mq, mk, mv, mo, p);
 }
 
 }  // namespace mpfa

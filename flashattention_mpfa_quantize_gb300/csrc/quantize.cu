@@ -863,6 +863,52 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
   }
 }
 
+// Full-FP4 PV ablation: V^T in NVFP4 along the keys (the reduction
+// dimension of P V), one CTA per (b, KV head, 128-key tile).  The tile's
+// 128 keys x 128 channels come into shared memory row by row (coalesced),
+// then thread t codes channel t % 128 over the 64 keys of half t / 128: four
+// 16-key blocks with the same block routine (and so the same codes) as K,
+// 32 code bytes and one word of four block scales.
+__global__ void __launch_bounds__(256) vt_quant_kernel(QuantArgs a) {
+  __shared__ uint4 tile[128][16];   // [key][16-byte chunk of 8 channels]
+  pdl_wait();   // amax(V) from the statistics kernel
+  pdl_trigger();
+  const int ntiles = a.Nk / 128;
+  const int u = blockIdx.x, j = u % ntiles, bh = u / ntiles;
+  const int h = bh % a.Hkv, b = bh / a.Hkv;
+  const float s = tensor_scale(a.amax[2], kNvfp4Max);
+  if (u == 0 && threadIdx.x == 0) *a.s_v = s;
+  const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(a.v);
+  for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {
+    const int key = i >> 4, ch = i & 15;
+    tile[key][ch] = __ldg(reinterpret_cast<const uint4*>(
+        v + (((size_t)b * a.Nk + (size_t)j * 128 + key) * a.Hkv + h) * 128 + 8 * ch));
+  }
+  __syncthreads();
+  const int c = threadIdx.x & 127, half = threadIdx.x >> 7;
+  const __nv_bfloat16* tb = reinterpret_cast<const __nv_bfloat16*>(&tile[0][0]);
+  uint32_t cw[8];
+  uint32_t sbw = 0;
+#pragma unroll
+  for (int kb = 0; kb < 4; ++kb) {
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = __bfloat162float(tb[(64 * half + 16 * kb + i) * 128 + c]);
+    uint2 codes;
+    uint32_t sb;
+    nvfp4_block(x, s, codes, sb);
+    cw[2 * kb] = codes.x;
+    cw[2 * kb + 1] = codes.y;
+    sbw |= sb << (8 * kb);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(a.vtc + ((size_t)bh * 128 + c) * (a.Nk / 2) +
+                                        (size_t)j * 64 + 32 * half);
+  dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+  dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+  *reinterpret_cast<uint32_t*>(a.vts + ((size_t)bh * ntiles + j) * 1024 + 512 * half +
+                               (c & 31) * 16 + ((c >> 5) & 3) * 4) = sbw;
+}
+
 int num_sms() {
   const int n = sm_count(current_device());
   return n > 0 ? n : 148;
@@ -916,6 +962,20 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
     e = launch_pdl(quant_kernel<false>, grid, dim3(kThreads), 0, stream, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_vt(const QuantArgs& a, cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(a.amax, 0, 3 * sizeof(unsigned), stream);
+  if (e != cudaSuccess) return e;
+  const int sms = num_sms();
+  const size_t n8 = (size_t)a.B * a.Nk * a.Hkv * 16;
+  size_t need = (n8 + kStatsThreads - 1) / kStatsThreads;
+  const size_t cap = (size_t)sms * kStatsCtasPerSm;
+  const int nv = (int)(need < cap ? (need ? need : 1) : cap);
+  stats_kernel<<<nv, kStatsThreads, 0, stream>>>(a, 0, 0, nv);   // amax(V) only
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_pdl(vt_quant_kernel, dim3(a.B * a.Hkv * (a.Nk / 128)), dim3(256), 0, stream, a);
 }
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {

@@ -199,6 +199,39 @@ mpfa_status mpfa_prefill(const mpfa_nvfp4 *q, const mpfa_rank1 *qbar, const mpfa
                          int compensate, int T, void *o_bf16, float *lse,
                          const float *lse_shift, mpfa_stream_t stream);
 
+/*
+ * Full-FP4 PV ablation (the MpFA abstract weighs QK4PV8 against full FP4):
+ * V^T quantized to NVFP4 along the keys, the reduction dimension of P V.
+ * Per (b, KV head, channel) row of V^T, 16-key blocks with E4M3 block scales
+ * and one fp32 tensor scale fp32(amax(V) / 2688), the same quantizer rules
+ * as K.
+ *   v_bf16 [B][Nk][Hkv][d], Nk a multiple of 128, d == 128.
+ *   vt_out->codes [B][Hkv][d][Nk/2] (key 2i in the low nibble of byte i);
+ *   vt_out->scales one 1 KB tile per (b, KV head, 128-key tile) in the
+ *   tensor core's scale-copy order (byte (c%32)*16 + ((c/32)%4)*4 + j%4 of
+ *   the 512-byte block j/4 for channel c, 16-key block j);
+ *   vt_out->tensor_scale: one float.
+ *   workspace: device, 16-byte aligned, >= 256 bytes (the amax words).
+ * Caller-owned buffers; asynchronous on `stream`.
+ */
+mpfa_status mpfa_quantize_v_fp4(const void *v_bf16, int B, int Nk, int Hkv, int d,
+                                mpfa_nvfp4 *vt_out, void *workspace, size_t ws_bytes,
+                                mpfa_stream_t stream);
+
+/*
+ * Prefill forward with the full-FP4 PV of the ablation: as mpfa_prefill up
+ * to p = 2^(t - m) under the same reference-max rule; then x = 2^4 p coded in
+ * NVFP4 per 16 keys of a row with the fixed tensor scale
+ * fp32(2^8 / 2688), multiplied in block-scaled FP4 with vt from
+ * mpfa_quantize_v_fp4; the row sum l adds the same rounded values.
+ *   Arguments as mpfa_prefill, vt in place of v; no lse_shift (the key-side
+ *   smoothing is not part of the ablation).
+ */
+mpfa_status mpfa_prefill_fp4pv(const mpfa_nvfp4 *q, const mpfa_rank1 *qbar,
+                               const mpfa_nvfp4 *k, const mpfa_nvfp4 *vt, int B, int N, int Hq,
+                               int Hkv, int d, int causal, int compensate, int T, void *o_bf16,
+                               float *lse, mpfa_stream_t stream);
+
 /* Bytes of device workspace mpfa_decode needs for kv_chunk (0 = the chunk
  * the library would choose). */
 size_t mpfa_decode_workspace_size(int B, int Hq, int Hkv, int d, int Lmax, int kv_chunk);

@@ -40,3 +40,54 @@ def oracle_quantize(Q, K, V, compensate, T):
     if V is not None:
         out["v"] = orc.quantize_v(np_f32(V))
     return out
+
+
+# Full-FP4 PV: decisions that may fall either way in fp32 arithmetic
+S_P = np.float32(256.0 / 2688.0)
+# How far the kernel's log2 scores may sit from the oracle's fp64 ones: fp32
+# accumulation of the score products in another order (relative ~1e-6 of
+# scores up to ~20) plus the hardware exponential (2^-22 relative).
+T_SLACK = 1e-5
+
+
+def fp4p_flip_allowance(qz, kz, vz, b, h, g):
+    """Single 128-key tile per row (N = 128, causal), so m is the row max and
+    x = 2^(t - m + 4).  A block-scale or code decision whose x lies within
+    T_SLACK (log2 units) of an E4M3 or E2M1 rounding boundary may fall either
+    way in fp32 arithmetic: each such unit (a whole block if its scale moves,
+    else one key) may move O by |dP (v - o)| / l and l by |sum dP|.  Returns
+    the per-element sum of the O moves [rows, d] and the bound on the LSE's
+    move, -ln(1 - s) with s the sum of the relative l moves [rows]."""
+    q, qadd, k, _ = orc._head_operands(qz, kz, None, b, h, g)
+    t = (q + qadd) @ k.T * orc.score_scale_log2(qz["s_q"], kz["s_k"])
+    n = t.shape[0]
+    t = np.where(np.arange(n)[None, :] > np.arange(n)[:, None], -np.inf, t)
+    m = t.max(axis=1, keepdims=True)
+    v = orc.nvfp4_dequant(vz["vc4"][b, h // g], vz["vs4"][b, h // g]).T * np.float64(vz["s_v"])
+
+    def quant(tt):
+        c, sc = orc.nvfp4_quantize(np.exp2(tt - m + 4).astype(np.float32), S_P)
+        return orc.nvfp4_dequant(c, sc) * np.float64(S_P), sc
+
+    P, sc = quant(t)
+    l = P.sum(axis=1, keepdims=True)
+    o = P @ v / l
+    allow = np.zeros_like(o)
+    rel_l = np.zeros(n)
+    for shift in (T_SLACK, -T_SLACK):
+        Pa, sca = quant(t + shift)
+        for r in range(n):
+            for blk in range(8):
+                sl = slice(16 * blk, 16 * blk + 16)
+                if sca[r, blk] != sc[r, blk]:
+                    dP = Pa[r, sl] - P[r, sl]
+                    allow[r] += np.abs(dP[None, :] @ (v[sl] - o[r])).ravel() / l[r, 0]
+                    rel_l[r] += abs(dP.sum()) / l[r, 0]
+                else:
+                    for j in np.nonzero(Pa[r, sl] != P[r, sl])[0]:
+                        key = 16 * blk + j
+                        dp = Pa[r, key] - P[r, key]
+                        allow[r] += np.abs(dp * (v[key] - o[r])) / l[r, 0]
+                        rel_l[r] += abs(dp) / l[r, 0]
+    assert (rel_l < 0.5).all()
+    return allow, -np.log1p(-rel_l)

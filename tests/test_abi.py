@@ -56,6 +56,14 @@ def test_host_side_validation_without_gpu(lib):
     # d != 128 -> unsupported; null tensors -> invalid
     assert f(None, None, None, None, 1, 128, 1, 1, 64, 0, 0, 0, None, None, None, None) == 2
     assert f(None, None, None, None, 1, 128, 1, 1, 128, 0, 0, 0, None, None, None, None) == 1
+    f4 = lib.mpfa_prefill_fp4pv
+    f4.restype = ctypes.c_int
+    assert f4(None, None, None, None, 1, 128, 1, 1, 64, 0, 0, 0, None, None, None) == 2
+    assert f4(None, None, None, None, 1, 128, 1, 1, 128, 0, 0, 0, None, None, None) == 1
+    v4 = lib.mpfa_quantize_v_fp4
+    v4.restype = ctypes.c_int
+    assert v4(None, 1, 128, 1, 64, None, None, ctypes.c_size_t(0), None) == 2
+    assert v4(None, 1, 128, 1, 128, None, None, ctypes.c_size_t(0), None) == 1
     q = lib.mpfa_quantize_qkv
     q.restype = ctypes.c_int
     assert q(None, None, None, 1, 128, 128, 1, 1, 128, 0, 2, None, None, None, None, None, None,

@@ -5,7 +5,9 @@ FP8 PV is the better trade; on the synthetic inputs the FP8 variant's output
 is closer to exact fp64 attention, and with the scores left unquantized the
 PV format's own error is several times smaller in FP8.
 
-Full-FP4 variant, written out here (no kernel has it): scores in log2 units
+Full-FP4 variant, written out here with a full softmax (the kernel variant,
+prefill_kernel<true>, is checked against the oracle's online emulation in
+test_gpu_fp4pv.py): scores in log2 units
 from the dequantized Q, K and rank-one term; exact row max; p = 2^(t - max)
 in [0, 1]; P in NVFP4 along the keys (16-key blocks, tensor scale 1/2688 so
 that p = 1 maps to code 6 under block scale 448); V in NVFP4 along the keys
