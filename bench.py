@@ -315,28 +315,35 @@ def run_reference(args):
 # GPU arm
 # ----------------------------------------------------------------------------
 
-def prefill_roofline(cfg, pre_ms, peaks):
+def prefill_roofline(cfg, pre_ms, peaks, pv4=False):
     """prefill_kernel against the FP4 QK^T + FP8 PV tensor-pipe roofline: the
-    measured bf16 peak times the nominal dense ratios (FP4 = 6x, FP8 = 2x)."""
+    measured bf16 peak times the nominal dense ratios (FP4 = 6x, FP8 = 2x).
+    pv4 (the full-FP4 PV ablation): both products at the FP4 ratio."""
     flops = FLOP_PER_PAIR * cfg.pairs
     f4 = f8 = flops / 2
     p4, p8 = 6 * peaks["bf16"], 2 * peaks["bf16"]
-    t_roof = f4 / (p4 * 1e12) + f8 / (p8 * 1e12)
+    t_roof = (flops / (p4 * 1e12) if pv4 else f4 / (p4 * 1e12) + f8 / (p8 * 1e12))
     peak_eff = flops / t_roof / 1e12
     achieved = flops / (pre_ms * 1e-3) / 1e12
     return {"bound": "tensor", "achieved": achieved, "peak": peak_eff, "unit": "TFLOP/s",
-            "frac": achieved / peak_eff, "traffic": measured_traffic("prefill_kernel", cfg.name),
+            "frac": achieved / peak_eff,
+            "traffic": None if pv4 else measured_traffic("prefill_kernel", cfg.name),
             "traffic_unit": "bytes per launch (ncu dram read + write)",
-            "algorithmic_bytes": prefill_algo_bytes(cfg), "kernel": "prefill_kernel",
-            "peak_source": peaks["source"] + " bf16 burst x nominal FP4 (6x) / FP8 (2x) "
-            "ratios, harmonic mix for equal FP4 and FP8 FLOPs"}
+            "algorithmic_bytes": None if pv4 else prefill_algo_bytes(cfg),
+            "kernel": "prefill_kernel<true> (full-FP4 PV)" if pv4 else "prefill_kernel",
+            "peak_source": peaks["source"] + (" bf16 burst x nominal FP4 ratio (6x)" if pv4 else
+                                              " bf16 burst x nominal FP4 (6x) / FP8 (2x) "
+                                              "ratios, harmonic mix for equal FP4 and FP8 FLOPs")}
 
 
 def time_prefill(mp, cfg, Q, K, V, flush, stream, steps, warmup, compensate=True, T=T_TERMS,
-                 clocks=None, k_smooth=False):
+                 clocks=None, k_smooth=False, pv4=False):
     """Quantize + prefill of `cfg` timed with CUDA events on the launching
-    stream, L2 flushed before every step.  Returns (step, quantize, prefill)
-    mean ms."""
+    stream, L2 flushed before every step.  pv4: the full-FP4 PV ablation
+    (V^T quantized to NVFP4, the FP4-PV prefill kernel) in place of the
+    method's FP8 PV.  Returns (step, quantize, prefill) mean ms."""
+    if pv4:
+        return _time_prefill_pv4(mp, cfg, Q, K, V, flush, stream, steps, warmup, clocks)
     z = mp.quantize_qkv(Q, K, V, compensate=compensate, T=T, k_smooth=k_smooth)
     ws = z["_workspace"]
     o, lse = mp.prefill(z, causal=cfg.causal)
@@ -370,6 +377,40 @@ def time_prefill(mp, cfg, Q, K, V, flush, stream, steps, warmup, compensate=True
             statistics.mean(e[1].elapsed_time(e[2]) for e in evs))
 
 
+def _time_prefill_pv4(mp, cfg, Q, K, V, flush, stream, steps, warmup, clocks):
+    z = mp.quantize_qkv(Q, K, None, compensate=True, T=T_TERMS)
+    vt = mp.quantize_v_fp4(V)
+    ws, wsv = z["_workspace"], vt["_workspace"]
+    o, lse = mp.prefill_fp4pv(z, vt, causal=cfg.causal)
+
+    def quant():
+        return (mp.quantize_qkv(Q, K, None, compensate=True, T=T_TERMS, workspace=ws),
+                mp.quantize_v_fp4(V, workspace=wsv))
+
+    for _ in range(max(warmup, 3)):
+        flush.zero_()
+        zz, vv = quant()
+        mp.prefill_fp4pv(zz, vv, causal=cfg.causal, out=o, lse=lse)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    if clocks is not None:
+        clocks.start()
+    torch.cuda.synchronize()
+    for ev in evs:
+        flush.zero_()
+        ev[0].record(stream)
+        zz, vv = quant()
+        ev[1].record(stream)
+        mp.prefill_fp4pv(zz, vv, causal=cfg.causal, out=o, lse=lse)
+        ev[2].record(stream)
+    torch.cuda.synchronize()
+    if mp.get_error() != 0:
+        raise RuntimeError(f"device status word set while timing {cfg.name} (FP4 PV)")
+    return (statistics.mean(e[0].elapsed_time(e[2]) for e in evs),
+            statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
+            statistics.mean(e[1].elapsed_time(e[2]) for e in evs))
+
+
 def run_gpu(args):
     import flashattention_mpfa_quantize_gb300 as mp
     ws, rank, local = _dist()
@@ -395,14 +436,15 @@ def run_gpu(args):
 
     Q, K, V = mi.prefill_inputs(cfg, dev, seed=rank)
     clocks = Clocks(dev.index)
+    pv4 = args.pv == "fp4"
     step_ms, quant_ms, pre_ms = time_prefill(mp, cfg, Q, K, V, flush, stream, args.steps,
-                                             args.warmup, clocks=clocks)
+                                             args.warmup, clocks=clocks, pv4=pv4)
     clk = clocks.stop()
-    launches += 3 * args.steps
+    launches += (5 if pv4 else 3) * args.steps
     flops = FLOP_PER_PAIR * cfg.pairs
     rate, ms = aggregate_rate(flops, step_ms, ws, dev)
     value = rate / 1e12
-    roofline = prefill_roofline(cfg, pre_ms, peaks)
+    roofline = prefill_roofline(cfg, pre_ms, peaks, pv4=pv4)
     roofline.update({"workload": cfg.name, "quantize_ms": quant_ms, "prefill_ms": pre_ms})
     # diagnostic: the exp-unit bound (one ex2 per pair at 32 per clock per SM)
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -466,10 +508,15 @@ def run_gpu(args):
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "nvfp4 e2m1 (QK) + fp8 e4m3 (PV), fp32 accumulate", "data": "synthetic",
+                "dtype": ("nvfp4 e2m1 (QK and PV: full-FP4 ablation), fp32 accumulate" if pv4
+                          else "nvfp4 e2m1 (QK) + fp8 e4m3 (PV), fp32 accumulate"),
+                "data": "synthetic",
                 "config": {"workload": cfg.name, "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv,
                            "N": cfg.N, "d": 128, "causal": cfg.causal, "compensate": True,
-                           "T": T_TERMS, "step": "mpfa_quantize_qkv + mpfa_prefill",
+                           "T": T_TERMS,
+                           "step": ("mpfa_quantize_qkv (Q, K) + mpfa_quantize_v_fp4 + "
+                                    "mpfa_prefill_fp4pv" if pv4
+                                    else "mpfa_quantize_qkv + mpfa_prefill"),
                            "l2": "inputs larger than L2, and L2 flushed (512 MB write) before "
                                  "every step",
                            "parallelism": "replicas" if ws > 1 else "single"},
@@ -752,11 +799,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the other prefill workloads")
+    ap.add_argument("--pv", choices=["fp8", "fp4"], default="fp8",
+                    help="fp4: time the full-FP4 PV ablation kernel instead of the method's "
+                         "FP8 PV (with --only prefill)")
     ap.add_argument("--only", choices=["prefill", "decode"], default=None,
                     help="profiling aid: time only this part (no e2e / cpu baseline)")
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="profiling aid: smaller decode batch than the workload's 64")
     args = ap.parse_args()
+    if args.pv == "fp4" and args.only != "prefill":
+        ap.error("--pv fp4 times the ablation kernel alone: give --only prefill")
     if args.impl == "reference":
         run_reference(args)
     else:
