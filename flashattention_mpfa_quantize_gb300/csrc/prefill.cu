@@ -227,9 +227,9 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ float rcp(float x) {
+__device__ __forceinline__ float lg2(float x) {
   float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
@@ -839,27 +839,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           // scale s_p = fp32(2^8 / 2688): block scale sb = E4M3(max x /
           // (6 s_p)), 1 / (6 s_p) = 1.75, with max x = x at the block's
           // largest score (x grows with the score; the block maxima come
-          // from the tile's max tree); code = E2M1(x / (value(sb) s_p)),
-          // the quotient as x * (10.5 / value(sb)) (1 / s_p = 10.5) on
-          // packed pairs.
+          // from the tile's max tree); code = E2M1(x / (value(sb) s_p)), the
+          // quotient taken in the exponent, 2^(t - m + 4 - log2(value(sb)
+          // s_p)), so a key costs what it costs the FP8 path: half a packed
+          // FMA, one exponential, half an E2M1 pair conversion.
           // pw[0..15]: 8 codes per word in key order; pw[16..17]: the block
           // scales of keys 0-63 and 64-127, four per word
           pw[16] = pw[17] = 0u;
 #pragma unroll
           for (int kb = 0; kb < 8; ++kb) {
-            const float bamax = ex2(__fmaf_rn(bmx[kb], cs, bias));
-            const uint32_t sb = e4m3_pos(__fmul_rn(bamax, 1.75f));
-            const float y = sb != 0u ? __fmul_rn(10.5f, rcp(e4m3_value(sb))) : 0.0f;
-            const float2 y2 = make_float2(y, y);
+            const uint32_t sb =
+                e4m3_pos(__fmul_rn(ex2(__fmaf_rn(bmx[kb], cs, bias)), 1.75f));
+            // a block with no code above zero gets the exponent -inf (code 0)
+            const float qb = sb != 0u ? bias - (lg2(e4m3_value(sb)) + kLog2SP4) : -INFINITY;
+            const float2 qb2 = make_float2(qb, qb);
             float q[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint32_t* sv = &sr[kb >> 1][16 * (kb & 1) + 2 * i];
+            for (int i = 0; i < 16; i += 2) {
+              const uint32_t* sv = &sr[kb >> 1][16 * (kb & 1) + i];
               const float2 t2 = __ffma2_rn(
-                  make_float2(__uint_as_float(sv[0]), __uint_as_float(sv[1])), cs2, bias2);
-              const float2 q2 = __fmul2_rn(make_float2(ex2(t2.x), ex2(t2.y)), y2);
-              q[2 * i] = q2.x;
-              q[2 * i + 1] = q2.y;
+                  make_float2(__uint_as_float(sv[0]), __uint_as_float(sv[1])), cs2, qb2);
+              q[i] = ex2(t2.x);
+              q[i + 1] = ex2(t2.y);
             }
             pw[2 * kb] = e2m1x8(q);
             pw[2 * kb + 1] = e2m1x8(q + 8);
