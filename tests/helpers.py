@@ -59,11 +59,23 @@ def fp4p_flip_allowance(qz, kz, vz, b, h, g):
     the per-element sum of the O moves [rows, d] and the bound on the LSE's
     move, -ln(1 - s) with s the sum of the relative l moves [rows]."""
     q, qadd, k, _ = orc._head_operands(qz, kz, None, b, h, g)
-    t = (q + qadd) @ k.T * orc.score_scale_log2(qz["s_q"], kz["s_k"])
-    n = t.shape[0]
-    t = np.where(np.arange(n)[None, :] > np.arange(n)[:, None], -np.inf, t)
-    m = t.max(axis=1, keepdims=True)
     v = orc.nvfp4_dequant(vz["vc4"][b, h // g], vz["vs4"][b, h // g]).T * np.float64(vz["s_v"])
+    return fp4p_first_tile_allowance(q + qadd, k, v, orc.score_scale_log2(qz["s_q"], kz["s_k"]),
+                                     np.arange(q.shape[0]))
+
+
+def fp4p_first_tile_allowance(qe, k, v, cs, rows):
+    """The flip allowance of fp4p_flip_allowance for causal query rows < 128
+    (rows: their indices), whose keys all lie in the first 128-key tile:
+    qe the rows' effective query vectors [len(rows), d] (dequantized, rank-one
+    terms added, no tensor scale), k and v the head's first 128 keys and
+    values (v with its tensor scale)."""
+    rows = np.asarray(rows)
+    assert (rows < 128).all()
+    t = qe @ k[:128].T * cs
+    t = np.where(np.arange(128)[None, :] > rows[:, None], -np.inf, t)
+    m = t.max(axis=1, keepdims=True)
+    v = v[:128]
 
     def quant(tt):
         c, sc = orc.nvfp4_quantize(np.exp2(tt - m + 4).astype(np.float32), S_P)
@@ -72,6 +84,7 @@ def fp4p_flip_allowance(qz, kz, vz, b, h, g):
     P, sc = quant(t)
     l = P.sum(axis=1, keepdims=True)
     o = P @ v / l
+    n = len(rows)
     allow = np.zeros_like(o)
     rel_l = np.zeros(n)
     for shift in (T_SLACK, -T_SLACK):

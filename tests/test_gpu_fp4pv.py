@@ -9,7 +9,8 @@ import torch
 
 import mpfa_inputs as mi
 import oracle as orc
-from helpers import fp4p_flip_allowance, np_f32, oracle_quantize, rel_l2, tiled_to_rows
+from helpers import (fp4p_first_tile_allowance, fp4p_flip_allowance, np_f32,
+                     oracle_quantize, rel_l2, tiled_to_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -142,3 +143,79 @@ def test_prefill_fp4pv_single_tile_items():
     got, want = np.concatenate(got), np.concatenate(want)
     assert np.isfinite(got).all()
     assert rel_l2(got, want) <= O_REL_L2, rel_l2(got, want)
+
+
+def _amax_bf16_chunks(t):
+    m = 0
+    for b in range(t.shape[0]):
+        bits = t[b].contiguous().view(torch.int16).cpu().numpy().view(np.uint16) & 0x7FFF
+        m = max(m, int(bits.max()))
+    return np.uint32(m << 16).view(np.float32)
+
+
+def _fp4pv_fullsize(cfg, heads, seed=0):
+    """The benchmark workload at full size, as bench.py's PV ablation runs
+    it: Vᵀ codes and scales of the sampled KV heads bit for bit, and sampled
+    query rows (first rows, tile boundaries, the last rows, random ones)
+    emulated one by one.  Rows below 128 see only the first key tile, where
+    one FP4 decision can move a short row's O; they get the flip allowance."""
+    import flashattention_mpfa_quantize_gb300 as mp
+    dev = torch.device("cuda:0")
+    Q, K, V = mi.prefill_inputs(cfg, dev, seed)
+    qz = mp.quantize_qkv(Q, K, None, compensate=True, T=2)
+    vt = mp.quantize_v_fp4(V)
+    o, lse = mp.prefill_fp4pv(qz, vt, causal=cfg.causal)
+    torch.cuda.synchronize()
+    assert mp.get_error() == 0
+    B, N, Hq, Hkv, g = cfg.B, cfg.N, cfg.Hq, cfg.Hkv, cfg.Hq // cfg.Hkv
+    s_q, s_k = qz["q"]["scale"].item(), qz["k"]["scale"].item()
+    s_v = orc.tensor_scale(_amax_bf16_chunks(V), 2688.0)
+    assert vt["scale"].item() == s_v
+    rng = np.random.default_rng(7)
+    rows = np.array(sorted({0, 1, 2, 63, 100, 127, 128, 129, 255, 256, N // 2, N - 129,
+                            N - 128, N - 1} | set(rng.integers(0, N, 6).tolist())), np.int64)
+    cs = orc.score_scale_log2(np.float32(s_q), np.float32(s_k))
+    nt = N // 128
+    for (b, h) in heads:
+        hk = h // g
+        vc, vs = orc.nvfp4_quantize(np.ascontiguousarray(np_f32(V[b, :, hk, :]).T), np.float32(s_v))
+        np.testing.assert_array_equal(vt["codes"][b, hk].cpu().numpy(), vc)
+        t0 = (b * Hkv + hk) * nt * 1024
+        got_s = tiled_to_rows(vt["scales"][t0:t0 + nt * 1024].cpu().numpy(), nt * 128)
+        np.testing.assert_array_equal(got_s.reshape(nt, 128, 8).transpose(1, 0, 2).reshape(128, -1),
+                                      vs)
+        mb, xp = orc.block_means(np_f32(Q[b, :, h, :]), 128)
+        qc, qs = orc.nvfp4_quantize(xp, np.float32(s_q))
+        tc, ts = orc.rank_one_terms(mb, np.float32(s_q), 2)
+        np.testing.assert_array_equal(qz["q"]["codes"][b, h].cpu().numpy(), qc)
+        kc, ks = orc.nvfp4_quantize(np_f32(K[b, :, hk, :]), np.float32(s_k))
+        q = orc.nvfp4_dequant(qc, qs)
+        qadd = np.repeat(sum(orc.nvfp4_dequant(np.ascontiguousarray(tc[:, t]),
+                                               np.ascontiguousarray(ts[:, t])) for t in range(2)),
+                         128, axis=0)
+        k = orc.nvfp4_dequant(kc, ks)
+        v = orc.nvfp4_dequant(vc, vs).T
+        oe, le = orc.attn_online(q, qadd, k, v, score_scale=cs, out_scale=float(s_v),
+                                 causal=cfg.causal, round_p=2, rows=rows)
+        want = orc.bf16_bits_to_float(orc.bf16_round(oe))
+        got = np_f32(o[b, rows, h, :])
+        lg = lse[b, h, rows].cpu().numpy()
+        allow = np.zeros_like(want)
+        allow_lse = np.zeros(len(rows))
+        first = rows < 128
+        a_o, a_l = fp4p_first_tile_allowance((q + qadd)[rows[first]], k, v * np.float64(s_v),
+                                             cs, rows[first])
+        allow[first], allow_lse[first] = a_o, a_l
+        assert np.isfinite(got).all()
+        err = np.abs(got - want)
+        assert (err <= O_MAX_ABS + allow).all(), (err.max(), (err - allow).max())
+        assert (np.abs(lg - le) <= LSE_ABS + allow_lse).all(), np.abs(lg - le).max()
+        assert rel_l2(got, want) <= O_REL_L2, rel_l2(got, want)
+
+
+def test_fp4pv_fullsize_llama8b_n16k_causal():
+    _fp4pv_fullsize(mi.PREFILL["llama8b_n16k_causal"], [(0, 0), (0, 31)])
+
+
+def test_fp4pv_fullsize_qwen14b_n128k_causal():
+    _fp4pv_fullsize(mi.PREFILL["qwen14b_n128k_causal"], [(0, 0), (0, 39)])
