@@ -82,3 +82,27 @@ def test_bench_traffic_table_is_keyed_by_kernel_and_workload():
     without a row gives None."""
     assert bench.measured_traffic("prefill_kernel", "no_such_workload") is None
     assert bench.prefill_algo_bytes(bench.mi.PREFILL["llama8b_n16k_causal"]) == 200867840
+
+
+def test_pv_fp4_option_needs_prefill_only():
+    """--pv fp4 times the ablation kernel alone: without --only prefill the
+    argument check rejects it before any GPU work."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--pv", "fp4"],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 2
+    assert "--only prefill" in r.stderr
+
+
+def test_fp4_roofline_is_all_fp4():
+    """The ablation's roofline puts both products at the FP4 rate: 6 x the
+    bf16 peak, against 3 x for the method's FP4 QK + FP8 PV mix."""
+    import mpfa_inputs as mi
+    cfg = mi.PREFILL["llama8b_n16k_causal"]
+    peaks = {"bf16": 1000.0, "source": "test"}
+    r8 = bench.prefill_roofline(cfg, 1.0, peaks)
+    r4 = bench.prefill_roofline(cfg, 1.0, peaks, pv4=True)
+    assert abs(r8["peak"] - 3000.0) < 1e-6 and abs(r4["peak"] - 6000.0) < 1e-6
+    assert r4["traffic"] is None and r4["kernel"].startswith("prefill_kernel<true>")
